@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE FFN layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--extras]
+
+Default workload: one full-size decode layer (T=1 token, d=2048, 512 experts + 1 shared expert,
+top-10, SwiGLU f=768, int4 group-32 weights with fp16 scales, bf16 activations, fp32 router).
+A step is one pass of the whole layer path (router + top-10 + dispatch + experts + shared
+expert + combine) for the batch, repeated over 48 distinct layers' weights so that every layer
+reads its experts cold from HBM (48 x ~29 MB per step > the 126 MB L2).  value = tokens through a
+MoE layer per second.  Runs are replicas across GPUs (one process per GPU, no data exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOP/s as % of B300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_init(gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.dev)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": float(np.median(loaded)) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+def traffic_from_profiles(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if the kernel source is unchanged."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    ent = d.get(f"{kernel}@{workload}")
+    if not ent:
+        return None
+    with open(os.path.join(ROOT, "routed_expert_ffn_07_b300", "csrc", source), "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+    return ent["dram_bytes_per_launch"] if ent.get("source_sha16") == sha else None
+
+
+def cpu_baseline_decode(wl, budget_s=12.0, max_layers=48):
+    """The fp64 oracle on host cores: the same decode layer (route + 10 experts + shared) for one
+    token, cycling layers, until the time budget is spent.  Expert bytes are generated outside
+    the timed part."""
+    import oracle
+    from routed_expert_ffn_07_b300 import inputs
+    from routed_expert_ffn_07_b300.workloads import host_experts
+
+    x = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)
+    tokens = 0
+    spent = 0.0
+    layers = 0
+    for l in range(max_layers):
+        Wr = inputs.gen_router(wl.seed, l, wl.E, wl.d)
+        _, idx, _, _ = oracle.route(x, Wr, None, wl.K, nthreads=1)
+        ex = host_experts(wl, l, sorted(set(idx.ravel().tolist())) + [wl.E])
+        sh = ex.pop(wl.E)
+        t0 = time.perf_counter()
+        oracle.layer(x, Wr, None, ex, wl.E, wl.K, shared=sh, nthreads=1)
+        spent += time.perf_counter() - t0
+        tokens += wl.T
+        layers += 1
+        if spent > budget_s:
+            break
+    return {"value": tokens / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{layers} decode-layer calls (T={wl.T}, one per distinct layer), fp64, single thread; "
+                      f"{spent:.1f} s of oracle time"}
+
+
+def measure_decode_layer(wl, steps, warmup, rank, world, extras):
+    import torch
+    from routed_expert_ffn_07_b300 import capi
+    from routed_expert_ffn_07_b300.workloads import alloc_and_fill, create_handle, expert_bytes
+    from routed_expert_ffn_07_b300 import inputs
+
+    L = 48
+    T, d, f = wl.T, wl.d, wl.f
+    wts = alloc_and_fill(wl, n_layers=L)
+    h = create_handle(wl, wts, max_tokens=max(T, 1), n_layers=L, prenorm=False)
+    x_np = inputs.gen_activations(wl.seed, T, d, wl.act)
+    x = torch.from_numpy(x_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    torch.cuda.synchronize()
+
+    def sweep(stream):
+        for l in range(L):
+            capi.moe_layer_forward(h, l, x, T, y, stream)
+
+    # graph of one step (48 layer calls)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sweep(s.cuda_stream)  # warm the kernels outside capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        sweep(torch.cuda.current_stream().cuda_stream)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(steps):
+        g.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    t_ms = ev0.elapsed_time(ev1)
+    t_max = allreduce_max(t_ms, world)
+    assert capi.moe_get_device_status(h) == 0
+    counts = capi.moe_get_active_counts(h, L)
+
+    # per-stage timing pass: same 48-layer step captured with event records between the kernels
+    capi.moe_timing_enable(h, L)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        sweep(torch.cuda.current_stream().cuda_stream)
+    stage = []
+    for _ in range(max(3, min(steps, 20))):
+        g2.replay()
+        stage.append(capi.moe_timing_read(h, L, torch.cuda.current_stream().cuda_stream))
+    stage = np.concatenate(stage)  # [reps*L, 3]
+    capi.moe_timing_enable(h, 0)
+
+    gu_bytes = 2 * f * d // 2 + 2 * f * (d // 32) * 2
+    dn_bytes = d * f // 2 + d * (f // 32) * 2
+    slots = counts.astype(np.float64) + (1 if wl.shared else 0)
+    act_b = T * d * 2
+    bytes_gu = float(np.mean(slots)) * gu_bytes + act_b           # per launch of the gate/up kernel
+    bytes_layer = float(np.mean(slots)) * expert_bytes(d, f) + 2 * act_b
+    ms_route, ms_gu, ms_dn = (float(v) for v in stage.mean(axis=0))
+    pk, src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    ms_step = t_max / steps
+    layer_us = ms_step * 1e3 / L
+    res = {
+        "value": world * steps * L * T / (t_max / 1e3),
+        "ms_per_step": ms_step,
+        "clocks": ck,
+        "counts": counts,
+        "roofline": {"bound": "hbm", "achieved": bytes_gu / (ms_gu * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": bytes_gu / (ms_gu * 1e-3) / 1e9 / hbm,
+                     "traffic": traffic_from_profiles("gu_int4_kernel", "experts_gemv.cu", "decode_T1"),
+                     "kernel": "gu_int4_kernel (expert gate/up GEMV + SwiGLU)",
+                     "algorithmic_bytes_per_launch": bytes_gu,
+                     "avg_launch_us": ms_gu * 1e3, "peak_source": f"{src} hbm_gbs (copy bandwidth)"},
+        "layer": {"us_per_layer": layer_us, "algorithmic_bytes": bytes_layer,
+                  "hbm_frac_of_" + src: bytes_layer / (layer_us * 1e-6) / 1e9 / hbm,
+                  "stage_us": {"route": ms_route * 1e3, "gate_up": ms_gu * 1e3, "down_combine": ms_dn * 1e3},
+                  "distinct_experts_per_layer": float(np.mean(counts))},
+        "gpu_launches": steps * L * 3,
+    }
+    # end to end through the host-buffer entry point
+    xh = torch.from_numpy(x_np.view(np.int16).copy()).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    st = torch.cuda.current_stream().cuda_stream
+    for i in range(warmup):
+        capi.moe_layer_forward_host(h, i % L, xh, T, yh, st)
+    n_e2e = max(steps, 48)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        capi.moe_layer_forward_host(h, i % L, xh, T, yh, st)
+    te = time.perf_counter() - t0
+    te = allreduce_max(te, world)
+    res["e2e"] = {"value": world * n_e2e * T / te, "unit": "tokens/s", "h2d_bytes_per_step": T * d * 2,
+                  "d2h_bytes_per_step": T * d * 2,
+                  "step": "one moe_layer_forward_host call (pinned host x in, host y out, synchronised)"}
+    capi.moe_destroy(h)
+    del wts, g, g2
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    rank, world, local = dist_init(args.gpus)
+    import torch
+    from routed_expert_ffn_07_b300 import build
+    if rank == 0 and not os.path.exists(os.path.join(ROOT, "routed_expert_ffn_07_b300", "libmoe_b300.so")):
+        build.build()
+    barrier(world)
+    from routed_expert_ffn_07_b300.workloads import WORKLOADS
+    wl = WORKLOADS[2]
+    res = measure_decode_layer(wl, args.steps, args.warmup, rank, world, args.extras)
+    line = {
+        "metric": METRIC,
+        "value": res["value"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4 weights (fp16 group scales) x bf16 activations, fp32 accumulate",
+        "data": "synthetic (seeded SplitMix64 generator; int4 codes uniform, scales U(0.005,0.02), x ~ N(0,1) bf16, router ~ N(0,0.02) fp32)",
+        "config": {"workload": wl.name, "tokens_per_layer_call": wl.T, "layer_calls_per_step": 48,
+                   "distinct_layers_cycled": 48,
+                   "l2": "inputs larger than L2: each step reads 48 distinct layers' experts (~1.4 GB) > 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": res["roofline"],
+        "layer": res["layer"],
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step a bounded sample (one decode-layer call)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    from routed_expert_ffn_07_b300 import inputs
+    from routed_expert_ffn_07_b300.workloads import WORKLOADS, host_experts
+    wl = WORKLOADS[2]
+    x = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)
+    n = args.warmup + args.steps
+    prepared = []
+    for i in range(n):
+        l = i % 48
+        Wr = inputs.gen_router(wl.seed, l, wl.E, wl.d)
+        _, idx, _, _ = oracle.route(x, Wr, None, wl.K, nthreads=1)
+        ex = host_experts(wl, l, sorted(set(idx.ravel().tolist())) + [wl.E])
+        prepared.append((Wr, ex))
+    for i in range(args.warmup):
+        Wr, ex = prepared[i]
+        ex = dict(ex)
+        sh = ex.pop(wl.E)
+        oracle.layer(x, Wr, None, ex, wl.E, wl.K, shared=sh, nthreads=1)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, n):
+        Wr, ex = prepared[i]
+        ex = dict(ex)
+        sh = ex.pop(wl.E)
+        oracle.layer(x, Wr, None, ex, wl.E, wl.K, shared=sh, nthreads=1)
+    t = time.perf_counter() - t0
+    v = args.steps * wl.T / t
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same generator and workload as the CUDA arm)",
+            "config": {"workload": WORKLOADS[2].name, "tokens_per_layer_call": wl.T,
+                       "step": "one decode-layer call of the fp64 CPU oracle (router + 10 experts + shared expert), layers cycled",
+                       "parallelism": "host, 1 thread"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} timed decode-layer calls (T=1) after {args.warmup} warm-up calls"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--extras", action="store_true", help="also measure the stack and prefill workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * Routed mixture-of-experts FFN layer for one B300 (sm_103a): C ABI.
+ *
+ * The layer is the one the Strata engine pages describe for Qwen3.8-Flash-Next:
+ *   - 48 layers, each with 512 experts and a router that picks 10 of them per token, plus a
+ *     shared expert that every token uses -- 'Strata はなぜ少ない VRAM でも速いのか'
+ *     (modeldock.net), section '問題：1,250 億パラメータと 12 GB';
+ *   - per layer the router runs, the chosen experts compute, the results are summed and the next
+ *     layer starts, the 48-layer step replayed as one CUDA graph -- same page, section
+ *     '1 トークン、三者の分担';
+ *   - a verify pass runs 1 new + up to 3 drafted tokens through all 48 layers at once -- same
+ *     page, section '予測してから検証する';
+ *   - prefill runs chunks of thousands of tokens that reach almost every expert -- same page,
+ *     section '長いプロンプトを読む：大きなまとまりで流す'.
+ * The pages fix no formula, activation or number format.  This library computes:
+ *   logits[t,e] = sum_j x[t,j] * router_w[e,j] (+ router_b[e])              (fp32)
+ *   p = softmax over all E logits; keep the K largest logits (ties: lower expert index first);
+ *   w[t,k] = p[idx[t,k]] / sum_k' p[idx[t,k']]                                (renormalised)
+ *   FFN_e(x) = W_down,e ( silu(W_gate,e x) * (W_up,e x) ),  silu(z) = z / (1 + exp(-z))
+ *   y[t] = sum_{k=0..K-1} w[t,k] FFN_{idx[t,k]}(x[t])  (+ FFN_shared(x[t]) with weight 1),
+ *   summed in fp32 in ascending k with the shared expert last, rounded once to the output type.
+ *
+ * Conventions (all entry points):
+ *   - Pointers are DEVICE pointers owned by the caller unless a parameter says "host".
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.  Every
+ *     call is asynchronous on that stream unless stated otherwise; none synchronises it except
+ *     moe_get_device_status and the *_host entry points.
+ *   - Arguments are validated before anything is launched; on error nothing is launched and an
+ *     error status is returned.  Status codes are returned, never printed.
+ *   - The library allocates device memory only in moe_create (workspace sized for max_tokens) and
+ *     frees it only in moe_destroy.  Weights are never copied: moe_set_layer stores pointers.
+ *   - A handle is not thread-safe, and calls made with one handle on different streams that
+ *     overlap in time race on its workspace.
+ *
+ * Weight storage (our definition; the pages give none):
+ *   MOE_W_INT4_G32: a matrix [rows x K] is stored row-major, two 4-bit two's-complement values per
+ *     byte, the even column in the low nibble; 32 consecutive columns (16 bytes) form a group
+ *     with one fp16 scale; value = q * scale, q in [-8, 7].  Scales: fp16 [rows x K/32].
+ *   MOE_W_F32: the same matrices as plain fp32 [rows x K], no scales.
+ *   Routed experts of a layer are stacked by expert index:
+ *     gu_q  [E][2f][d/2] bytes   (rows 0..f-1 = gate, rows f..2f-1 = up), gu_s [E][2f][d/32] fp16
+ *     dn_q  [E][d][f/2] bytes,                                             dn_s [E][d][f/32] fp16
+ *   (fp32: gu [E][2f][d], dn [E][d][f]).  The shared expert uses the same per-expert layout.
+ *   Router: router_w fp32 [E][d], router_b fp32 [E] or NULL.
+ *   Every base pointer must be 16-byte aligned.  INT4 needs d % 128 == 0 and f % 128 == 0.
+ * Activations: [T][d] row-major, bf16 (MOE_ACT_BF16) or fp32 (MOE_ACT_F32).
+ */
+#ifndef ROUTED_MOE_B300_MOE_H
+#define ROUTED_MOE_B300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx* moe_handle;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, T > max_tokens, ...        */
+  MOE_ERR_UNSUPPORTED = 2, /* a shape or format this build does not implement                 */
+  MOE_ERR_OOM = 3,         /* workspace allocation failed in moe_create                        */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed (including earlier asynchronous errors) */
+  MOE_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up (reported by get_device_status) */
+  MOE_ERR_NOT_SET = 6,     /* the layer's weights were never registered with moe_set_layer      */
+  MOE_ERR_DEVICE = 7       /* a device-side check failed (reported by get_device_status)        */
+} moe_status;
+
+enum { MOE_ACT_F32 = 0, MOE_ACT_BF16 = 1 };
+enum { MOE_W_F32 = 0, MOE_W_INT4_G32 = 1 };
+
+typedef struct {
+  int d;          /* hidden size                                                    */
+  int f;          /* expert FFN width                                               */
+  int n_experts;  /* E, routed experts per layer (<= 1024)                          */
+  int top_k;      /* K, experts kept per token (1 <= K <= min(E, 32))               */
+  int n_layers;   /* L                                                              */
+  int max_tokens; /* largest T any call will pass (sizes the workspace)             */
+  int has_shared; /* 1: every layer has a shared expert with weight 1               */
+  int prenorm;    /* stack only: x <- x + MoE(RMSNorm(x)), RMSNorm without weight   */
+  float norm_eps; /* RMSNorm epsilon                                                */
+  int wfmt;       /* MOE_W_INT4_G32 or MOE_W_F32                                    */
+  int act;        /* MOE_ACT_BF16 or MOE_ACT_F32                                    */
+} moe_config;
+
+typedef struct {
+  const float* router_w; /* fp32 [E][d]                          */
+  const float* router_b; /* fp32 [E] or NULL                     */
+  const void* gu_q;      /* routed experts, gate/up (see above)  */
+  const void* gu_s;
+  const void* dn_q;      /* routed experts, down                 */
+  const void* dn_s;
+  const void* sh_gu_q;   /* shared expert (NULL if !has_shared)  */
+  const void* sh_gu_s;
+  const void* sh_dn_q;
+  const void* sh_dn_s;
+} moe_layer_weights;
+
+/* Create a handle on the current CUDA device and allocate its workspace for cfg->max_tokens.
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for bad configs, MOE_ERR_OOM if the
+ * workspace cannot be allocated.  *out is set only on success. */
+moe_status moe_create(const moe_config* cfg, moe_handle* out);
+
+/* Register the weights of layer `layer` (0 <= layer < n_layers).  Stores the pointers only;
+ * the memory must stay valid while the handle uses it.  Pointers are checked for NULL (scales
+ * only for INT4, shared planes only with has_shared) and 16-byte alignment. */
+moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w);
+
+/* Router + top-K + dispatch of one layer for T tokens (1 <= T <= max_tokens):
+ *   topk_idx [T*K] int32, slot order = selection order (largest logit first, ties lower index);
+ *   topk_w [T*K] fp32 renormalised weights;
+ *   expert_offs [E+1] int32: assignments of expert e are perm[offs[e] .. offs[e+1]);
+ *   perm [T*K] int32: assignment ids a = t*K + k stably sorted by expert (ascending t per expert).
+ * Any of the four outputs may be NULL (not written).  x is [T][d] of the configured act type. */
+moe_status moe_route(moe_handle h, int layer, const void* x, int T, int32_t* topk_idx, float* topk_w,
+                     int32_t* expert_offs, int32_t* perm, void* stream);
+
+/* y = MoE_layer(x) for T tokens.  x, y: [T][d] of the configured act type; y must not overlap x.
+ * T <= 16 runs the split-K GEMV path; larger T runs the grouped tensor-core path. */
+moe_status moe_layer_forward(moe_handle h, int layer, const void* x, int T, void* y, void* stream);
+
+/* All n_layers layers in order, in place: x <- x + MoE_l(N(x)) with N = RMSNorm (no weight,
+ * norm_eps) if cfg.prenorm, else the identity; the residual is added in fp32 and rounded once.
+ * Replays one CUDA graph per T (captured at the first call with that T; capture happens on an
+ * internal stream, so the first call for a T must not be made while `stream` is being captured).
+ * trace: NULL, or a device buffer of n_layers*2*T*d activations receiving, per layer l, the
+ * layer input x_l and the normalised input N(x_l) (both in the act type); with a trace the
+ * layers are launched directly instead of through the graph. */
+moe_status moe_stack_forward(moe_handle h, void* x_inout, int T, void* trace, void* stream);
+
+/* End-to-end form of moe_layer_forward for HOST buffers: copies x_host to the device, runs the
+ * layer, copies the result to y_host and synchronises `stream`.  x_host / y_host should be
+ * page-locked for the copies to be asynchronous.  Blocks the calling thread until done. */
+moe_status moe_layer_forward_host(moe_handle h, int layer, const void* x_host, int T, void* y_host,
+                                  void* stream);
+
+/* Host copy of the per-layer count of distinct routed experts selected by the most recent
+ * route of each layer (n_layers int32 values).  Synchronises `stream`. */
+moe_status moe_get_active_counts(moe_handle h, int32_t* counts_host, void* stream);
+
+/* Synchronises `stream` and reports pending errors: MOE_ERR_CUDA for a CUDA error,
+ * MOE_ERR_DEVICE / MOE_ERR_TIMEOUT if a kernel recorded a failed check or an exhausted wait in
+ * the handle's status word (which is then cleared). */
+moe_status moe_get_device_status(moe_handle h, void* stream);
+
+/* Free the workspace and any captured graphs.  Synchronises the device first. */
+moe_status moe_destroy(moe_handle h);
+
+/* Stage timing (tracing).  moe_timing_enable(h, n) creates 4*n CUDA events; afterwards every
+ * layer enqueued by moe_layer_forward / moe_stack_forward (also inside a graph captured after
+ * this call) records events before routing, after routing, after the first expert kernel and
+ * after the combine, until n layer records are used.  moe_timing_read synchronises `stream`
+ * and writes, for each of the *n_records recorded layers, 3 durations in milliseconds
+ * (route, experts stage A = gate/up, experts stage B = down + combine) into ms[3*i .. 3*i+2]
+ * (capacity: max_records records); moe_timing_rewind restarts recording at record 0 (events of
+ * a captured graph keep their record indices).  moe_timing_enable(h, 0) frees the events. */
+moe_status moe_timing_enable(moe_handle h, int n_records);
+moe_status moe_timing_rewind(moe_handle h);
+moe_status moe_timing_read(moe_handle h, float* ms, int max_records, int* n_records, void* stream);
+
+const char* moe_status_str(moe_status s);
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ROUTED_MOE_B300_MOE_H */

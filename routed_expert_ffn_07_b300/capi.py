@@ -1,0 +1,185 @@
+"""Routed MoE FFN layer on one B300: thin Python binding of the C ABI in include/moe.h (and moe_gen.h).
+
+Every function here only marshals arguments (torch tensors or integer device pointers, streams)
+into the C entry points of ``libmoe_b300.so``; all computation runs in the library's CUDA kernels.
+Importing this package fails loudly if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_NOT_SET", 7: "MOE_ERR_DEVICE"}
+MOE_ACT_F32, MOE_ACT_BF16 = 0, 1
+MOE_W_F32, MOE_W_INT4_G32 = 0, 1
+SMALL_T = 16  # T <= SMALL_T runs the split-K GEMV path
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("f", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("n_layers", ctypes.c_int), ("max_tokens", ctypes.c_int), ("has_shared", ctypes.c_int),
+                ("prenorm", ctypes.c_int), ("norm_eps", ctypes.c_float), ("wfmt", ctypes.c_int),
+                ("act", ctypes.c_int)]
+
+
+class moe_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("router_w", "router_b", "gu_q", "gu_s", "dn_q", "dn_s",
+                                                "sh_gu_q", "sh_gu_s", "sh_dn_q", "sh_dn_s")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library not built: {LIB_PATH} is missing "
+                          "(run `python -m routed_expert_ffn_07_b300.build`)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, ci, i32p = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    sig = {
+        "moe_create": ([ctypes.POINTER(moe_config), ctypes.POINTER(vp)], ci),
+        "moe_set_layer": ([vp, ci, ctypes.POINTER(moe_layer_weights)], ci),
+        "moe_route": ([vp, ci, vp, ci, i32p, vp, i32p, i32p, vp], ci),
+        "moe_layer_forward": ([vp, ci, vp, ci, vp, vp], ci),
+        "moe_stack_forward": ([vp, vp, ci, vp, vp], ci),
+        "moe_layer_forward_host": ([vp, ci, vp, ci, vp, vp], ci),
+        "moe_get_active_counts": ([vp, i32p, vp], ci),
+        "moe_get_device_status": ([vp, vp], ci),
+        "moe_destroy": ([vp], ci),
+        "moe_timing_enable": ([vp, ci], ci),
+        "moe_timing_rewind": ([vp], ci),
+        "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
+        "moe_status_str": ([ci], ctypes.c_char_p),
+        "moe_version": ([], ci),
+        "moe_gen_int4_planes": ([vp, ctypes.c_uint64, ci, ci, ci, ci, ctypes.c_size_t, vp], ci),
+        "moe_gen_scale_planes": ([vp, ctypes.c_uint64, ci, ci, ci, ci, ctypes.c_size_t, vp], ci),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
+lib = _load()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take a pointer of {type(x)}")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream  # torch.cuda.Stream
+
+
+def _check(fn, st):
+    if st != MOE_OK:
+        raise MoeError(fn, st)
+
+
+def moe_create(d, f, n_experts, top_k, n_layers, max_tokens, has_shared=True, prenorm=False, norm_eps=1e-6,
+               wfmt=MOE_W_INT4_G32, act=MOE_ACT_BF16):
+    cfg = moe_config(d, f, n_experts, top_k, n_layers, max_tokens, int(has_shared), int(prenorm),
+                     float(norm_eps), wfmt, act)
+    h = ctypes.c_void_p()
+    _check("moe_create", lib.moe_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h.value
+
+
+def moe_set_layer(h, layer, router_w, gu_q, gu_s, dn_q, dn_s, router_b=None, sh_gu_q=None, sh_gu_s=None,
+                  sh_dn_q=None, sh_dn_s=None):
+    w = moe_layer_weights(*[_ptr(p) for p in (router_w, router_b, gu_q, gu_s, dn_q, dn_s,
+                                              sh_gu_q, sh_gu_s, sh_dn_q, sh_dn_s)])
+    _check("moe_set_layer", lib.moe_set_layer(h, layer, ctypes.byref(w)))
+
+
+def moe_route(h, layer, x, T, topk_idx=None, topk_w=None, expert_offs=None, perm=None, stream=None):
+    _check("moe_route", lib.moe_route(h, layer, _ptr(x), T, _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offs),
+                                      _ptr(perm), _stream(stream)))
+
+
+def moe_layer_forward(h, layer, x, T, y, stream=None):
+    _check("moe_layer_forward", lib.moe_layer_forward(h, layer, _ptr(x), T, _ptr(y), _stream(stream)))
+
+
+def moe_stack_forward(h, x_inout, T, trace=None, stream=None):
+    _check("moe_stack_forward", lib.moe_stack_forward(h, _ptr(x_inout), T, _ptr(trace), _stream(stream)))
+
+
+def moe_layer_forward_host(h, layer, x_host, T, y_host, stream=None):
+    _check("moe_layer_forward_host",
+           lib.moe_layer_forward_host(h, layer, _ptr(x_host), T, _ptr(y_host), _stream(stream)))
+
+
+def moe_get_active_counts(h, n_layers, stream=None):
+    import numpy as np
+    out = np.zeros(n_layers, dtype=np.int32)
+    _check("moe_get_active_counts", lib.moe_get_active_counts(h, out.ctypes.data, _stream(stream)))
+    return out
+
+
+def moe_get_device_status(h, stream=None):
+    return lib.moe_get_device_status(h, _stream(stream))
+
+
+def moe_destroy(h):
+    _check("moe_destroy", lib.moe_destroy(h))
+
+
+def moe_timing_enable(h, n_records):
+    _check("moe_timing_enable", lib.moe_timing_enable(h, n_records))
+
+
+def moe_timing_rewind(h):
+    _check("moe_timing_rewind", lib.moe_timing_rewind(h))
+
+
+def moe_timing_read(h, max_records, stream=None):
+    """Returns a float32 array [n_records, 3] of (route, experts A, experts B) milliseconds."""
+    import numpy as np
+    ms = np.zeros((max(max_records, 1), 3), dtype=np.float32)
+    n = ctypes.c_int(0)
+    _check("moe_timing_read", lib.moe_timing_read(h, ms.ctypes.data, max_records, ctypes.byref(n), _stream(stream)))
+    return ms[: n.value].copy()
+
+
+def moe_status_str(s):
+    return lib.moe_status_str(s).decode()
+
+
+def moe_version():
+    return lib.moe_version()
+
+
+def moe_gen_int4_planes(dst, seed, layer, tensor, expert0, n_experts, bytes_per_expert, stream=None):
+    rc = lib.moe_gen_int4_planes(_ptr(dst), seed, layer, tensor, expert0, n_experts, bytes_per_expert,
+                                 _stream(stream))
+    if rc:
+        raise RuntimeError(f"moe_gen_int4_planes failed ({rc})")
+
+
+def moe_gen_scale_planes(dst, seed, layer, tensor, expert0, n_experts, scales_per_expert, stream=None):
+    rc = lib.moe_gen_scale_planes(_ptr(dst), seed, layer, tensor, expert0, n_experts, scales_per_expert,
+                                  _stream(stream))
+    if rc:
+        raise RuntimeError(f"moe_gen_scale_planes failed ({rc})")

@@ -1,0 +1,110 @@
+// Shared device helpers and launch-argument structs of the routed MoE library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kActF32 = 0;
+constexpr int kActBf16 = 1;
+constexpr int kWF32 = 0;
+constexpr int kWInt4 = 1;
+
+constexpr int kSmallT = 16;   // T <= kSmallT: fused router + split-K GEMV experts
+constexpr int kMaxK = 32;
+constexpr int kMaxE = 1024;
+constexpr int kRouterWarps = 8;
+
+// bits of the device status word
+constexpr unsigned kStatusBadIndex = 1u;
+constexpr unsigned kStatusTimeout = 2u;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float load_act(const void* p, int act, size_t i) {
+  if (act == kActBf16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  return static_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ void store_act(void* p, int act, size_t i, float v) {
+  if (act == kActBf16)
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float*>(p)[i] = v;
+}
+
+// Value of v after rounding to the activation type.
+__device__ __forceinline__ float round_act(int act, float v) {
+  return act == kActBf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------------ launch arguments
+struct RouteArgs {
+  const void* x;     // [T][d] activations (layer input)
+  int act, T, d, E, K;
+  const float* Wr;   // [E][d]
+  const float* bias; // [E] or null
+  int prenorm;       // 1: route / compute on RMSNorm(x) rounded to the act type
+  float eps;
+  void* xnorm;       // [T][d] receives RMSNorm(x) when prenorm (written by block 0)
+  float* logits;     // [T][E]
+  int32_t* idx;      // [T][K]
+  float* w;          // [T][K]
+  int32_t* counts;   // [E]
+  int32_t* offs;     // [E+1]
+  int32_t* perm;     // [T*K]
+  int32_t* active;   // [E] distinct experts, ascending
+  int32_t* n_active; // [1]
+  int32_t* stat;     // [1] or null: receives n_active (per-layer statistics)
+  int32_t* blockhist;// [nblocks][E] (large-T dispatch)
+  unsigned* ticket;  // last-block-done counter (zero between launches)
+  unsigned* status;  // device status word
+};
+
+struct ExpertArgs {
+  int T, d, f, E, K, act, has_shared;
+  const void* x;          // [T][d] expert input (normalised input in the stack)
+  const void* gu_q;       // [E][2f][..] routed gate/up
+  const __half* gu_s;
+  const void* dn_q;       // [E][d][..] routed down
+  const __half* dn_s;
+  const void* sh_gu_q;
+  const __half* sh_gu_s;
+  const void* sh_dn_q;
+  const __half* sh_dn_s;
+  const int32_t* offs;
+  const int32_t* perm;
+  const int32_t* active;
+  const int32_t* n_active;
+  const float* topk_w;    // [T][K]
+  float* h;               // [(T*K + T)][f] fp32 (GEMV path)
+  void* y;                // [T][d]
+  const void* resid;      // [T][d] or null: y = resid + moe
+  unsigned* status;
+};
+
+}  // namespace moe

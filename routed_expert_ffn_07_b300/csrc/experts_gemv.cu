@@ -1,0 +1,465 @@
+// Decode / verify experts: split-K GEMV over the distinct experts the batch routed to (sm_103a).
+//
+// A decode step touches only the experts its tokens routed to, so its cost is the bytes of
+// those experts ('Strata はなぜ少ない VRAM でも速いのか' (modeldock.net), section
+// '1 トークン、三者の分担': the step is bound by how fast expert bytes stream; section
+// '予測してから検証する': verifying several tokens costs only the extra experts they route to).
+// Every distinct expert is read from HBM exactly once per layer, whatever the number of tokens
+// routed to it, and all its tokens are served from that one read.
+//
+// Kernels (one launch each):
+//   gu_*  : work item = (slot, 16 consecutive f indices); slot = a distinct routed expert or the
+//           shared expert.  Each warp owns 2 f indices (gate row + up row each), each lane a fixed
+//           set of 32-column groups, so one warp load instruction covers 512 contiguous bytes.
+//           h = silu(gate . x) * (up . x) in fp32 -> workspace h[assignment][f].
+//   dn_*  : block = 16 output rows; its warps split the slots; each lane owns one 32-column
+//           group of h and reuses it for the 16 rows.  Per-assignment results land in shared
+//           memory and are combined in fixed order (ascending k, shared expert last), plus the
+//           optional residual, and rounded once to the activation type.
+//
+// int4 dot product without per-element integer->float conversion: a code o = q + 8 (offset
+// binary, 0..15) placed in mantissa bits 16..19 under exponent 2^-1 is the fp32 value
+// v = 0.5 + o/256 (one byte permute per element).  With x' = 256 x,
+//   sum_k q_k x_k = sum_k v_k x'_k - 136 sum_k x_k,
+// the second term precomputed per (token, group).  v_k x'_k is exact in fp32 for bf16 x; the
+// accumulation is fp32; the group scale multiplies the group sum once.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kGuWarps = 8;             // warps per block of the gate/up kernel
+constexpr int kGuFPerWarp = 2;          // f indices per warp
+constexpr int kGuFPerItem = kGuWarps * kGuFPerWarp;  // 16
+constexpr int kDnRows = 16;             // output rows per block of the down kernel
+constexpr int kDnWarps = 16;
+constexpr int kTB = 2;                  // tokens per register batch
+
+// ------------------------------------------------------------------ slot -> (expert, tokens)
+struct SlotInfo {
+  int n;           // tokens routed to the slot
+  bool shared;
+  int e;
+};
+
+// Token list of slot s: tok[i] = token index, asg[i] = assignment row (t*K+k, or T*K+t for shared).
+__device__ __forceinline__ SlotInfo slot_tokens(const ExpertArgs& a, int s, int n_act, int* tok, int* asg) {
+  SlotInfo si;
+  if (s < n_act) {
+    const int e = a.active[s];
+    const int b = a.offs[e], n = a.offs[e + 1] - b;
+    for (int i = 0; i < n; ++i) {
+      const int as = a.perm[b + i];
+      tok[i] = as / a.K;
+      asg[i] = as;
+    }
+    si.n = n;
+    si.shared = false;
+    si.e = e;
+  } else {
+    for (int i = 0; i < a.T; ++i) {
+      tok[i] = i;
+      asg[i] = a.T * a.K + i;
+    }
+    si.n = a.T;
+    si.shared = true;
+    si.e = -1;
+  }
+  return si;
+}
+
+__device__ __forceinline__ float v_lo(uint32_t lo, int b) {
+  return __int_as_float(__byte_perm(lo, 0x3F000000u, 0x7054u | (b << 8)));
+}
+
+// ------------------------------------------------------------------ gate/up, int4
+// Shared memory: x' [T][m4=0..7][G][4] (x * 256, group-interleaved), xs136 [T][G].
+template <int NG>  // 32-column groups per lane per row (d = NG * 1024 at full width)
+__global__ void __launch_bounds__(256, 2) gu_int4_kernel(ExpertArgs a) {
+  extern __shared__ float4 smem4[];
+  const int d = a.d, f = a.f, G = d / 32;
+  float4* xq = smem4;                                            // [T][8][G] float4
+  float* xs136 = reinterpret_cast<float*>(smem4 + (size_t)a.T * 8 * G);  // [T][G]
+  __shared__ int tok_s[kSmallT], asg_s[kSmallT];
+  __shared__ int n_s, shared_s, e_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_act = *a.n_active;
+  const int n_slots = n_act + a.has_shared;
+  const int items_per_slot = f / kGuFPerItem;
+  const long long N = (long long)n_slots * items_per_slot;
+  const long long beg = N * blockIdx.x / gridDim.x, end = N * (blockIdx.x + 1) / gridDim.x;
+  int loaded = -1;
+  for (long long it = beg; it < end; ++it) {
+    const int s = (int)(it / items_per_slot), c = (int)(it % items_per_slot);
+    if (s != loaded) {
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const SlotInfo si = slot_tokens(a, s, n_act, tok_s, asg_s);
+        n_s = si.n;
+        shared_s = si.shared;
+        e_s = si.e;
+      }
+      __syncthreads();
+      const int n = n_s;
+      for (int i = threadIdx.x; i < n * d; i += blockDim.x) {
+        const int ti = i / d, k = i - ti * d;
+        const float v = load_act(a.x, a.act, (size_t)tok_s[ti] * d + k) * 256.0f;
+        const int g = k >> 5, m = k & 31;
+        reinterpret_cast<float*>(xq)[(((size_t)ti * 8 + (m >> 2)) * G + g) * 4 + (m & 3)] = v;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < n * G; i += blockDim.x) {
+        const int ti = i / G, g = i - ti * G;
+        float sx = 0.f;
+        for (int m = 0; m < 32; ++m)
+          sx += reinterpret_cast<const float*>(xq)[(((size_t)ti * 8 + (m >> 2)) * G + g) * 4 + (m & 3)];
+        xs136[i] = sx * (136.0f / 256.0f);
+      }
+      __syncthreads();
+      loaded = s;
+    }
+    const int n = n_s;
+    const uint8_t* gq;
+    const __half* gs;
+    if (shared_s) {
+      gq = static_cast<const uint8_t*>(a.sh_gu_q);
+      gs = a.sh_gu_s;
+    } else {
+      gq = static_cast<const uint8_t*>(a.gu_q) + (size_t)e_s * 2 * f * (d / 2);
+      gs = a.gu_s + (size_t)e_s * 2 * f * G;
+    }
+    const int fi0 = c * kGuFPerItem + warp * kGuFPerWarp;
+    // rows: 0,1 = gate fi0, fi0+1; 2,3 = up fi0, fi0+1
+    uint4 wq[4][NG];
+    float sc[4][NG];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = (r < 2 ? 0 : f) + fi0 + (r & 1);
+#pragma unroll
+      for (int j = 0; j < NG; ++j) {
+        const int g = lane + 32 * j;
+        if (g < G) {
+          wq[r][j] = ldg_nc_v4(gq + (size_t)row * (d / 2) + g * 16);
+          sc[r][j] = __half2float(gs[(size_t)row * G + g]);
+        } else {
+          wq[r][j] = make_uint4(0, 0, 0, 0);
+          sc[r][j] = 0.f;
+        }
+      }
+    }
+    for (int t0 = 0; t0 < n; t0 += kTB) {
+      float acc[4][kTB];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int tt = 0; tt < kTB; ++tt) acc[r][tt] = 0.f;
+#pragma unroll
+      for (int j = 0; j < NG; ++j) {
+        const int g = lane + 32 * j;
+        if (g >= G) continue;
+        float part[4][kTB];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int tt = 0; tt < kTB; ++tt) part[r][tt] = 0.f;
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          float4 xa[kTB], xb[kTB];
+#pragma unroll
+          for (int tt = 0; tt < kTB; ++tt) {
+            const int ti = (t0 + tt < n) ? t0 + tt : t0;
+            const float4* xp = xq + (size_t)ti * 8 * G + g;
+            xa[tt] = xp[(2 * wd) * G];
+            xb[tt] = xp[(2 * wd + 1) * G];
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            uint32_t w32 = wd == 0 ? wq[r][j].x : wd == 1 ? wq[r][j].y : wd == 2 ? wq[r][j].z : wq[r][j].w;
+            asm volatile("" : "+r"(w32));  // keep the dequantisation inside the token loop
+            const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
+            const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+            const float v0 = v_lo(lo, 0), v1 = v_lo(hi, 0), v2 = v_lo(lo, 1), v3 = v_lo(hi, 1);
+            const float v4 = v_lo(lo, 2), v5 = v_lo(hi, 2), v6 = v_lo(lo, 3), v7 = v_lo(hi, 3);
+#pragma unroll
+            for (int tt = 0; tt < kTB; ++tt) {
+              float p = part[r][tt];
+              p = fmaf(v0, xa[tt].x, p);
+              p = fmaf(v1, xa[tt].y, p);
+              p = fmaf(v2, xa[tt].z, p);
+              p = fmaf(v3, xa[tt].w, p);
+              p = fmaf(v4, xb[tt].x, p);
+              p = fmaf(v5, xb[tt].y, p);
+              p = fmaf(v6, xb[tt].z, p);
+              p = fmaf(v7, xb[tt].w, p);
+              part[r][tt] = p;
+            }
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < kTB; ++tt) {
+          const int ti = (t0 + tt < n) ? t0 + tt : t0;
+          const float x136 = xs136[ti * G + g];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[r][tt] = fmaf(sc[r][j], part[r][tt] - x136, acc[r][tt]);
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < kTB; ++tt) {
+        if (t0 + tt >= n) continue;
+        float gsum[2], usum[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          gsum[p] = warp_sum(acc[p][tt]);
+          usum[p] = warp_sum(acc[2 + p][tt]);
+        }
+        if (lane < 2) {
+          const float hv = silu(gsum[lane]) * usum[lane];
+          a.h[(size_t)asg_s[t0 + tt] * f + fi0 + lane] = hv;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ down + combine, int4
+// One lane per 32-column group of h (f/32 <= 32 lanes active); 16 rows per block.
+// Shared memory: P [T*K + T][16] floats.
+__global__ void __launch_bounds__(kDnWarps * 32, 1) dn_int4_kernel(ExpertArgs a) {
+  extern __shared__ float P[];
+  __shared__ int tok_s[kDnWarps][kSmallT], asg_s[kDnWarps][kSmallT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, f = a.f, G = f / 32, T = a.T, K = a.K;
+  const int j0 = blockIdx.x * kDnRows;
+  const int n_act = *a.n_active;
+  const int n_slots = n_act + a.has_shared;
+  for (int s = warp; s < n_slots; s += kDnWarps) {
+    SlotInfo si;
+    if (lane == 0) si = slot_tokens(a, s, n_act, tok_s[warp], asg_s[warp]);
+    __syncwarp();
+    si.n = __shfl_sync(0xffffffffu, si.n, 0);
+    si.e = __shfl_sync(0xffffffffu, si.e, 0);
+    si.shared = __shfl_sync(0xffffffffu, (int)si.shared, 0);
+    const uint8_t* q;
+    const __half* sp;
+    if (si.shared) {
+      q = static_cast<const uint8_t*>(a.sh_dn_q);
+      sp = a.sh_dn_s;
+    } else {
+      q = static_cast<const uint8_t*>(a.dn_q) + (size_t)si.e * d * (f / 2);
+      sp = a.dn_s + (size_t)si.e * d * G;
+    }
+    const bool on = lane < G;
+    uint4 wq[kDnRows];
+    __half sch[kDnRows];
+#pragma unroll
+    for (int r = 0; r < kDnRows; ++r) {
+      if (on) {
+        wq[r] = ldg_nc_v4(q + (size_t)(j0 + r) * (f / 2) + lane * 16);
+        sch[r] = sp[(size_t)(j0 + r) * G + lane];
+      } else {
+        wq[r] = make_uint4(0, 0, 0, 0);
+        sch[r] = __float2half(0.f);
+      }
+    }
+    for (int i = 0; i < si.n; ++i) {
+      const int as = asg_s[warp][i];
+      float part[kDnRows];
+#pragma unroll
+      for (int r = 0; r < kDnRows; ++r) part[r] = 0.f;
+      float hsum = 0.f;
+      const float4* hp = reinterpret_cast<const float4*>(a.h + (size_t)as * f + (on ? lane : 0) * 32);
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {
+        float4 xa = on ? __ldcg(hp + 2 * wd) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 xb = on ? __ldcg(hp + 2 * wd + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        hsum += ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
+        xa.x *= 256.f; xa.y *= 256.f; xa.z *= 256.f; xa.w *= 256.f;
+        xb.x *= 256.f; xb.y *= 256.f; xb.z *= 256.f; xb.w *= 256.f;
+#pragma unroll
+        for (int r = 0; r < kDnRows; ++r) {
+          uint32_t w32 = wd == 0 ? wq[r].x : wd == 1 ? wq[r].y : wd == 2 ? wq[r].z : wq[r].w;
+          asm volatile("" : "+r"(w32));  // keep the dequantisation inside the token loop
+          const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
+          const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+          float p = part[r];
+          p = fmaf(v_lo(lo, 0), xa.x, p);
+          p = fmaf(v_lo(hi, 0), xa.y, p);
+          p = fmaf(v_lo(lo, 1), xa.z, p);
+          p = fmaf(v_lo(hi, 1), xa.w, p);
+          p = fmaf(v_lo(lo, 2), xb.x, p);
+          p = fmaf(v_lo(hi, 2), xb.y, p);
+          p = fmaf(v_lo(lo, 3), xb.z, p);
+          p = fmaf(v_lo(hi, 3), xb.w, p);
+          part[r] = p;
+        }
+      }
+      const float h136 = hsum * 136.0f;
+#pragma unroll
+      for (int r = 0; r < kDnRows; ++r) {
+        const float pr = on ? __half2float(sch[r]) * (part[r] - h136) : 0.f;
+        const float o = warp_sum(pr);
+        if (lane == 0) P[(size_t)as * kDnRows + r] = o;
+      }
+    }
+  }
+  __syncthreads();
+  // fixed-order combine: ascending k, shared expert last, optional residual, one rounding
+  for (int i = threadIdx.x; i < T * kDnRows; i += blockDim.x) {
+    const int t = i / kDnRows, r = i - t * kDnRows;
+    float y = 0.f;
+    for (int k = 0; k < K; ++k) y = fmaf(a.topk_w[t * K + k], P[(size_t)(t * K + k) * kDnRows + r], y);
+    if (a.has_shared) y += P[(size_t)(T * K + t) * kDnRows + r];
+    const size_t o = (size_t)t * d + j0 + r;
+    if (a.resid) y = load_act(a.resid, a.act, o) + y;
+    store_act(a.y, a.act, o, y);
+  }
+}
+
+// ------------------------------------------------------------------ fp32 weights (tiny layer)
+// Same decomposition; a lane owns float4 column chunks instead of int4 groups.
+__global__ void __launch_bounds__(256) gu_f32_kernel(ExpertArgs a) {
+  extern __shared__ float xs[];  // [T][d]
+  __shared__ int tok_s[kSmallT], asg_s[kSmallT];
+  __shared__ int n_s, shared_s, e_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, f = a.f;
+  const int n_act = *a.n_active;
+  const int n_slots = n_act + a.has_shared;
+  const int items_per_slot = (f + kGuFPerItem - 1) / kGuFPerItem;
+  const long long N = (long long)n_slots * items_per_slot;
+  const long long beg = N * blockIdx.x / gridDim.x, end = N * (blockIdx.x + 1) / gridDim.x;
+  int loaded = -1;
+  for (long long it = beg; it < end; ++it) {
+    const int s = (int)(it / items_per_slot), c = (int)(it % items_per_slot);
+    if (s != loaded) {
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const SlotInfo si = slot_tokens(a, s, n_act, tok_s, asg_s);
+        n_s = si.n;
+        shared_s = si.shared;
+        e_s = si.e;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < n_s * d; i += blockDim.x)
+        xs[i] = load_act(a.x, a.act, (size_t)tok_s[i / d] * d + (i % d));
+      __syncthreads();
+      loaded = s;
+    }
+    const float* W = shared_s ? static_cast<const float*>(a.sh_gu_q)
+                              : static_cast<const float*>(a.gu_q) + (size_t)e_s * 2 * f * d;
+    for (int p = 0; p < kGuFPerWarp; ++p) {
+      const int fi = c * kGuFPerItem + warp * kGuFPerWarp + p;
+      if (fi >= f) continue;
+      for (int i = 0; i < n_s; ++i) {
+        float g = 0.f, u = 0.f;
+        for (int k4 = lane; k4 < d / 4; k4 += 32) {
+          const float4 xv = reinterpret_cast<const float4*>(xs + (size_t)i * d)[k4];
+          const float4 wg = __ldg(reinterpret_cast<const float4*>(W + (size_t)fi * d) + k4);
+          const float4 wu = __ldg(reinterpret_cast<const float4*>(W + (size_t)(f + fi) * d) + k4);
+          g = fmaf(wg.x, xv.x, fmaf(wg.y, xv.y, fmaf(wg.z, xv.z, fmaf(wg.w, xv.w, g))));
+          u = fmaf(wu.x, xv.x, fmaf(wu.y, xv.y, fmaf(wu.z, xv.z, fmaf(wu.w, xv.w, u))));
+        }
+        g = warp_sum(g);
+        u = warp_sum(u);
+        if (lane == 0) a.h[(size_t)asg_s[i] * f + fi] = silu(g) * u;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kDnWarps * 32, 1) dn_f32_kernel(ExpertArgs a) {
+  extern __shared__ float P[];
+  __shared__ int tok_s[kDnWarps][kSmallT], asg_s[kDnWarps][kSmallT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, f = a.f, T = a.T, K = a.K;
+  const int j0 = blockIdx.x * kDnRows;
+  const int n_act = *a.n_active;
+  const int n_slots = n_act + a.has_shared;
+  for (int s = warp; s < n_slots; s += kDnWarps) {
+    SlotInfo si;
+    if (lane == 0) si = slot_tokens(a, s, n_act, tok_s[warp], asg_s[warp]);
+    __syncwarp();
+    si.n = __shfl_sync(0xffffffffu, si.n, 0);
+    si.e = __shfl_sync(0xffffffffu, si.e, 0);
+    si.shared = __shfl_sync(0xffffffffu, (int)si.shared, 0);
+    const float* W = si.shared ? static_cast<const float*>(a.sh_dn_q)
+                               : static_cast<const float*>(a.dn_q) + (size_t)si.e * d * f;
+    for (int i = 0; i < si.n; ++i) {
+      const int as = asg_s[warp][i];
+      for (int r = 0; r < kDnRows; ++r) {
+        const int j = j0 + r;
+        float acc = 0.f;
+        if (j < d) {
+          for (int k4 = lane; k4 < f / 4; k4 += 32) {
+            const float4 hv = __ldcg(reinterpret_cast<const float4*>(a.h + (size_t)as * f) + k4);
+            const float4 wv = __ldg(reinterpret_cast<const float4*>(W + (size_t)j * f) + k4);
+            acc = fmaf(wv.x, hv.x, fmaf(wv.y, hv.y, fmaf(wv.z, hv.z, fmaf(wv.w, hv.w, acc))));
+          }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) P[(size_t)as * kDnRows + r] = acc;
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * kDnRows; i += blockDim.x) {
+    const int t = i / kDnRows, r = i - t * kDnRows;
+    if (j0 + r >= d) continue;
+    float y = 0.f;
+    for (int k = 0; k < K; ++k) y = fmaf(a.topk_w[t * K + k], P[(size_t)(t * K + k) * kDnRows + r], y);
+    if (a.has_shared) y += P[(size_t)(T * K + t) * kDnRows + r];
+    const size_t o = (size_t)t * d + j0 + r;
+    if (a.resid) y = load_act(a.resid, a.act, o) + y;
+    store_act(a.y, a.act, o, y);
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+static int g_num_sms = 148;
+
+cudaError_t gemv_kernels_init(int num_sms) {
+  g_num_sms = num_sms;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gu_int4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  if ((e = cudaFuncSetAttribute(gu_int4_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  if ((e = cudaFuncSetAttribute(gu_int4_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  if ((e = cudaFuncSetAttribute(gu_int4_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  if ((e = cudaFuncSetAttribute(gu_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  if ((e = cudaFuncSetAttribute(dn_int4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  if ((e = cudaFuncSetAttribute(dn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
+  return cudaSuccess;
+}
+
+size_t gemv_smem_gu(int wfmt, int T, int d) {
+  if (wfmt == kWInt4) return (size_t)T * 8 * (d / 32) * sizeof(float4) + (size_t)T * (d / 32) * sizeof(float);
+  return (size_t)T * d * sizeof(float);
+}
+
+size_t gemv_smem_dn(int T, int K) { return (size_t)(T * K + T) * kDnRows * sizeof(float); }
+
+// Launches gate/up then down+combine for T <= kSmallT tokens.
+cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid) {
+  const int dn_grid = (a.d + kDnRows - 1) / kDnRows;
+  const size_t sm_gu = gemv_smem_gu(wfmt, a.T, a.d);
+  const size_t sm_dn = gemv_smem_dn(a.T, a.K);
+  if (wfmt == kWInt4) {
+    const int G = a.d / 32;
+    const int ng = (G + 31) / 32;
+    const int grid = g_num_sms * (sm_gu <= 100 * 1024 ? 2 : 1);
+    switch (ng) {
+      case 1: gu_int4_kernel<1><<<grid, 256, sm_gu, st>>>(a); break;
+      case 2: gu_int4_kernel<2><<<grid, 256, sm_gu, st>>>(a); break;
+      case 3: gu_int4_kernel<3><<<grid, 256, sm_gu, st>>>(a); break;
+      case 4: gu_int4_kernel<4><<<grid, 256, sm_gu, st>>>(a); break;
+      default: return cudaErrorInvalidValue;
+    }
+    if (mid) cudaEventRecord(mid, st);
+    dn_int4_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
+  } else {
+    gu_f32_kernel<<<g_num_sms, 256, sm_gu, st>>>(a);
+    if (mid) cudaEventRecord(mid, st);
+    dn_f32_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

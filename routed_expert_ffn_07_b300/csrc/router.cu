@@ -1,0 +1,418 @@
+// Router, top-K selection and token->expert dispatch (sm_103a).
+//
+// The router scores every expert of the layer for every token and keeps the 10 best per token
+// ('Strata はなぜ少ない VRAM でも速いのか' (modeldock.net), section '問題：1,250 億パラメータと
+// 12 GB'); the chosen expert numbers are handed on to whoever computes the experts (same page,
+// section '1 トークン、三者の分担', where they go to a page-locked "doorbell" for the CPU).  Here
+// every expert is in HBM, so the hand-off is a device-side dispatch: a per-expert histogram, an
+// exclusive prefix sum and a stable counting sort of the assignments, plus the ascending list of
+// distinct experts, all deterministic.
+//
+// Arithmetic: logits in fp32 (FMA, fixed per-lane order + fixed shuffle tree), softmax over all E
+// logits with expf, K rounds of warp arg-max (larger logit first, ties to the lower index), the
+// kept probabilities renormalised.  Selection compares fp32 logits.
+#include "common.cuh"
+
+namespace moe {
+
+// Block-wide exclusive scan of vals[0..n) in shared memory, n <= 4 * blockDim.x, blockDim a
+// multiple of 32 and <= 1024.  Returns the total on every thread.
+__device__ int block_exclusive_scan(int* vals, int n, int* scratch /* >= 33 ints */) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;  // <= 4
+  int loc[4];
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = tid * per + i;
+    loc[i] = (i < per && j < n) ? vals[j] : 0;
+    s += loc[i];
+  }
+  int incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nwarps ? scratch[lane] : 0;
+    int wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    scratch[lane] = wi - v;          // exclusive prefix of warp totals
+    if (lane == 31) scratch[32] = wi; // grand total
+  }
+  __syncthreads();
+  int run = scratch[warp] + incl - s;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = tid * per + i;
+    if (i < per && j < n) {
+      vals[j] = run;
+      run += loc[i];
+    }
+  }
+  const int total = scratch[32];
+  __syncthreads();
+  return total;
+}
+
+// Softmax over E logits (in shared memory, one warp), the K largest (ties: lower index), weights
+// renormalised over the kept K.  Writes idx/w for the token (global).  sidx / sp: K-entry scratch.
+__device__ void topk_warp(const float* lg, int E, int K, int32_t* out_idx, float* out_w, int32_t* sidx,
+                          float* sp) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int e = lane; e < E; e += 32) m = fmaxf(m, lg[e]);
+  m = warp_max(m);
+  float z = 0.f;
+  for (int e = lane; e < E; e += 32) z += expf(lg[e] - m);
+  z = warp_sum(z);
+  uint32_t taken = 0u;
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    int j = 0;
+    for (int e = lane; e < E; e += 32, ++j) {
+      if ((taken >> j) & 1u) continue;
+      const float v = lg[e];
+      if (bi == 0x7fffffff || v > bv) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) {
+      sidx[k] = bi;
+      sp[k] = expf(bv - m) / z;
+    }
+  }
+  __syncwarp();
+  if (lane < K) {
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) s += sp[k];
+    out_idx[lane] = sidx[lane];
+    out_w[lane] = sp[lane] / s;
+  }
+  __syncwarp();
+}
+
+// Dispatch of n = T*K assignments held in shared memory (one block, any blockDim multiple of 32).
+// cnt: E ints of shared scratch.  Writes counts, offs, perm, active, n_active, stat.
+__device__ void dispatch_block(const int32_t* idx_s, int n, int E, int* cnt, int* scratch, const RouteArgs& a) {
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[idx_s[i]], 1);
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) a.counts[e] = cnt[e];
+  __syncthreads();
+  const int total = block_exclusive_scan(cnt, E, scratch);  // cnt now holds offs
+  for (int e = tid; e < E; e += blockDim.x) a.offs[e] = cnt[e];
+  if (tid == 0) a.offs[E] = total;
+  // perm: rank of assignment i among the earlier assignments of the same expert
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int e = idx_s[i];
+    int r = 0;
+    for (int j = 0; j < i; ++j) r += (idx_s[j] == e);
+    a.perm[cnt[e] + r] = i;
+  }
+  __syncthreads();
+  // active list: experts with a non-zero count, ascending
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = a.counts[e] > 0 ? 1 : 0;
+  __syncthreads();
+  const int nact = block_exclusive_scan(cnt, E, scratch);
+  for (int e = tid; e < E; e += blockDim.x)
+    if (a.counts[e] > 0) a.active[cnt[e]] = e;
+  if (tid == 0) {
+    *a.n_active = nact;
+    if (a.stat) *a.stat = nact;
+  }
+}
+
+// ------------------------------------------------------------------ small T (fused, one launch)
+// grid = ceil(E / 8) blocks of 256 threads; each warp scores one expert for all T tokens; the last
+// block to finish (ticket) runs softmax/top-K for every token and the dispatch.
+// Dynamic shared memory: T*d floats (activations) + 8*E floats (per-warp logit rows).
+__global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
+  extern __shared__ float smem[];
+  float* xs = smem;                         // [T][d]
+  float* lgs = smem + (size_t)a.T * a.d;    // [8][E]
+  __shared__ int32_t idx_s[kSmallT * kMaxK];
+  __shared__ int32_t sidx[kRouterWarps][kMaxK];
+  __shared__ float sp[kRouterWarps][kMaxK];
+  __shared__ float inv_s[kSmallT];
+  __shared__ int scratch[40];
+  __shared__ int is_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = a.T, d = a.d, E = a.E, K = a.K;
+
+  if (a.prenorm) {
+    for (int t = warp; t < T; t += kRouterWarps) {
+      float ss = 0.f;
+      for (int j = lane; j < d; j += 32) {
+        const float v = load_act(a.x, a.act, (size_t)t * d + j);
+        ss += v * v;
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) inv_s[t] = 1.0f / sqrtf(ss / (float)d + a.eps);
+    }
+    __syncthreads();
+  }
+  for (int i = tid; i < T * d; i += blockDim.x) {
+    float v = load_act(a.x, a.act, i);
+    if (a.prenorm) {
+      v = round_act(a.act, v * inv_s[i / d]);
+      if (blockIdx.x == 0) store_act(a.xnorm, a.act, i, v);
+    }
+    xs[i] = v;
+  }
+  __syncthreads();
+
+  const int e = blockIdx.x * kRouterWarps + warp;
+  if (e < E) {
+    float acc[kSmallT];
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
+    const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)e * d);
+    const int nc = d >> 2;
+#pragma unroll 4
+    for (int c = lane; c < nc; c += 32) {
+      const float4 wv = __ldg(wr + c);
+#pragma unroll
+      for (int t = 0; t < kSmallT; ++t) {
+        if (t < T) {
+          const float4 xv = reinterpret_cast<const float4*>(xs + (size_t)t * d)[c];
+          acc[t] = fmaf(wv.x, xv.x, acc[t]);
+          acc[t] = fmaf(wv.y, xv.y, acc[t]);
+          acc[t] = fmaf(wv.z, xv.z, acc[t]);
+          acc[t] = fmaf(wv.w, xv.w, acc[t]);
+        }
+      }
+    }
+    const float b = a.bias ? a.bias[e] : 0.f;
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t) {
+      if (t < T) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) a.logits[(size_t)t * E + e] = v + b;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned tk = atomicAdd(a.ticket, 1u);
+    is_last = (tk == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // ---- last block: top-K per token (one warp per token)
+  float* lg = lgs + (size_t)warp * E;
+  for (int t = warp; t < T; t += kRouterWarps) {
+    for (int j = lane; j < E; j += 32) lg[j] = __ldcg(a.logits + (size_t)t * E + j);
+    __syncwarp();
+    topk_warp(lg, E, K, a.idx + (size_t)t * K, a.w + (size_t)t * K, sidx[warp], sp[warp]);
+    if (lane < K) idx_s[t * K + lane] = sidx[warp][lane];
+    __syncwarp();
+  }
+  __syncthreads();
+  int* cnt = reinterpret_cast<int*>(lgs);  // reuse (E ints)
+  dispatch_block(idx_s, T * K, E, cnt, scratch, a);
+  if (tid == 0) *a.ticket = 0u;
+}
+
+// ------------------------------------------------------------------ large T
+// RMSNorm without weight, one warp per token: xnorm = round_act(x / sqrt(mean(x^2) + eps)).
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const void* x, void* xnorm, int act, int T, int d, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float ss = 0.f;
+  for (int j = lane; j < d; j += 32) {
+    const float v = load_act(x, act, (size_t)t * d + j);
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int j = lane; j < d; j += 32)
+    store_act(xnorm, act, (size_t)t * d + j, load_act(x, act, (size_t)t * d + j) * inv);
+}
+
+// logits[T][E] = X[T][d] * Wr[E][d]^T (+ bias), fp32 FMA in ascending k per output.
+// Tile 64 tokens x 64 experts x 16 k, 256 threads, 4x4 outputs per thread.
+__global__ void __launch_bounds__(256) router_logits_kernel(const void* x, int act, const float* Wr, const float* bias,
+                                                            float* logits, int T, int d, int E) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < d; k0 += 16) {
+    for (int i = tid; i < 64 * 16; i += 256) {
+      const int r = i >> 4, kk = i & 15;
+      const int t = t0 + r, e = e0 + r;
+      As[kk][r] = (t < T) ? load_act(x, act, (size_t)t * d + k0 + kk) : 0.f;
+      Bs[kk][r] = (e < E) ? Wr[(size_t)e * d + k0 + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        av[i] = As[kk][ty * 4 + i];
+        bv[i] = Bs[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+    }
+  }
+}
+
+// Top-K for T tokens, one warp per token.  Dynamic shared memory: 8*E floats.
+__global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
+  extern __shared__ float smem[];
+  __shared__ int32_t sidx[kRouterWarps][kMaxK];
+  __shared__ float sp[kRouterWarps][kMaxK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kRouterWarps + warp;
+  if (t >= a.T) return;
+  float* lg = smem + (size_t)warp * a.E;
+  for (int j = lane; j < a.E; j += 32) lg[j] = a.logits[(size_t)t * a.E + j];
+  __syncwarp();
+  topk_warp(lg, a.E, a.K, a.idx + (size_t)t * a.K, a.w + (size_t)t * a.K, sidx[warp], sp[warp]);
+}
+
+constexpr int kDispatchBlock = 256;  // assignments per block of the large-T dispatch
+
+// Per-block histogram of expert ids: blockhist[b][e].
+__global__ void __launch_bounds__(kDispatchBlock) dispatch_hist_kernel(RouteArgs a) {
+  __shared__ int cnt[kMaxE];
+  const int n = a.T * a.K;
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int i = blockIdx.x * kDispatchBlock + threadIdx.x;
+  if (i < n) {
+    const int e = a.idx[i];
+    if (e >= 0 && e < a.E)
+      atomicAdd(&cnt[e], 1);
+    else
+      atomicOr(a.status, kStatusBadIndex);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) a.blockhist[(size_t)blockIdx.x * a.E + e] = cnt[e];
+}
+
+// One block of 1024 threads: counts, offs, per-block bases (in place in blockhist), active list.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(RouteArgs a, int nblocks) {
+  __shared__ int vals[kMaxE];
+  __shared__ int scratch[40];
+  const int E = a.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int b = 0; b < nblocks; ++b) s += a.blockhist[(size_t)b * E + e];
+    a.counts[e] = s;
+    vals[e] = s;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(vals, E, scratch);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    a.offs[e] = vals[e];
+    int run = vals[e];
+    for (int b = 0; b < nblocks; ++b) {
+      const int c = a.blockhist[(size_t)b * E + e];
+      a.blockhist[(size_t)b * E + e] = run;
+      run += c;
+    }
+  }
+  if (threadIdx.x == 0) a.offs[E] = total;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) vals[e] = a.counts[e] > 0 ? 1 : 0;
+  __syncthreads();
+  const int nact = block_exclusive_scan(vals, E, scratch);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (a.counts[e] > 0) a.active[vals[e]] = e;
+  if (threadIdx.x == 0) {
+    *a.n_active = nact;
+    if (a.stat) *a.stat = nact;
+  }
+}
+
+// Stable scatter: assignment i goes to base[b][e] + (rank among earlier same-expert ones in block b).
+__global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(RouteArgs a) {
+  __shared__ int32_t ids[kDispatchBlock];
+  const int n = a.T * a.K;
+  const int i0 = blockIdx.x * kDispatchBlock;
+  const int i = i0 + threadIdx.x;
+  ids[threadIdx.x] = (i < n) ? a.idx[i] : -1;
+  __syncthreads();
+  if (i >= n) return;
+  const int e = ids[threadIdx.x];
+  if (e < 0 || e >= a.E) return;
+  int r = 0;
+  for (int j = 0; j < (int)threadIdx.x; ++j) r += (ids[j] == e);
+  a.perm[a.blockhist[(size_t)blockIdx.x * a.E + e] + r] = i;
+}
+
+// ------------------------------------------------------------------ host-side launchers
+size_t route_small_smem(int T, int d, int E) { return ((size_t)T * d + (size_t)kRouterWarps * E) * sizeof(float); }
+
+cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t st) {
+  if (a.T <= kSmallT && (size_t)a.T * a.d * 4 <= 160 * 1024) {
+    const size_t sm = route_small_smem(a.T, a.d, a.E);
+    const int grid = (a.E + kRouterWarps - 1) / kRouterWarps;
+    route_small_kernel<<<grid, 256, sm, st>>>(a);
+    return cudaGetLastError();
+  }
+  const void* xin = a.x;
+  if (a.prenorm) {
+    rmsnorm_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a.x, a.xnorm, a.act, a.T, a.d, a.eps);
+    xin = a.xnorm;
+  }
+  dim3 g((a.E + 63) / 64, (a.T + 63) / 64);
+  router_logits_kernel<<<g, 256, 0, st>>>(xin, a.act, a.Wr, a.bias, a.logits, a.T, a.d, a.E);
+  topk_kernel<<<(a.T + kRouterWarps - 1) / kRouterWarps, 256, (size_t)kRouterWarps * a.E * sizeof(float), st>>>(a);
+  dispatch_hist_kernel<<<nblocks_dispatch, kDispatchBlock, 0, st>>>(a);
+  dispatch_scan_kernel<<<1, 1024, 0, st>>>(a, nblocks_dispatch);
+  dispatch_scatter_kernel<<<nblocks_dispatch, kDispatchBlock, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t route_kernels_init() {
+  cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+}
+
+}  // namespace moe

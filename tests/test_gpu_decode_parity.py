@@ -1,0 +1,268 @@
+"""GPU (CUDA library, through the C ABI) vs the fp64 oracle: router, dispatch, GEMV experts, stack."""
+import numpy as np
+import pytest
+
+import oracle
+from routed_expert_ffn_07_b300 import inputs
+from routed_expert_ffn_07_b300.workloads import WORKLOADS, Workload, alloc_and_fill, create_handle, host_experts
+from tests.parity import (Y_TOL, W_ATOL, check_dispatch, check_routing, from_torch_act, to_torch_act, y_error)
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def run_layer(h, wl, weights, x_np, T, layer=0, gen_layer=0):
+    """Route + forward one layer on the GPU and check everything against the oracle."""
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    K, E = wl.K, wl.E
+    x = to_torch_act(x_np)
+    idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T * K, dtype=torch.float32, device="cuda")
+    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    capi.moe_route(h, layer, x, T, idx, w, offs, perm)
+    y = torch.empty_like(x)
+    capi.moe_layer_forward(h, layer, x, T, y)
+    torch.cuda.synchronize()
+    assert capi.moe_get_device_status(h) == 0
+    Wr = weights["router"][layer].cpu().numpy()
+    bias = None if weights["bias"] is None else weights["bias"][layer].cpu().numpy()
+    logits, idx_ref, w_ref, gap = oracle.route(x_np, Wr, bias, K)
+    idx_g = idx.cpu().numpy().reshape(T, K)
+    flagged = check_routing(logits, idx_ref, gap, idx_g)
+    check_dispatch(idx_g, E, offs.cpu().numpy(), perm.cpu().numpy())
+    w_exp = oracle.weights_for(logits, idx_g)
+    np.testing.assert_allclose(w.cpu().numpy().reshape(T, K), w_exp, rtol=0, atol=W_ATOL)
+    used = sorted(set(idx_g.ravel().tolist()))
+    ex = host_experts(wl, gen_layer, used + ([E] if wl.shared else []))
+    sh = ex.pop(E) if wl.shared else None
+    y_ref, _, _ = oracle.layer(x_np, Wr, bias, ex, E, K, shared=sh, idx=idx_g)
+    err = y_error(oracle.widen(from_torch_act(y)), y_ref)
+    assert err <= Y_TOL, f"max err {err:.3e} > {Y_TOL}"
+    return y, err, flagged
+
+
+def test_device_generator_matches_host():
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl = WORKLOADS[2]
+    d, f = 1024, 256
+    for layer, e0, n in ((0, 0, 3), (7, 511, 2)):
+        gu = torch.empty((n, 2 * f, d // 2), dtype=torch.uint8, device="cuda")
+        gs = torch.empty((n, 2 * f, d // 32), dtype=torch.float16, device="cuda")
+        dn = torch.empty((n, d, f // 2), dtype=torch.uint8, device="cuda")
+        ds = torch.empty((n, d, f // 32), dtype=torch.float16, device="cuda")
+        capi.moe_gen_int4_planes(gu, wl.seed, layer, inputs.T_GU_Q, e0, n, gu[0].numel())
+        capi.moe_gen_scale_planes(gs, wl.seed, layer, inputs.T_GU_S, e0, n, gs[0].numel())
+        capi.moe_gen_int4_planes(dn, wl.seed, layer, inputs.T_DN_Q, e0, n, dn[0].numel())
+        capi.moe_gen_scale_planes(ds, wl.seed, layer, inputs.T_DN_S, e0, n, ds[0].numel())
+        torch.cuda.synchronize()
+        for i in range(n):
+            ref = inputs.gen_expert_int4(wl.seed, layer, e0 + i, d, f)
+            np.testing.assert_array_equal(gu[i].cpu().numpy(), ref["gu_q"])
+            np.testing.assert_array_equal(gs[i].cpu().numpy().view(np.uint16), ref["gu_s"])
+            np.testing.assert_array_equal(dn[i].cpu().numpy(), ref["dn_q"])
+            np.testing.assert_array_equal(ds[i].cpu().numpy().view(np.uint16), ref["dn_s"])
+
+
+def test_tiny_fp32_layer():
+    from routed_expert_ffn_07_b300 import capi
+    wl = WORKLOADS[1]
+    wts = alloc_and_fill(wl)
+    h = create_handle(wl, wts)
+    try:
+        x = inputs.gen_activations(wl.seed, wl.T, wl.d, "f32")
+        _, err, _ = run_layer(h, wl, wts, x, wl.T)
+        assert err < 1e-4  # fp32 everywhere
+        for T in (1, 3, 7):
+            run_layer(h, wl, wts, x[:T], T)
+    finally:
+        capi.moe_destroy(h)
+
+
+SMALL = [
+    # d, f, E, K, shared, T values
+    (1024, 256, 32, 4, True, (1, 2, 5, 16)),
+    (2048, 128, 16, 3, False, (1, 4, 9)),
+    (3072, 384, 24, 6, True, (1, 7, 16)),
+    (1024, 512, 8, 8, True, (1, 3)),     # K = E: every expert for every token
+    (2048, 256, 64, 1, True, (1, 16)),   # K = 1
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_int4_shapes(case):
+    from routed_expert_ffn_07_b300 import capi
+    d, f, E, K, sh, Ts = SMALL[case]
+    wl = Workload(200 + case, f"small{case}", max(Ts), d, E, K, f, sh, "int4", "bf16", 2, False)
+    wts = alloc_and_fill(wl)
+    h = create_handle(wl, wts)
+    try:
+        for layer in (0, 1):
+            x = inputs.gen_activations(wl.seed, max(Ts), d, "bf16", layer=layer)
+            for T in Ts:
+                run_layer(h, wl, wts, x[:T], T, layer=layer, gen_layer=layer)
+    finally:
+        capi.moe_destroy(h)
+
+
+def test_exact_ties_lower_index_on_gpu():
+    """Duplicated router rows give bit-identical logits on both sides: the lower index must win."""
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl = Workload(250, "ties", 4, 1024, 32, 4, 128, True, "int4", "bf16", 1, False)
+    wts = alloc_and_fill(wl)
+    r = wts["router"][0]
+    for a, b in ((3, 17), (5, 6), (9, 30), (12, 2)):
+        r[b] = r[a]
+    h = create_handle(wl, wts)
+    try:
+        x = inputs.gen_activations(wl.seed, 4, wl.d, "bf16")
+        run_layer(h, wl, wts, x, 4)
+    finally:
+        capi.moe_destroy(h)
+
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    from routed_expert_ffn_07_b300 import capi
+    wl = WORKLOADS[2]
+    wts = alloc_and_fill(wl, n_layers=3)
+    h = create_handle(wl, wts, max_tokens=16)
+    yield wl, wts, h
+    capi.moe_destroy(h)
+
+
+def test_decode_layer_full_size(decode_layer):
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl, wts, h = decode_layer
+    for layer in range(3):
+        x = inputs.gen_activations(wl.seed, 1, wl.d, "bf16", layer=layer)
+        y, err, _ = run_layer(h, wl, wts, x, 1, layer=layer, gen_layer=layer)
+        # run-to-run bit identity
+        y2 = torch.empty_like(y)
+        capi.moe_layer_forward(h, layer, to_torch_act(x), 1, y2)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+        # the host-buffer entry point gives the same bits
+        yh = np.zeros_like(x)
+        capi.moe_layer_forward_host(h, layer, np.ascontiguousarray(x), 1, yh)
+        np.testing.assert_array_equal(yh, from_torch_act(y))
+
+
+def test_decode_layer_batch_sizes(decode_layer):
+    wl, wts, h = decode_layer
+    x = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=5)
+    for T in (2, 4, 16):
+        run_layer(h, wl, wts, x[:T], T, layer=1, gen_layer=1)
+
+
+def _stack_parity(wl, sample_layers):
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wts = alloc_and_fill(wl)
+    L, T, d, K, E = wl.layers, wl.T, wl.d, wl.K, wl.E
+    h = create_handle(wl, wts)
+    try:
+        x0 = inputs.gen_activations(wl.seed, T, d, "bf16")
+        xa = to_torch_act(x0)
+        trace = torch.empty((L, 2, T, d), dtype=torch.bfloat16, device="cuda")
+        capi.moe_stack_forward(h, xa, T, trace)
+        xg = to_torch_act(x0)
+        capi.moe_stack_forward(h, xg, T)   # graph replay
+        capi.moe_stack_forward(h, xg2 := to_torch_act(x0), T)
+        torch.cuda.synchronize()
+        assert capi.moe_get_device_status(h) == 0
+        assert torch.equal(xa.view(torch.int16), xg.view(torch.int16)), "graph replay != eager launches"
+        assert torch.equal(xg.view(torch.int16), xg2.view(torch.int16)), "graph replays differ"
+        tr = trace.view(torch.int16).cpu().numpy().view(np.uint16)
+        final = from_torch_act(xa)
+        counts = capi.moe_get_active_counts(h, L)
+        flagged_total = 0
+        worst = 0.0
+        for l in sample_layers:
+            x_l, xn_l = tr[l, 0], tr[l, 1]
+            x_next = tr[l + 1, 0] if l + 1 < L else final
+            # RMSNorm (fp32 on the GPU, rounded to bf16) vs fp64: within one bf16 ulp
+            ref_n = oracle.rmsnorm(x_l, 1e-6)
+            got_n = oracle.widen(xn_l)
+            assert np.all(np.abs(got_n - ref_n) <= 2.0 ** -8 * np.abs(ref_n) + 1e-30)
+            # routing of the layer on its (GPU) normalised input, re-run through the public route call
+            idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
+            offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+            perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
+            capi.moe_route(h, l, to_torch_act(xn_l), T, idx, None, offs, perm)
+            torch.cuda.synchronize()
+            Wr = wts["router"][l].cpu().numpy()
+            bias = None if wts["bias"] is None else wts["bias"][l].cpu().numpy()
+            logits, idx_ref, _, gap = oracle.route(xn_l, Wr, bias, K)
+            idx_g = idx.cpu().numpy().reshape(T, K)
+            flagged_total += check_routing(logits, idx_ref, gap, idx_g)
+            active = check_dispatch(idx_g, E, offs.cpu().numpy(), perm.cpu().numpy())
+            assert counts[l] == len(active)
+            ex = host_experts(wl, l, sorted(set(idx_g.ravel().tolist())) + [E])
+            sh = ex.pop(E)
+            y_ref, _, _ = oracle.layer(xn_l, Wr, bias, ex, E, K, shared=sh, idx=idx_g)
+            x_ref = oracle.widen(x_l) + y_ref
+            got = oracle.widen(x_next)
+            tol = Y_TOL * np.abs(y_ref).max() + 2.0 ** -8 * np.abs(x_ref)
+            bad = np.abs(got - x_ref) > tol
+            assert not bad.any(), f"layer {l}: {bad.sum()} elements out of tolerance"
+            worst = max(worst, float((np.abs(got - x_ref) / (np.abs(y_ref).max())).max()))
+        return counts, flagged_total, worst
+    finally:
+        capi.moe_destroy(h)
+        del wts
+        torch.cuda.empty_cache()
+
+
+def test_verify_stack_T4_48_layers():
+    wl = WORKLOADS[3]
+    counts, flagged, worst = _stack_parity(wl, sample_layers=[0, 1, 2, 7, 15, 23, 24, 31, 40, 45, 46, 47])
+    assert all(10 <= c <= 40 for c in counts)
+
+
+def test_skewed_stack_T16_zipf():
+    wl = WORKLOADS[5]
+    counts, flagged, worst = _stack_parity(wl, sample_layers=[0, 5, 17, 29, 41, 47])
+    assert all(10 <= c <= 160 for c in counts)
+    assert np.mean(counts) < 120  # the popularity prior concentrates the routing
+
+
+def test_invalid_arguments_rejected():
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl = Workload(260, "args", 4, 1024, 16, 2, 128, True, "int4", "bf16", 2, False)
+    wts = alloc_and_fill(wl, n_layers=1)
+    h = capi.moe_create(wl.d, wl.f, wl.E, wl.K, 2, 4, has_shared=True)
+    try:
+        x = torch.zeros((8, wl.d), dtype=torch.bfloat16, device="cuda")
+        y = torch.zeros_like(x)
+        with pytest.raises(capi.MoeError) as ei:
+            capi.moe_layer_forward(h, 0, x, 2, y)
+        assert ei.value.status == 6  # weights not set
+        capi.moe_set_layer(h, 0, wts["router"][0], wts["gu_q"][0], wts["gu_s"][0], wts["dn_q"][0], wts["dn_s"][0],
+                           sh_gu_q=wts["sh_gu_q"][0], sh_gu_s=wts["sh_gu_s"][0], sh_dn_q=wts["sh_dn_q"][0],
+                           sh_dn_s=wts["sh_dn_s"][0])
+        for bad in (lambda: capi.moe_layer_forward(h, 0, x, 5, y),          # T > max_tokens
+                    lambda: capi.moe_layer_forward(h, 0, x, 0, y),          # T = 0
+                    lambda: capi.moe_layer_forward(h, 2, x, 2, y),          # layer out of range
+                    lambda: capi.moe_layer_forward(h, 0, x, 2, x),          # y overlaps x
+                    lambda: capi.moe_layer_forward(h, 0, 0, 2, y),          # null x
+                    lambda: capi.moe_layer_forward(h, 0, x.data_ptr() + 2, 2, y)):  # misaligned
+            with pytest.raises(capi.MoeError) as ei:
+                bad()
+            assert ei.value.status == 1
+        with pytest.raises(capi.MoeError):
+            capi.moe_set_layer(h, 1, 0, wts["gu_q"][0], wts["gu_s"][0], wts["dn_q"][0], wts["dn_s"][0])
+        capi.moe_layer_forward(h, 0, x, 2, y)
+        torch.cuda.synchronize()
+        assert capi.moe_get_device_status(h) == 0
+    finally:
+        capi.moe_destroy(h)
