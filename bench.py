@@ -271,6 +271,27 @@ def measure_decode_layer(wl, steps, warmup, rank, world, extras):
     return res
 
 
+def run_profile_case(args):
+    """Small case for ncu: the decode layer over 2 layers' weights (about 2.7 GB on the device),
+    `warmup` + `steps` graph replays, nothing else.  Not a benchmark line."""
+    import torch
+    from routed_expert_ffn_07_b300 import capi, inputs
+    from routed_expert_ffn_07_b300.workloads import WORKLOADS, alloc_and_fill, create_handle
+    wl = WORKLOADS[2]
+    L = 2
+    wts = alloc_and_fill(wl, n_layers=L)
+    h = create_handle(wl, wts, max_tokens=wl.T, n_layers=L, prenorm=False)
+    x_np = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)
+    x = torch.from_numpy(x_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    for i in range(args.warmup + args.steps):
+        capi.moe_layer_forward(h, i % L, x, wl.T, y)
+    torch.cuda.synchronize()
+    assert capi.moe_get_device_status(h) == 0
+    capi.moe_destroy(h)
+    print(json.dumps({"profile_case": wl.name, "layers": L, "calls": args.warmup + args.steps}))
+
+
 def run_ours(args):
     rank, world, local = dist_init(args.gpus)
     import torch
@@ -366,10 +387,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--extras", action="store_true", help="also measure the stack and prefill workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="small case for ncu captures (not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

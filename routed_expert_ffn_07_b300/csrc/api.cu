@@ -17,11 +17,17 @@ cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t 
 cudaError_t route_kernels_init();
 cudaError_t gemv_kernels_init(int num_sms);
 cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid);
-size_t gemv_smem_gu(int wfmt, int T, int d);
-size_t gemv_smem_dn(int T, int K);
+size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K);
+size_t gemv_smem_dn(int T, int K, int E);
 cudaError_t gemm_kernels_init(int num_sms);
 size_t gemm_workspace_bytes(int max_tokens, int d, int f, int E, int K);
-cudaError_t launch_experts_gemm(const ExpertArgs& a, void* gemm_ws, cudaStream_t st, cudaEvent_t mid);
+bool gemm_shape_ok(int d, int f);
+void* gemm_maps_new();
+void gemm_maps_free(void* p);
+cudaError_t gemm_build_maps(void* maps, int E, int d, int f, int has_shared, const void* gu_q, const void* gu_s,
+                            const void* dn_q, const void* dn_s, const void* sh_gu_q, const void* sh_gu_s,
+                            const void* sh_dn_q, const void* sh_dn_s);
+cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps, void* gemm_ws, cudaStream_t st, cudaEvent_t mid);
 constexpr int kDispatchBlockHost = 256;
 }  // namespace moe
 
@@ -30,6 +36,7 @@ using namespace moe;
 struct LayerW {
   moe_layer_weights w;
   bool set = false;
+  void* maps = nullptr;  // TMA descriptors of the layer's planes (tensor-core path only)
 };
 
 struct moe_ctx {
@@ -49,6 +56,7 @@ struct moe_ctx {
   int32_t* active;
   int32_t* n_active;
   int32_t* stats;
+  int4* slots;
   unsigned* ticket;
   unsigned* status;
   int32_t* blockhist;
@@ -110,6 +118,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   if (c.wfmt == MOE_W_INT4_G32) {
     if (c.d % 128 || c.f % 128) return MOE_ERR_UNSUPPORTED;
     if (c.d > 4096 || c.f > 1024) return MOE_ERR_UNSUPPORTED;  // GEMV lane mapping limits
+    if (c.max_tokens > kSmallT && !gemm_shape_ok(c.d, c.f)) return MOE_ERR_UNSUPPORTED;  // tensor-core path
   } else {
     if (c.max_tokens > kSmallT) return MOE_ERR_UNSUPPORTED;   // fp32 experts: GEMV path only
   }
@@ -144,6 +153,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   sz[n++] = up256((size_t)E * 4);                     // active
   sz[n++] = up256(4);                                 // n_active
   sz[n++] = up256((size_t)c.n_layers * 4);            // stats
+  sz[n++] = up256((size_t)E * 16);                    // slot table
   sz[n++] = up256(4);                                 // ticket
   sz[n++] = up256(4);                                 // status
   sz[n++] = up256((size_t)h->nblocks_max * E * 4);    // blockhist
@@ -173,6 +183,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   h->active = reinterpret_cast<int32_t*>(p); p += sz[i++];
   h->n_active = reinterpret_cast<int32_t*>(p); p += sz[i++];
   h->stats = reinterpret_cast<int32_t*>(p); p += sz[i++];
+  h->slots = reinterpret_cast<int4*>(p); p += sz[i++];
   h->ticket = reinterpret_cast<unsigned*>(p); p += sz[i++];
   h->status = reinterpret_cast<unsigned*>(p); p += sz[i++];
   h->blockhist = reinterpret_cast<int32_t*>(p); p += sz[i++];
@@ -204,8 +215,18 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
     if (q4 && (!w->sh_gu_s || !w->sh_dn_s || !aligned16(w->sh_gu_s) || !aligned16(w->sh_dn_s)))
       return MOE_ERR_INVALID_ARG;
   }
-  h->layers[layer].w = *w;
-  h->layers[layer].set = true;
+  LayerW& L = h->layers[layer];
+  if (h->cfg.max_tokens > kSmallT) {
+    if (!L.maps) L.maps = gemm_maps_new();
+    if (!L.maps) return MOE_ERR_OOM;
+    if (gemm_build_maps(L.maps, h->cfg.n_experts, h->cfg.d, h->cfg.f, h->cfg.has_shared, w->gu_q, w->gu_s, w->dn_q,
+                        w->dn_s, w->sh_gu_q, w->sh_gu_s, w->sh_dn_q, w->sh_dn_s) != cudaSuccess) {
+      L.set = false;
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
+  L.w = *w;
+  L.set = true;
   return MOE_OK;
 }
 
@@ -236,6 +257,7 @@ static RouteArgs make_route_args(moe_ctx* h, int layer, const void* x, int T, bo
   a.active = h->active;
   a.n_active = h->n_active;
   a.stat = stat;
+  a.slots = h->slots;
   a.blockhist = h->blockhist;
   a.ticket = h->ticket;
   a.status = h->status;
@@ -266,6 +288,7 @@ static ExpertArgs make_expert_args(moe_ctx* h, int layer, const void* x, int T, 
   a.perm = h->perm;
   a.active = h->active;
   a.n_active = h->n_active;
+  a.slots = h->slots;
   a.topk_w = h->w;
   a.h = h->h;
   a.y = y;
@@ -284,20 +307,20 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
     if (h->t_next / 4 > h->t_used) h->t_used = h->t_next / 4;
   }
   cudaError_t e;
-  if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return e;
+  if (ev && (e = cudaEventRecordWithFlags(ev[0], st, cudaEventRecordExternal)) != cudaSuccess) return e;
   RouteArgs ra = make_route_args(h, layer, x, T, prenorm, h->stats + layer);
   const int nb = (T * h->cfg.top_k + kDispatchBlockHost - 1) / kDispatchBlockHost;
   e = launch_route(ra, nb, st);
   if (e != cudaSuccess) return e;
-  if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return e;
+  if (ev && (e = cudaEventRecordWithFlags(ev[1], st, cudaEventRecordExternal)) != cudaSuccess) return e;
   const void* xin = prenorm ? h->xnorm : x;
   ExpertArgs ea = make_expert_args(h, layer, xin, T, y, resid);
   if (T <= kSmallT)
     e = launch_experts_gemv(ea, h->cfg.wfmt, st, ev ? ev[2] : nullptr);
   else
-    e = launch_experts_gemm(ea, h->gemm_ws, st, ev ? ev[2] : nullptr);
+    e = launch_experts_gemm(ea, h->layers[layer].maps, h->gemm_ws, st, ev ? ev[2] : nullptr);
   if (e != cudaSuccess) return e;
-  if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return e;
+  if (ev && (e = cudaEventRecordWithFlags(ev[3], st, cudaEventRecordExternal)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -477,6 +500,8 @@ moe_status moe_destroy(moe_handle h) {
   if (!h) return MOE_ERR_INVALID_ARG;
   cudaError_t e = cudaDeviceSynchronize();
   for (cudaEvent_t ev : h->tev) cudaEventDestroy(ev);
+  for (LayerW& L : h->layers)
+    if (L.maps) gemm_maps_free(L.maps);
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->slab) cudaFree(h->slab);

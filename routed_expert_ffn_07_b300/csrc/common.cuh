@@ -18,6 +18,7 @@ constexpr int kSmallT = 16;   // T <= kSmallT: fused router + split-K GEMV exper
 constexpr int kMaxK = 32;
 constexpr int kMaxE = 1024;
 constexpr int kRouterWarps = 8;
+constexpr int kRouterExpertsPerBlock = 4;  // small-T router: 2 warps per expert row
 
 // bits of the device status word
 constexpr unsigned kStatusBadIndex = 1u;
@@ -80,6 +81,7 @@ struct RouteArgs {
   int32_t* active;   // [E] distinct experts, ascending
   int32_t* n_active; // [1]
   int32_t* stat;     // [1] or null: receives n_active (per-layer statistics)
+  int4* slots;       // [E] per distinct expert s: {expert, first perm position, count, 0}
   int32_t* blockhist;// [nblocks][E] (large-T dispatch)
   unsigned* ticket;  // last-block-done counter (zero between launches)
   unsigned* status;  // device status word
@@ -100,6 +102,7 @@ struct ExpertArgs {
   const int32_t* perm;
   const int32_t* active;
   const int32_t* n_active;
+  const int4* slots;      // [E] {expert, first perm position, count, 0}
   const float* topk_w;    // [T][K]
   float* h;               // [(T*K + T)][f] fp32 (GEMV path)
   void* y;                // [T][d]

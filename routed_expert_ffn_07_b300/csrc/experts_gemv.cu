@@ -72,151 +72,186 @@ __device__ __forceinline__ float v_lo(uint32_t lo, int b) {
 }
 
 // ------------------------------------------------------------------ gate/up, int4
-// Shared memory: x' [T][m4=0..7][G][4] (x * 256, group-interleaved), xs136 [T][G].
-template <int NG>  // 32-column groups per lane per row (d = NG * 1024 at full width)
-__global__ void __launch_bounds__(256, 2) gu_int4_kernel(ExpertArgs a) {
-  extern __shared__ float4 smem4[];
+// Persistent: one block per SM, 16 warps.  The (gate row, up row) pairs of all slots are numbered
+// slot-major, p = slot * f + i, and split into one contiguous range per block; warp w of a block
+// takes pairs w, w+16, ... of that range and keeps the next pair's loads in flight while it
+// computes the current one.  All T tokens' activations are staged once per block in shared memory
+// as x' = 256 x in a group-interleaved layout [t][m4=0..7][G][4], with 136 * (group sum) beside.
+constexpr int kGuThreads = 512;
+constexpr int kGuW = kGuThreads / 32;
+
+template <int NG>
+struct PairRegs {
+  uint4 q[2][NG];
+  __half2 s[NG];  // .x = gate scale, .y = up scale
+};
+
+template <int NG>
+__device__ __forceinline__ void gu_load_pair(const ExpertArgs& a, const int4* slot_s, int n_act, int p, int lane,
+                                             PairRegs<NG>& r) {
   const int d = a.d, f = a.f, G = d / 32;
-  float4* xq = smem4;                                            // [T][8][G] float4
-  float* xs136 = reinterpret_cast<float*>(smem4 + (size_t)a.T * 8 * G);  // [T][G]
-  __shared__ int tok_s[kSmallT], asg_s[kSmallT];
-  __shared__ int n_s, shared_s, e_s;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_act = *a.n_active;
-  const int n_slots = n_act + a.has_shared;
-  const int items_per_slot = f / kGuFPerItem;
-  const long long N = (long long)n_slots * items_per_slot;
-  const long long beg = N * blockIdx.x / gridDim.x, end = N * (blockIdx.x + 1) / gridDim.x;
-  int loaded = -1;
-  for (long long it = beg; it < end; ++it) {
-    const int s = (int)(it / items_per_slot), c = (int)(it % items_per_slot);
-    if (s != loaded) {
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const SlotInfo si = slot_tokens(a, s, n_act, tok_s, asg_s);
-        n_s = si.n;
-        shared_s = si.shared;
-        e_s = si.e;
-      }
-      __syncthreads();
-      const int n = n_s;
-      for (int i = threadIdx.x; i < n * d; i += blockDim.x) {
-        const int ti = i / d, k = i - ti * d;
-        const float v = load_act(a.x, a.act, (size_t)tok_s[ti] * d + k) * 256.0f;
-        const int g = k >> 5, m = k & 31;
-        reinterpret_cast<float*>(xq)[(((size_t)ti * 8 + (m >> 2)) * G + g) * 4 + (m & 3)] = v;
-      }
-      __syncthreads();
-      for (int i = threadIdx.x; i < n * G; i += blockDim.x) {
-        const int ti = i / G, g = i - ti * G;
-        float sx = 0.f;
-        for (int m = 0; m < 32; ++m)
-          sx += reinterpret_cast<const float*>(xq)[(((size_t)ti * 8 + (m >> 2)) * G + g) * 4 + (m & 3)];
-        xs136[i] = sx * (136.0f / 256.0f);
-      }
-      __syncthreads();
-      loaded = s;
-    }
-    const int n = n_s;
-    const uint8_t* gq;
-    const __half* gs;
-    if (shared_s) {
-      gq = static_cast<const uint8_t*>(a.sh_gu_q);
-      gs = a.sh_gu_s;
+  const int s = p / f, i = p - s * f;
+  const uint8_t* gq;
+  const __half* gs;
+  if (s < n_act) {
+    const int e = slot_s[s].x;
+    gq = static_cast<const uint8_t*>(a.gu_q) + (size_t)e * 2 * f * (d / 2);
+    gs = a.gu_s + (size_t)e * 2 * f * G;
+  } else {
+    gq = static_cast<const uint8_t*>(a.sh_gu_q);
+    gs = a.sh_gu_s;
+  }
+#pragma unroll
+  for (int j = 0; j < NG; ++j) {
+    const int g = lane + 32 * j;
+    if (g < G) {
+      r.q[0][j] = ldg_nc_v4(gq + (size_t)i * (d / 2) + g * 16);
+      r.q[1][j] = ldg_nc_v4(gq + (size_t)(f + i) * (d / 2) + g * 16);
+      r.s[j] = __halves2half2(gs[(size_t)i * G + g], gs[(size_t)(f + i) * G + g]);
     } else {
-      gq = static_cast<const uint8_t*>(a.gu_q) + (size_t)e_s * 2 * f * (d / 2);
-      gs = a.gu_s + (size_t)e_s * 2 * f * G;
+      r.q[0][j] = r.q[1][j] = make_uint4(0, 0, 0, 0);
+      r.s[j] = __float2half2_rn(0.f);
     }
-    const int fi0 = c * kGuFPerItem + warp * kGuFPerWarp;
-    // rows: 0,1 = gate fi0, fi0+1; 2,3 = up fi0, fi0+1
-    uint4 wq[4][NG];
-    float sc[4][NG];
+  }
+}
+
+template <int NG>
+__device__ __forceinline__ void gu_compute_pair(const ExpertArgs& a, const int4* slot_s, const int* perm_s,
+                                                int n_act, int p, int lane, const float4* xq, const float* xs136,
+                                                const PairRegs<NG>& r) {
+  const int d = a.d, f = a.f, G = d / 32, K = a.K;
+  const int s = p / f, i = p - s * f;
+  int n, pbase;
+  bool shared;
+  if (s < n_act) {
+    const int4 sl = slot_s[s];
+    pbase = sl.y;
+    n = sl.z;
+    shared = false;
+  } else {
+    pbase = 0;
+    n = a.T;
+    shared = true;
+  }
+  for (int t0 = 0; t0 < n; t0 += kTB) {
+    int tok[kTB];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int row = (r < 2 ? 0 : f) + fi0 + (r & 1);
-#pragma unroll
-      for (int j = 0; j < NG; ++j) {
-        const int g = lane + 32 * j;
-        if (g < G) {
-          wq[r][j] = ldg_nc_v4(gq + (size_t)row * (d / 2) + g * 16);
-          sc[r][j] = __half2float(gs[(size_t)row * G + g]);
-        } else {
-          wq[r][j] = make_uint4(0, 0, 0, 0);
-          sc[r][j] = 0.f;
-        }
-      }
+    for (int tt = 0; tt < kTB; ++tt) {
+      const int ti = t0 + tt < n ? t0 + tt : t0;
+      tok[tt] = shared ? ti : perm_s[pbase + ti] / K;
     }
-    for (int t0 = 0; t0 < n; t0 += kTB) {
-      float acc[4][kTB];
+    float acc[2][kTB];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int tt = 0; tt < kTB; ++tt) acc[r][tt] = 0.f;
+      for (int tt = 0; tt < kTB; ++tt) acc[m][tt] = 0.f;
 #pragma unroll
-      for (int j = 0; j < NG; ++j) {
-        const int g = lane + 32 * j;
-        if (g >= G) continue;
-        float part[4][kTB];
+    for (int j = 0; j < NG; ++j) {
+      const int g = lane + 32 * j;
+      if (g >= G) continue;
+      float part[2][kTB];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-          for (int tt = 0; tt < kTB; ++tt) part[r][tt] = 0.f;
+        for (int tt = 0; tt < kTB; ++tt) part[m][tt] = 0.f;
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-          float4 xa[kTB], xb[kTB];
-#pragma unroll
-          for (int tt = 0; tt < kTB; ++tt) {
-            const int ti = (t0 + tt < n) ? t0 + tt : t0;
-            const float4* xp = xq + (size_t)ti * 8 * G + g;
-            xa[tt] = xp[(2 * wd) * G];
-            xb[tt] = xp[(2 * wd + 1) * G];
-          }
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            uint32_t w32 = wd == 0 ? wq[r][j].x : wd == 1 ? wq[r][j].y : wd == 2 ? wq[r][j].z : wq[r][j].w;
-            asm volatile("" : "+r"(w32));  // keep the dequantisation inside the token loop
-            const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
-            const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-            const float v0 = v_lo(lo, 0), v1 = v_lo(hi, 0), v2 = v_lo(lo, 1), v3 = v_lo(hi, 1);
-            const float v4 = v_lo(lo, 2), v5 = v_lo(hi, 2), v6 = v_lo(lo, 3), v7 = v_lo(hi, 3);
-#pragma unroll
-            for (int tt = 0; tt < kTB; ++tt) {
-              float p = part[r][tt];
-              p = fmaf(v0, xa[tt].x, p);
-              p = fmaf(v1, xa[tt].y, p);
-              p = fmaf(v2, xa[tt].z, p);
-              p = fmaf(v3, xa[tt].w, p);
-              p = fmaf(v4, xb[tt].x, p);
-              p = fmaf(v5, xb[tt].y, p);
-              p = fmaf(v6, xb[tt].z, p);
-              p = fmaf(v7, xb[tt].w, p);
-              part[r][tt] = p;
-            }
-          }
-        }
+      for (int wd = 0; wd < 4; ++wd) {
+        float4 xa[kTB], xb[kTB];
 #pragma unroll
         for (int tt = 0; tt < kTB; ++tt) {
-          const int ti = (t0 + tt < n) ? t0 + tt : t0;
-          const float x136 = xs136[ti * G + g];
+          const float4* xp = xq + (size_t)tok[tt] * 8 * G + g;
+          xa[tt] = xp[(2 * wd) * G];
+          xb[tt] = xp[(2 * wd + 1) * G];
+        }
 #pragma unroll
-          for (int r = 0; r < 4; ++r) acc[r][tt] = fmaf(sc[r][j], part[r][tt] - x136, acc[r][tt]);
+        for (int m = 0; m < 2; ++m) {
+          uint32_t w32 = wd == 0 ? r.q[m][j].x : wd == 1 ? r.q[m][j].y : wd == 2 ? r.q[m][j].z : r.q[m][j].w;
+          asm volatile("" : "+r"(w32));  // keep the dequantisation inside the token loop
+          const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
+          const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+          const float v0 = v_lo(lo, 0), v1 = v_lo(hi, 0), v2 = v_lo(lo, 1), v3 = v_lo(hi, 1);
+          const float v4 = v_lo(lo, 2), v5 = v_lo(hi, 2), v6 = v_lo(lo, 3), v7 = v_lo(hi, 3);
+#pragma unroll
+          for (int tt = 0; tt < kTB; ++tt) {
+            float q = part[m][tt];
+            q = fmaf(v0, xa[tt].x, q);
+            q = fmaf(v1, xa[tt].y, q);
+            q = fmaf(v2, xa[tt].z, q);
+            q = fmaf(v3, xa[tt].w, q);
+            q = fmaf(v4, xb[tt].x, q);
+            q = fmaf(v5, xb[tt].y, q);
+            q = fmaf(v6, xb[tt].z, q);
+            q = fmaf(v7, xb[tt].w, q);
+            part[m][tt] = q;
+          }
         }
       }
+      const float2 sc = __half22float2(r.s[j]);
 #pragma unroll
       for (int tt = 0; tt < kTB; ++tt) {
-        if (t0 + tt >= n) continue;
-        float gsum[2], usum[2];
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          gsum[p] = warp_sum(acc[p][tt]);
-          usum[p] = warp_sum(acc[2 + p][tt]);
-        }
-        if (lane < 2) {
-          const float hv = silu(gsum[lane]) * usum[lane];
-          a.h[(size_t)asg_s[t0 + tt] * f + fi0 + lane] = hv;
-        }
+        const float x136 = xs136[tok[tt] * G + g];
+        acc[0][tt] = fmaf(sc.x, part[0][tt] - x136, acc[0][tt]);
+        acc[1][tt] = fmaf(sc.y, part[1][tt] - x136, acc[1][tt]);
       }
     }
+#pragma unroll
+    for (int tt = 0; tt < kTB; ++tt) {
+      if (t0 + tt >= n) continue;
+      const float gsum = warp_sum(acc[0][tt]);
+      const float usum = warp_sum(acc[1][tt]);
+      if (lane == 0) {
+        const int as = shared ? a.T * K + (t0 + tt) : perm_s[pbase + t0 + tt];
+        a.h[(size_t)as * f + i] = silu(gsum) * usum;
+      }
+    }
+  }
+}
+
+template <int NG>  // 32-column groups per lane per row (d = NG * 1024 at full width)
+__global__ void __launch_bounds__(kGuThreads, 1) gu_int4_kernel(ExpertArgs a) {
+  extern __shared__ float4 smem4[];
+  const int d = a.d, f = a.f, G = d / 32, T = a.T, K = a.K;
+  float4* xq = smem4;                                                     // [T][8][G] float4
+  float* xs136 = reinterpret_cast<float*>(smem4 + (size_t)T * 8 * G);     // [T][G]
+  int4* slot_s = reinterpret_cast<int4*>(xs136 + (size_t)T * G);          // [E]
+  int* perm_s = reinterpret_cast<int*>(slot_s + a.E);                     // [T*K]
+  __shared__ int n_act_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) n_act_s = *a.n_active;
+  for (int i = threadIdx.x; i < T * K; i += blockDim.x) perm_s[i] = a.perm[i];
+  __syncthreads();
+  const int n_act = n_act_s;
+  for (int i = threadIdx.x; i < n_act; i += blockDim.x) slot_s[i] = a.slots[i];
+  __syncthreads();
+  const int n_slots = n_act + a.has_shared;
+  const int Np = n_slots * f;
+  const int p0 = (int)((long long)Np * blockIdx.x / gridDim.x);
+  const int p1 = (int)((long long)Np * (blockIdx.x + 1) / gridDim.x);
+  PairRegs<NG> ra, rb;
+  int p = p0 + warp;
+  if (p < p1) gu_load_pair<NG>(a, slot_s, n_act, p, lane, ra);  // in flight while x is staged
+  // stage x' = 256 x for all tokens, group-interleaved, and 136 * group sums
+  for (int i = threadIdx.x; i < T * d; i += blockDim.x) {
+    const int ti = i / d, k = i - ti * d;
+    const float v = load_act(a.x, a.act, i) * 256.0f;
+    const int g = k >> 5, m = k & 31;
+    reinterpret_cast<float*>(xq)[(((size_t)ti * 8 + (m >> 2)) * G + g) * 4 + (m & 3)] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * G; i += blockDim.x) {
+    const int ti = i / G, g = i - ti * G;
+    const float* xb = reinterpret_cast<const float*>(xq) + (size_t)ti * 8 * G * 4;
+    float sx = 0.f;
+    for (int m = 0; m < 32; ++m) sx += xb[((m >> 2) * G + g) * 4 + (m & 3)];
+    xs136[i] = sx * (136.0f / 256.0f);
+  }
+  __syncthreads();
+  for (; p < p1; p += 2 * kGuW) {
+    const int pn = p + kGuW;
+    if (pn < p1) gu_load_pair<NG>(a, slot_s, n_act, pn, lane, rb);
+    gu_compute_pair<NG>(a, slot_s, perm_s, n_act, p, lane, xq, xs136, ra);
+    if (pn + kGuW < p1) gu_load_pair<NG>(a, slot_s, n_act, pn + kGuW, lane, ra);
+    if (pn < p1) gu_compute_pair<NG>(a, slot_s, perm_s, n_act, pn, lane, xq, xs136, rb);
   }
 }
 
@@ -224,30 +259,27 @@ __global__ void __launch_bounds__(256, 2) gu_int4_kernel(ExpertArgs a) {
 // One lane per 32-column group of h (f/32 <= 32 lanes active); 16 rows per block.
 // Shared memory: P [T*K + T][16] floats.
 __global__ void __launch_bounds__(kDnWarps * 32, 1) dn_int4_kernel(ExpertArgs a) {
-  extern __shared__ float P[];
-  __shared__ int tok_s[kDnWarps][kSmallT], asg_s[kDnWarps][kSmallT];
+  extern __shared__ float P[];  // [T*K + T][kDnRows], then slot table [E] int4, perm [T*K]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, f = a.f, G = f / 32, T = a.T, K = a.K;
+  int4* slot_s = reinterpret_cast<int4*>(P + (size_t)(T * K + T) * kDnRows);
+  int* perm_s = reinterpret_cast<int*>(slot_s + a.E);
+  __shared__ int n_act_s;
   const int j0 = blockIdx.x * kDnRows;
-  const int n_act = *a.n_active;
+  if (threadIdx.x == 0) n_act_s = *a.n_active;
+  for (int i = threadIdx.x; i < T * K; i += blockDim.x) perm_s[i] = a.perm[i];
+  __syncthreads();
+  const int n_act = n_act_s;
+  for (int i = threadIdx.x; i < n_act; i += blockDim.x) slot_s[i] = a.slots[i];
+  __syncthreads();
   const int n_slots = n_act + a.has_shared;
+  const bool on = lane < G;
   for (int s = warp; s < n_slots; s += kDnWarps) {
-    SlotInfo si;
-    if (lane == 0) si = slot_tokens(a, s, n_act, tok_s[warp], asg_s[warp]);
-    __syncwarp();
-    si.n = __shfl_sync(0xffffffffu, si.n, 0);
-    si.e = __shfl_sync(0xffffffffu, si.e, 0);
-    si.shared = __shfl_sync(0xffffffffu, (int)si.shared, 0);
-    const uint8_t* q;
-    const __half* sp;
-    if (si.shared) {
-      q = static_cast<const uint8_t*>(a.sh_dn_q);
-      sp = a.sh_dn_s;
-    } else {
-      q = static_cast<const uint8_t*>(a.dn_q) + (size_t)si.e * d * (f / 2);
-      sp = a.dn_s + (size_t)si.e * d * G;
-    }
-    const bool on = lane < G;
+    const bool shared = s >= n_act;
+    const int4 sl = shared ? make_int4(-1, 0, T, 0) : slot_s[s];
+    const uint8_t* q = shared ? static_cast<const uint8_t*>(a.sh_dn_q)
+                              : static_cast<const uint8_t*>(a.dn_q) + (size_t)sl.x * d * (f / 2);
+    const __half* sp = shared ? a.sh_dn_s : a.dn_s + (size_t)sl.x * d * G;
     uint4 wq[kDnRows];
     __half sch[kDnRows];
 #pragma unroll
@@ -260,8 +292,8 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) dn_int4_kernel(ExpertArgs a)
         sch[r] = __float2half(0.f);
       }
     }
-    for (int i = 0; i < si.n; ++i) {
-      const int as = asg_s[warp][i];
+    for (int i = 0; i < sl.z; ++i) {
+      const int as = shared ? T * K + i : perm_s[sl.y + i];
       float part[kDnRows];
 #pragma unroll
       for (int r = 0; r < kDnRows; ++r) part[r] = 0.f;
@@ -280,16 +312,16 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) dn_int4_kernel(ExpertArgs a)
           asm volatile("" : "+r"(w32));  // keep the dequantisation inside the token loop
           const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
           const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-          float p = part[r];
-          p = fmaf(v_lo(lo, 0), xa.x, p);
-          p = fmaf(v_lo(hi, 0), xa.y, p);
-          p = fmaf(v_lo(lo, 1), xa.z, p);
-          p = fmaf(v_lo(hi, 1), xa.w, p);
-          p = fmaf(v_lo(lo, 2), xb.x, p);
-          p = fmaf(v_lo(hi, 2), xb.y, p);
-          p = fmaf(v_lo(lo, 3), xb.z, p);
-          p = fmaf(v_lo(hi, 3), xb.w, p);
-          part[r] = p;
+          float pv = part[r];
+          pv = fmaf(v_lo(lo, 0), xa.x, pv);
+          pv = fmaf(v_lo(hi, 0), xa.y, pv);
+          pv = fmaf(v_lo(lo, 1), xa.z, pv);
+          pv = fmaf(v_lo(hi, 1), xa.w, pv);
+          pv = fmaf(v_lo(lo, 2), xb.x, pv);
+          pv = fmaf(v_lo(hi, 2), xb.y, pv);
+          pv = fmaf(v_lo(lo, 3), xb.z, pv);
+          pv = fmaf(v_lo(hi, 3), xb.w, pv);
+          part[r] = pv;
         }
       }
       const float h136 = hsum * 136.0f;
@@ -429,34 +461,38 @@ cudaError_t gemv_kernels_init(int num_sms) {
   return cudaSuccess;
 }
 
-size_t gemv_smem_gu(int wfmt, int T, int d) {
-  if (wfmt == kWInt4) return (size_t)T * 8 * (d / 32) * sizeof(float4) + (size_t)T * (d / 32) * sizeof(float);
+size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K) {
+  if (wfmt == kWInt4)
+    return (size_t)T * 8 * (d / 32) * sizeof(float4) + (size_t)T * (d / 32) * sizeof(float) + (size_t)E * sizeof(int4) +
+           (size_t)T * K * sizeof(int);
   return (size_t)T * d * sizeof(float);
 }
 
-size_t gemv_smem_dn(int T, int K) { return (size_t)(T * K + T) * kDnRows * sizeof(float); }
+size_t gemv_smem_dn(int T, int K, int E) {
+  return (size_t)(T * K + T) * kDnRows * sizeof(float) + (size_t)E * sizeof(int4) + (size_t)T * K * sizeof(int);
+}
 
 // Launches gate/up then down+combine for T <= kSmallT tokens.
 cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid) {
   const int dn_grid = (a.d + kDnRows - 1) / kDnRows;
-  const size_t sm_gu = gemv_smem_gu(wfmt, a.T, a.d);
-  const size_t sm_dn = gemv_smem_dn(a.T, a.K);
+  const size_t sm_gu = gemv_smem_gu(wfmt, a.T, a.d, a.E, a.K);
+  const size_t sm_dn = gemv_smem_dn(a.T, a.K, a.E);
   if (wfmt == kWInt4) {
     const int G = a.d / 32;
     const int ng = (G + 31) / 32;
-    const int grid = g_num_sms * (sm_gu <= 100 * 1024 ? 2 : 1);
+    const int grid = g_num_sms;
     switch (ng) {
-      case 1: gu_int4_kernel<1><<<grid, 256, sm_gu, st>>>(a); break;
-      case 2: gu_int4_kernel<2><<<grid, 256, sm_gu, st>>>(a); break;
-      case 3: gu_int4_kernel<3><<<grid, 256, sm_gu, st>>>(a); break;
-      case 4: gu_int4_kernel<4><<<grid, 256, sm_gu, st>>>(a); break;
+      case 1: gu_int4_kernel<1><<<grid, kGuThreads, sm_gu, st>>>(a); break;
+      case 2: gu_int4_kernel<2><<<grid, kGuThreads, sm_gu, st>>>(a); break;
+      case 3: gu_int4_kernel<3><<<grid, kGuThreads, sm_gu, st>>>(a); break;
+      case 4: gu_int4_kernel<4><<<grid, kGuThreads, sm_gu, st>>>(a); break;
       default: return cudaErrorInvalidValue;
     }
-    if (mid) cudaEventRecord(mid, st);
+    if (mid) cudaEventRecordWithFlags(mid, st, cudaEventRecordExternal);
     dn_int4_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
   } else {
     gu_f32_kernel<<<g_num_sms, 256, sm_gu, st>>>(a);
-    if (mid) cudaEventRecord(mid, st);
+    if (mid) cudaEventRecordWithFlags(mid, st, cudaEventRecordExternal);
     dn_f32_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
   }
   return cudaGetLastError();

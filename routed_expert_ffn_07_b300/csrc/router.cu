@@ -111,56 +111,36 @@ __device__ void topk_warp(const float* lg, int E, int K, int32_t* out_idx, float
   __syncwarp();
 }
 
-// Dispatch of n = T*K assignments held in shared memory (one block, any blockDim multiple of 32).
-// cnt: E ints of shared scratch.  Writes counts, offs, perm, active, n_active, stat.
-__device__ void dispatch_block(const int32_t* idx_s, int n, int E, int* cnt, int* scratch, const RouteArgs& a) {
-  const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[idx_s[i]], 1);
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) a.counts[e] = cnt[e];
-  __syncthreads();
-  const int total = block_exclusive_scan(cnt, E, scratch);  // cnt now holds offs
-  for (int e = tid; e < E; e += blockDim.x) a.offs[e] = cnt[e];
-  if (tid == 0) a.offs[E] = total;
-  // perm: rank of assignment i among the earlier assignments of the same expert
-  for (int i = tid; i < n; i += blockDim.x) {
-    const int e = idx_s[i];
-    int r = 0;
-    for (int j = 0; j < i; ++j) r += (idx_s[j] == e);
-    a.perm[cnt[e] + r] = i;
-  }
-  __syncthreads();
-  // active list: experts with a non-zero count, ascending
-  for (int e = tid; e < E; e += blockDim.x) cnt[e] = a.counts[e] > 0 ? 1 : 0;
-  __syncthreads();
-  const int nact = block_exclusive_scan(cnt, E, scratch);
-  for (int e = tid; e < E; e += blockDim.x)
-    if (a.counts[e] > 0) a.active[cnt[e]] = e;
-  if (tid == 0) {
-    *a.n_active = nact;
-    if (a.stat) *a.stat = nact;
-  }
-}
-
 // ------------------------------------------------------------------ small T (fused, one launch)
-// grid = ceil(E / 8) blocks of 256 threads; each warp scores one expert for all T tokens; the last
-// block to finish (ticket) runs softmax/top-K for every token and the dispatch.
-// Dynamic shared memory: T*d floats (activations) + 8*E floats (per-warp logit rows).
+// grid = ceil(E / 4) blocks of 256 threads; two warps score one expert (half a row each) for all T
+// tokens; the last block to finish (ticket) runs softmax/top-K for every token (logits held in
+// registers, one warp per token) and the dispatch, entirely from shared memory.
+// Dynamic shared memory: T*d floats (activations).
 __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
   extern __shared__ float smem[];
   float* xs = smem;                         // [T][d]
-  float* lgs = smem + (size_t)a.T * a.d;    // [8][E]
+  __shared__ float part[kRouterExpertsPerBlock][2][kSmallT];
   __shared__ int32_t idx_s[kSmallT * kMaxK];
-  __shared__ int32_t sidx[kRouterWarps][kMaxK];
-  __shared__ float sp[kRouterWarps][kMaxK];
+  __shared__ int cnt[kMaxE], offv[kMaxE], flag[kMaxE];
   __shared__ float inv_s[kSmallT];
   __shared__ int scratch[40];
   __shared__ int is_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = a.T, d = a.d, E = a.E, K = a.K;
 
+  const int e = blockIdx.x * kRouterExpertsPerBlock + (warp >> 1);
+  const int half = warp & 1;
+  const int nc = d >> 2;
+  const int hc = (nc + 1) >> 1;
+  const int cbeg = half ? hc : 0, cend = half ? nc : hc;
+  const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)(e < E ? e : 0) * d);
+  // the router row does not depend on x: start its loads before the activations are staged
+  float4 wv[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int c = cbeg + lane + 32 * i;
+    wv[i] = (e < E && c < cend) ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (a.prenorm) {
     for (int t = warp; t < T; t += kRouterWarps) {
       float ss = 0.f;
@@ -183,35 +163,48 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
   }
   __syncthreads();
 
-  const int e = blockIdx.x * kRouterWarps + warp;
-  if (e < E) {
+  {
     float acc[kSmallT];
 #pragma unroll
     for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
-    const float4* wr = reinterpret_cast<const float4*>(a.Wr + (size_t)e * d);
-    const int nc = d >> 2;
-#pragma unroll 4
-    for (int c = lane; c < nc; c += 32) {
-      const float4 wv = __ldg(wr + c);
+    for (int c0 = cbeg; c0 < cend; c0 += 32 * 16) {
+      if (c0 > cbeg) {
 #pragma unroll
-      for (int t = 0; t < kSmallT; ++t) {
-        if (t < T) {
-          const float4 xv = reinterpret_cast<const float4*>(xs + (size_t)t * d)[c];
-          acc[t] = fmaf(wv.x, xv.x, acc[t]);
-          acc[t] = fmaf(wv.y, xv.y, acc[t]);
-          acc[t] = fmaf(wv.z, xv.z, acc[t]);
-          acc[t] = fmaf(wv.w, xv.w, acc[t]);
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 + lane + 32 * i;
+          wv[i] = (e < E && c < cend) ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < cend) {
+#pragma unroll
+          for (int t = 0; t < kSmallT; ++t) {
+            if (t < T) {
+              const float4 xv = reinterpret_cast<const float4*>(xs + (size_t)t * d)[c];
+              acc[t] = fmaf(wv[i].x, xv.x, acc[t]);
+              acc[t] = fmaf(wv[i].y, xv.y, acc[t]);
+              acc[t] = fmaf(wv[i].z, xv.z, acc[t]);
+              acc[t] = fmaf(wv[i].w, xv.w, acc[t]);
+            }
+          }
         }
       }
     }
-    const float b = a.bias ? a.bias[e] : 0.f;
 #pragma unroll
     for (int t = 0; t < kSmallT; ++t) {
       if (t < T) {
         const float v = warp_sum(acc[t]);
-        if (lane == 0) a.logits[(size_t)t * E + e] = v + b;
+        if (lane == 0) part[warp >> 1][half][t] = v;
       }
     }
+  }
+  __syncthreads();
+  if (tid < kRouterExpertsPerBlock * T) {
+    const int le = tid / T, t = tid - le * T;
+    const int ee = blockIdx.x * kRouterExpertsPerBlock + le;
+    if (ee < E) a.logits[(size_t)t * E + ee] = (part[le][0][t] + part[le][1][t]) + (a.bias ? a.bias[ee] : 0.f);
   }
   __syncthreads();
   if (tid == 0) {
@@ -223,19 +216,94 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  // ---- last block: top-K per token (one warp per token)
-  float* lg = lgs + (size_t)warp * E;
+  // ---- last block: softmax + top-K per token, one warp per token, logits in registers
+  for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
   for (int t = warp; t < T; t += kRouterWarps) {
-    for (int j = lane; j < E; j += 32) lg[j] = __ldcg(a.logits + (size_t)t * E + j);
-    __syncwarp();
-    topk_warp(lg, E, K, a.idx + (size_t)t * K, a.w + (size_t)t * K, sidx[warp], sp[warp]);
-    if (lane < K) idx_s[t * K + lane] = sidx[warp][lane];
-    __syncwarp();
+    float lv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int ej = lane + 32 * j;
+      lv[j] = ej < E ? __ldcg(a.logits + (size_t)t * E + ej) : -INFINITY;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) m = fmaxf(m, lv[j]);
+    m = warp_max(m);
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (lane + 32 * j < E) z += expf(lv[j] - m);
+    z = warp_sum(z);
+    uint32_t taken = 0u;
+    float psum = 0.f, my_p = 0.f;
+    int my_i = 0;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int ej = lane + 32 * j;
+        if (ej < E && !((taken >> j) & 1u) && (bi == 0x7fffffff || lv[j] > bv)) {
+          bv = lv[j];
+          bi = ej;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float p = expf(bv - m) / z;
+      if (lane == k) {
+        my_i = bi;
+        my_p = p;
+      }
+      psum += p;
+    }
+    if (lane < K) {
+      a.idx[(size_t)t * K + lane] = my_i;
+      a.w[(size_t)t * K + lane] = my_p / psum;
+      idx_s[t * K + lane] = my_i;
+    }
   }
   __syncthreads();
-  int* cnt = reinterpret_cast<int*>(lgs);  // reuse (E ints)
-  dispatch_block(idx_s, T * K, E, cnt, scratch, a);
-  if (tid == 0) *a.ticket = 0u;
+  // ---- dispatch (shared memory only)
+  const int n = T * K;
+  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[idx_s[i]], 1);
+  __syncthreads();
+  for (int i = tid; i < E; i += blockDim.x) {
+    const int c = cnt[i];
+    a.counts[i] = c;
+    offv[i] = c;
+    flag[i] = c > 0 ? 1 : 0;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(offv, E, scratch);
+  const int nact = block_exclusive_scan(flag, E, scratch);
+  for (int i = tid; i < E; i += blockDim.x) {
+    a.offs[i] = offv[i];
+    if (cnt[i] > 0) {
+      a.active[flag[i]] = i;
+      a.slots[flag[i]] = make_int4(i, offv[i], cnt[i], 0);
+    }
+  }
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int ei = idx_s[i];
+    int r = 0;
+    for (int j = 0; j < i; ++j) r += (idx_s[j] == ei);
+    a.perm[offv[ei] + r] = i;
+  }
+  if (tid == 0) {
+    a.offs[E] = total;
+    *a.n_active = nact;
+    if (a.stat) *a.stat = nact;
+    *a.ticket = 0u;
+  }
 }
 
 // ------------------------------------------------------------------ large T
@@ -362,7 +430,10 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(RouteArgs a, int nb
   __syncthreads();
   const int nact = block_exclusive_scan(vals, E, scratch);
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (a.counts[e] > 0) a.active[vals[e]] = e;
+    if (a.counts[e] > 0) {
+      a.active[vals[e]] = e;
+      a.slots[vals[e]] = make_int4(e, a.offs[e], a.counts[e], 0);
+    }
   if (threadIdx.x == 0) {
     *a.n_active = nact;
     if (a.stat) *a.stat = nact;
@@ -386,12 +457,12 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(RouteA
 }
 
 // ------------------------------------------------------------------ host-side launchers
-size_t route_small_smem(int T, int d, int E) { return ((size_t)T * d + (size_t)kRouterWarps * E) * sizeof(float); }
+size_t route_small_smem(int T, int d, int E) { return (size_t)T * d * sizeof(float); }
 
 cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t st) {
   if (a.T <= kSmallT && (size_t)a.T * a.d * 4 <= 160 * 1024) {
     const size_t sm = route_small_smem(a.T, a.d, a.E);
-    const int grid = (a.E + kRouterWarps - 1) / kRouterWarps;
+    const int grid = (a.E + kRouterExpertsPerBlock - 1) / kRouterExpertsPerBlock;
     route_small_kernel<<<grid, 256, sm, st>>>(a);
     return cudaGetLastError();
   }
