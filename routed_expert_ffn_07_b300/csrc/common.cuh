@@ -48,6 +48,25 @@ __device__ __forceinline__ void store_act(void* p, int act, size_t i, float v) {
     static_cast<float*>(p)[i] = v;
 }
 
+// 8 consecutive activations starting at element i (i % 8 == 0, 16-byte aligned base): one 16-byte
+// load for bf16, two for fp32.
+__device__ __forceinline__ void load8_act(const void* p, int act, size_t i, float (&v)[8]) {
+  if (act == kActBf16) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
 // Value of v after rounding to the activation type.
 __device__ __forceinline__ float round_act(int act, float v) {
   return act == kActBf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;

@@ -231,11 +231,25 @@ __global__ void __launch_bounds__(kGuThreads, 1) gu_int4_kernel(ExpertArgs a) {
   int p = p0 + warp;
   if (p < p1) gu_load_pair<NG>(a, slot_s, n_act, p, lane, ra);  // in flight while x is staged
   // stage x' = 256 x for all tokens, group-interleaved, and 136 * group sums
-  for (int i = threadIdx.x; i < T * d; i += blockDim.x) {
-    const int ti = i / d, k = i - ti * d;
-    const float v = load_act(a.x, a.act, i) * 256.0f;
-    const int g = k >> 5, m = k & 31;
-    reinterpret_cast<float*>(xq)[(((size_t)ti * 8 + (m >> 2)) * G + g) * 4 + (m & 3)] = v;
+  const int nch = T * d / 8;
+  for (int c0 = threadIdx.x; c0 < nch; c0 += 4 * blockDim.x) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * blockDim.x;
+      if (c < nch) load8_act(a.x, a.act, (size_t)c * 8, v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * blockDim.x;
+      if (c < nch) {
+        const int ti = (c * 8) / d, k = c * 8 - ti * d;
+        const int g = k >> 5, m4 = (k & 31) >> 2;
+        float4* dst = xq + ((size_t)ti * 8 + m4) * G + g;
+        dst[0] = make_float4(v[u][0] * 256.f, v[u][1] * 256.f, v[u][2] * 256.f, v[u][3] * 256.f);
+        dst[G] = make_float4(v[u][4] * 256.f, v[u][5] * 256.f, v[u][6] * 256.f, v[u][7] * 256.f);
+      }
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < T * G; i += blockDim.x) {
@@ -281,38 +295,41 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) dn_int4_kernel(ExpertArgs a)
                               : static_cast<const uint8_t*>(a.dn_q) + (size_t)sl.x * d * (f / 2);
     const __half* sp = shared ? a.sh_dn_s : a.dn_s + (size_t)sl.x * d * G;
     uint4 wq[kDnRows];
-    __half sch[kDnRows];
+    __half2 sch[kDnRows / 2];  // scales of rows (2r, 2r+1)
 #pragma unroll
-    for (int r = 0; r < kDnRows; ++r) {
-      if (on) {
-        wq[r] = ldg_nc_v4(q + (size_t)(j0 + r) * (f / 2) + lane * 16);
-        sch[r] = sp[(size_t)(j0 + r) * G + lane];
-      } else {
-        wq[r] = make_uint4(0, 0, 0, 0);
-        sch[r] = __float2half(0.f);
-      }
-    }
+    for (int r = 0; r < kDnRows; ++r)
+      wq[r] = on ? ldg_nc_v4(q + (size_t)(j0 + r) * (f / 2) + lane * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kDnRows; r += 2)
+      sch[r / 2] = on ? __halves2half2(sp[(size_t)(j0 + r) * G + lane], sp[(size_t)(j0 + r + 1) * G + lane])
+                      : __float2half2_rn(0.f);
     for (int i = 0; i < sl.z; ++i) {
       const int as = shared ? T * K + i : perm_s[sl.y + i];
-      float part[kDnRows];
-#pragma unroll
-      for (int r = 0; r < kDnRows; ++r) part[r] = 0.f;
-      float hsum = 0.f;
+      // the token's 32 h values of this lane's group, all loads issued together
+      float4 hv[8];
       const float4* hp = reinterpret_cast<const float4*>(a.h + (size_t)as * f + (on ? lane : 0) * 32);
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        float4 xa = on ? __ldcg(hp + 2 * wd) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 xb = on ? __ldcg(hp + 2 * wd + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-        hsum += ((xa.x + xa.y) + (xa.z + xa.w)) + ((xb.x + xb.y) + (xb.z + xb.w));
-        xa.x *= 256.f; xa.y *= 256.f; xa.z *= 256.f; xa.w *= 256.f;
-        xb.x *= 256.f; xb.y *= 256.f; xb.z *= 256.f; xb.w *= 256.f;
+      for (int m = 0; m < 8; ++m) hv[m] = on ? __ldcg(hp + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float hsum = 0.f;
 #pragma unroll
-        for (int r = 0; r < kDnRows; ++r) {
+      for (int m = 0; m < 8; ++m) {
+        hsum += (hv[m].x + hv[m].y) + (hv[m].z + hv[m].w);
+        hv[m].x *= 256.f;
+        hv[m].y *= 256.f;
+        hv[m].z *= 256.f;
+        hv[m].w *= 256.f;
+      }
+      const float h136 = hsum * 136.0f;
+#pragma unroll
+      for (int r = 0; r < kDnRows; ++r) {
+        float pv = 0.f;
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
           uint32_t w32 = wd == 0 ? wq[r].x : wd == 1 ? wq[r].y : wd == 2 ? wq[r].z : wq[r].w;
           asm volatile("" : "+r"(w32));  // keep the dequantisation inside the token loop
           const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
           const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-          float pv = part[r];
+          const float4 xa = hv[2 * wd], xb = hv[2 * wd + 1];
           pv = fmaf(v_lo(lo, 0), xa.x, pv);
           pv = fmaf(v_lo(hi, 0), xa.y, pv);
           pv = fmaf(v_lo(lo, 1), xa.z, pv);
@@ -321,13 +338,9 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) dn_int4_kernel(ExpertArgs a)
           pv = fmaf(v_lo(hi, 2), xb.y, pv);
           pv = fmaf(v_lo(lo, 3), xb.z, pv);
           pv = fmaf(v_lo(hi, 3), xb.w, pv);
-          part[r] = pv;
         }
-      }
-      const float h136 = hsum * 136.0f;
-#pragma unroll
-      for (int r = 0; r < kDnRows; ++r) {
-        const float pr = on ? __half2float(sch[r]) * (part[r] - h136) : 0.f;
+        const float sr = (r & 1) ? __high2float(sch[r / 2]) : __low2float(sch[r / 2]);
+        const float pr = on ? sr * (pv - h136) : 0.f;
         const float o = warp_sum(pr);
         if (lane == 0) P[(size_t)as * kDnRows + r] = o;
       }

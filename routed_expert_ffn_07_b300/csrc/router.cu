@@ -111,6 +111,27 @@ __device__ void topk_warp(const float* lg, int E, int K, int32_t* out_idx, float
   __syncwarp();
 }
 
+// Descending bitonic sort of the first N entries of kv (N a power of two), fully unrolled.
+template <int N>
+__device__ __forceinline__ void bitonic_desc(uint64_t (&kv)[32]) {
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t x0 = kv[i], x1 = kv[ixj];
+          const bool sw = ((i & k) == 0) ? (x0 < x1) : (x0 > x1);
+          kv[i] = sw ? x1 : x0;
+          kv[ixj] = sw ? x0 : x1;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ small T (fused, one launch)
 // grid = ceil(E / 4) blocks of 256 threads; two warps score one expert (half a row each) for all T
 // tokens; the last block to finish (ticket) runs softmax/top-K for every token (logits held in
@@ -141,25 +162,55 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
     const int c = cbeg + lane + 32 * i;
     wv[i] = (e < E && c < cend) ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  const int nch = T * d / 8;  // 8-activation chunks, loaded 16 bytes at a time
   if (a.prenorm) {
+    // sum of squares per token: one warp per token, a lane's chunks loaded together
     for (int t = warp; t < T; t += kRouterWarps) {
       float ss = 0.f;
-      for (int j = lane; j < d; j += 32) {
-        const float v = load_act(a.x, a.act, (size_t)t * d + j);
-        ss += v * v;
+      for (int c0 = 0; c0 < d / 8; c0 += 32 * 8) {
+        float v[8][8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (c < d / 8) load8_act(a.x, a.act, (size_t)t * d + c * 8, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (c0 + lane + 32 * u < d / 8) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ss = fmaf(v[u][q], v[u][q], ss);
+          }
+        }
       }
       ss = warp_sum(ss);
       if (lane == 0) inv_s[t] = 1.0f / sqrtf(ss / (float)d + a.eps);
     }
     __syncthreads();
   }
-  for (int i = tid; i < T * d; i += blockDim.x) {
-    float v = load_act(a.x, a.act, i);
-    if (a.prenorm) {
-      v = round_act(a.act, v * inv_s[i / d]);
-      if (blockIdx.x == 0) store_act(a.xnorm, a.act, i, v);
+  for (int c0 = tid; c0 < nch; c0 += 4 * blockDim.x) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * blockDim.x;
+      if (c < nch) load8_act(a.x, a.act, (size_t)c * 8, v[u]);
     }
-    xs[i] = v;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * blockDim.x;
+      if (c < nch) {
+        if (a.prenorm) {
+          const float inv = inv_s[(c * 8) / d];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            v[u][q] = round_act(a.act, v[u][q] * inv);
+            if (blockIdx.x == 0) store_act(a.xnorm, a.act, (size_t)c * 8 + q, v[u][q]);
+          }
+        }
+        float4* xp = reinterpret_cast<float4*>(xs + (size_t)c * 8);
+        xp[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+        xp[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+      }
+    }
   }
   __syncthreads();
 
@@ -216,55 +267,55 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  // ---- last block: softmax + top-K per token, one warp per token, logits in registers
+  // ---- last block: softmax + top-K per token, one warp per token.  Each lane sorts its (up to 32)
+  // logits once; a round then takes the warp maximum of the lanes' heads with two redux
+  // reductions (largest order-preserving key, then lowest expert index among equal keys).
   for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
   for (int t = warp; t < T; t += kRouterWarps) {
-    float lv[32];
+    uint64_t kv[32];  // (order-preserving key of the logit) << 32 | (31 - j); larger = better
+    float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int ej = lane + 32 * j;
-      lv[j] = ej < E ? __ldcg(a.logits + (size_t)t * E + ej) : -INFINITY;
+      const float v = ej < E ? __ldcg(a.logits + (size_t)t * E + ej) : -INFINITY;
+      m = fmaxf(m, v);
+      const uint32_t u = __float_as_uint(v);
+      const uint32_t key = ej < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+      kv[j] = ((uint64_t)key << 32) | (uint32_t)(31 - j);
     }
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) m = fmaxf(m, lv[j]);
     m = warp_max(m);
     float z = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (lane + 32 * j < E) z += expf(lv[j] - m);
+    for (int j = 0; j < 32; ++j) {
+      const int ej = lane + 32 * j;
+      if (ej < E) z += expf(__ldcg(a.logits + (size_t)t * E + ej) - m);
+    }
     z = warp_sum(z);
-    uint32_t taken = 0u;
-    float psum = 0.f, my_p = 0.f;
+    // descending sort of the lane's keys (bitonic network; 16 keys per lane when E <= 512)
+    if (E <= 512)
+      bitonic_desc<16>(kv);
+    else
+      bitonic_desc<32>(kv);
+    int head = 0;
     int my_i = 0;
     for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
+      uint64_t hk = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int ej = lane + 32 * j;
-        if (ej < E && !((taken >> j) & 1u) && (bi == 0x7fffffff || lv[j] > bv)) {
-          bv = lv[j];
-          bi = ej;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float p = expf(bv - m) / z;
-      if (lane == k) {
-        my_i = bi;
-        my_p = p;
-      }
-      psum += p;
+      for (int j = 0; j < 32; ++j)
+        if (j == head) hk = kv[j];
+      const uint32_t key = (uint32_t)(hk >> 32);
+      const uint32_t best = __reduce_max_sync(0xffffffffu, key);
+      const int e_mine = lane + 32 * (31 - (int)(hk & 31u));
+      const uint32_t cand = (key == best && key != 0u) ? (uint32_t)e_mine : 0xffffffffu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      if (lane == (int)(win & 31u)) ++head;
+      if (lane == k) my_i = (int)win;
     }
+    // probabilities of the kept experts, renormalised in ascending k
+    float my_p = 0.f;
+    if (lane < K) my_p = expf(__ldcg(a.logits + (size_t)t * E + my_i) - m) / z;
+    float psum = 0.f;
+    for (int k = 0; k < K; ++k) psum += __shfl_sync(0xffffffffu, my_p, k);
     if (lane < K) {
       a.idx[(size_t)t * K + lane] = my_i;
       a.w[(size_t)t * K + lane] = my_p / psum;
