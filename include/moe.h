@@ -160,6 +160,26 @@ moe_status moe_timing_enable(moe_handle h, int n_records);
 moe_status moe_timing_rewind(moe_handle h);
 moe_status moe_timing_read(moe_handle h, float* ms, int max_records, int* n_records, void* stream);
 
+/* Routing without any allocation, for callers that cannot call cudaMalloc: code that runs while a
+ * stream is being captured into a CUDA graph owned by another framework (allocating there is not
+ * allowed), code that must stay inside a memory pool it was given, or latency-critical host
+ * threads that cannot afford the device synchronisation cudaMalloc may cause.  The pages describe
+ * no counterpart of this call: it exists only for such callers.
+ * It computes exactly what moe_route computes (router + softmax + top-K + dispatch, no RMSNorm)
+ * from plain pointers, without a handle: router_w fp32 [E][d], router_b fp32 [E] or NULL, x [T][d]
+ * of type `act`; outputs as in moe_route (each may be NULL).  Its scratch (logits, counts, slot
+ * table, ticket; 121,600 bytes) is one fixed device array inside this library, so it supports at
+ * most T = 16 tokens, E = 1024 experts, K = 32 and T*d*4 <= 163,840 bytes; larger sizes return
+ * MOE_ERR_UNSUPPORTED and launch nothing.  Every GPU that loads the library holds that array until
+ * the process exits.  All calls on a device share it, so calls that overlap on the GPU (different
+ * streams, or threads without ordering) race and give wrong results; the array keeps the last
+ * call's contents.  The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  No cudaMalloc, cudaFree or
+ * allocating library call is made. */
+moe_status moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int act, int T, int d,
+                             int E, int K, int32_t* topk_idx, float* topk_w, int32_t* expert_offs, int32_t* perm,
+                             void* stream);
+
 const char* moe_status_str(moe_status s);
 int moe_version(void);
 

@@ -54,6 +54,7 @@ def _load():
         "moe_get_active_counts": ([vp, i32p, vp], ci),
         "moe_get_device_status": ([vp, vp], ci),
         "moe_destroy": ([vp], ci),
+        "moe_route_noalloc": ([vp, vp, vp, ci, ci, ci, ci, ci, i32p, vp, i32p, i32p, vp], ci),
         "moe_timing_enable": ([vp, ci], ci),
         "moe_timing_rewind": ([vp], ci),
         "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
@@ -116,6 +117,14 @@ def moe_set_layer(h, layer, router_w, gu_q, gu_s, dn_q, dn_s, router_b=None, sh_
 def moe_route(h, layer, x, T, topk_idx=None, topk_w=None, expert_offs=None, perm=None, stream=None):
     _check("moe_route", lib.moe_route(h, layer, _ptr(x), T, _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offs),
                                       _ptr(perm), _stream(stream)))
+
+
+def moe_route_noalloc(router_w, router_b, x, act, T, d, E, K, topk_idx=None, topk_w=None, expert_offs=None,
+                      perm=None, stream=None):
+    """Routing that allocates nothing (fixed device scratch inside the library); see include/moe.h."""
+    _check("moe_route_noalloc", lib.moe_route_noalloc(_ptr(router_w), _ptr(router_b), _ptr(x), act, T, d, E, K,
+                                                      _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offs), _ptr(perm),
+                                                      _stream(stream)))
 
 
 def moe_layer_forward(h, layer, x, T, y, stream=None):

@@ -11,6 +11,9 @@
 // Arithmetic: logits in fp32 (FMA, fixed per-lane order + fixed shuffle tree), softmax over all E
 // logits with expf, K rounds of warp arg-max (larger logit first, ties to the lower index), the
 // kept probabilities renormalised.  Selection compares fp32 logits.
+#include <mutex>
+
+#include "../../include/moe.h"
 #include "common.cuh"
 
 namespace moe {
@@ -537,4 +540,85 @@ cudaError_t route_kernels_init() {
   return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
 }
 
+// ------------------------------------------------------------------ routing without allocation
+// Scratch of moe_route_noalloc: one file-scope device array, shared by every call on a device.
+// Layout (bytes): logits [16][1024] fp32 | idx [16*32] | w [16*32] | perm [16*32] | counts [1024] |
+// offs [1025] | active [1024] | slots [1024] int4 | n_active | ticket | status.
+namespace {
+constexpr int kNaMaxT = kSmallT, kNaMaxE = kMaxE, kNaMaxK = kMaxK;
+constexpr size_t kNaLogits = 0;
+constexpr size_t kNaIdx = kNaLogits + (size_t)kNaMaxT * kNaMaxE * 4;
+constexpr size_t kNaW = kNaIdx + (size_t)kNaMaxT * kNaMaxK * 4;
+constexpr size_t kNaPerm = kNaW + (size_t)kNaMaxT * kNaMaxK * 4;
+constexpr size_t kNaCounts = kNaPerm + (size_t)kNaMaxT * kNaMaxK * 4;
+constexpr size_t kNaOffs = kNaCounts + (size_t)kNaMaxE * 4;
+constexpr size_t kNaActive = kNaOffs + 256 * (((size_t)(kNaMaxE + 1) * 4 + 255) / 256);
+constexpr size_t kNaSlots = kNaActive + (size_t)kNaMaxE * 4;
+constexpr size_t kNaNActive = kNaSlots + (size_t)kNaMaxE * 16;
+constexpr size_t kNaTicket = kNaNActive + 256;
+constexpr size_t kNaStatus = kNaTicket + 256;
+constexpr size_t kNaBytes = kNaStatus + 256;  // 121,600 bytes
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_route_scratch[kNaBytes];
+
 }  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int act, int T,
+                                        int d, int E, int K, int32_t* topk_idx, float* topk_w, int32_t* expert_offs,
+                                        int32_t* perm, void* stream) {
+  using namespace moe;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!router_w || !x || !a16(router_w) || !a16(x) || (router_b && !a16(router_b))) return MOE_ERR_INVALID_ARG;
+  if (act != MOE_ACT_BF16 && act != MOE_ACT_F32) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || d < 8 || d % 8 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARG;
+  // beyond the fixed scratch: at most 16 tokens, 1024 experts, top-32, and T*d*4 <= 160 KB
+  if (T > kNaMaxT || E > kNaMaxE || K > kNaMaxK || (size_t)T * d * 4 > 160 * 1024) return MOE_ERR_UNSUPPORTED;
+
+  // per-device set-up: the device address of the scratch array (and kernel attributes)
+  static std::mutex mu;
+  static void* base[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  unsigned char* sc;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+      if (route_kernels_init() != cudaSuccess) return MOE_ERR_CUDA;
+      base[dev] = p;
+    }
+    sc = static_cast<unsigned char*>(base[dev]);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteArgs a;
+  a.x = x;
+  a.act = act;
+  a.T = T;
+  a.d = d;
+  a.E = E;
+  a.K = K;
+  a.Wr = router_w;
+  a.bias = router_b;
+  a.prenorm = 0;
+  a.eps = 0.f;
+  a.xnorm = nullptr;
+  a.logits = reinterpret_cast<float*>(sc + kNaLogits);
+  a.idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(sc + kNaIdx);
+  a.w = topk_w ? topk_w : reinterpret_cast<float*>(sc + kNaW);
+  a.perm = perm ? perm : reinterpret_cast<int32_t*>(sc + kNaPerm);
+  a.counts = reinterpret_cast<int32_t*>(sc + kNaCounts);
+  a.offs = expert_offs ? expert_offs : reinterpret_cast<int32_t*>(sc + kNaOffs);
+  a.active = reinterpret_cast<int32_t*>(sc + kNaActive);
+  a.slots = reinterpret_cast<int4*>(sc + kNaSlots);
+  a.n_active = reinterpret_cast<int32_t*>(sc + kNaNActive);
+  a.stat = nullptr;
+  a.blockhist = nullptr;
+  a.ticket = reinterpret_cast<unsigned*>(sc + kNaTicket);
+  a.status = reinterpret_cast<unsigned*>(sc + kNaStatus);
+  // the last-block ticket must start at zero
+  if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(a, 1, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -80,3 +80,17 @@ def test_null_handles_rejected(lib):
 def test_generator_rejects_bad_args(lib):
     assert lib.lib.moe_gen_int4_planes(None, 1, 0, 0, 0, 1, 16, None) == 1
     assert lib.lib.moe_gen_int4_planes(ctypes.c_void_p(16), 1, 0, 0, 0, 1, 12, None) == 1
+
+
+def test_noalloc_route_validates_before_touching_the_device(lib):
+    L = lib.lib
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    # T beyond the fixed scratch, E beyond it, K beyond it: unsupported; bad pointers / sizes: invalid
+    assert L.moe_route_noalloc(p, None, p, 1, 17, 256, 8, 2, None, None, None, None, None) == 2
+    assert L.moe_route_noalloc(p, None, p, 1, 4, 256, 2048, 2, None, None, None, None, None) == 2
+    assert L.moe_route_noalloc(p, None, p, 1, 4, 256, 64, 33, None, None, None, None, None) == 2
+    assert L.moe_route_noalloc(None, None, p, 1, 4, 256, 8, 2, None, None, None, None, None) == 1
+    assert L.moe_route_noalloc(p + 2, None, p, 1, 4, 256, 8, 2, None, None, None, None, None) == 1
+    assert L.moe_route_noalloc(p, None, p, 1, 4, 250, 8, 2, None, None, None, None, None) == 1
+    assert L.moe_route_noalloc(p, None, p, 7, 4, 256, 8, 2, None, None, None, None, None) == 1
