@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark of the routed MoE FFN layer on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--extras]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
 
 Default workload: one full-size decode layer (T=1 token, d=2048, 512 experts + 1 shared expert,
 top-10, SwiGLU f=768, int4 group-32 weights with fp16 scales, bf16 activations, fp32 router).
@@ -161,7 +161,7 @@ def cpu_baseline_decode(wl, budget_s=12.0, max_layers=48):
                       f"{spent:.1f} s of oracle time"}
 
 
-def measure_decode_layer(wl, steps, warmup, rank, world, extras):
+def measure_decode_layer(wl, steps, warmup, rank, world):
     import torch
     from routed_expert_ffn_07_b300 import capi
     from routed_expert_ffn_07_b300.workloads import alloc_and_fill, create_handle, expert_bytes
@@ -219,7 +219,9 @@ def measure_decode_layer(wl, steps, warmup, rank, world, extras):
     for _ in range(max(3, min(steps, 20))):
         g2.replay()
         stage.append(capi.moe_timing_read(h, L, torch.cuda.current_stream().cuda_stream))
-    stage = np.concatenate(stage)  # [reps*L, 3]
+    stage = np.concatenate(stage)  # [reps*L, 4]
+    del g2  # the graph records the timing events: release it before the events
+    torch.cuda.synchronize()
     capi.moe_timing_enable(h, 0)
 
     gu_bytes = 2 * f * d // 2 + 2 * f * (d // 32) * 2
@@ -228,7 +230,7 @@ def measure_decode_layer(wl, steps, warmup, rank, world, extras):
     act_b = T * d * 2
     bytes_gu = float(np.mean(slots)) * gu_bytes + act_b           # per launch of the gate/up kernel
     bytes_layer = float(np.mean(slots)) * expert_bytes(d, f) + 2 * act_b
-    ms_route, ms_gu, ms_dn = (float(v) for v in stage.mean(axis=0))
+    ms_route, ms_gu, ms_dn, _ = (float(v) for v in stage.mean(axis=0))
     pk, src = peaks()
     hbm = float(pk["hbm_gbs"])
     ms_step = t_max / steps
@@ -266,19 +268,20 @@ def measure_decode_layer(wl, steps, warmup, rank, world, extras):
                   "d2h_bytes_per_step": T * d * 2,
                   "step": "one moe_layer_forward_host call (pinned host x in, host y out, synchronised)"}
     capi.moe_destroy(h)
-    del wts, g, g2
+    del wts, g
     torch.cuda.empty_cache()
     return res
 
 
 def run_profile_case(args):
-    """Small case for ncu: the decode layer over 2 layers' weights (about 2.7 GB on the device),
-    `warmup` + `steps` graph replays, nothing else.  Not a benchmark line."""
+    """Small case for ncu, not a benchmark line: `--profile decode` runs the decode layer over 2
+    layers' weights (about 2.7 GB on the device); `--profile prefill` runs the 4096-token prefill
+    layer (about 1.7 GB).  `warmup` + `steps` layer calls, nothing else."""
     import torch
     from routed_expert_ffn_07_b300 import capi, inputs
     from routed_expert_ffn_07_b300.workloads import WORKLOADS, alloc_and_fill, create_handle
-    wl = WORKLOADS[2]
-    L = 2
+    wl = WORKLOADS[4] if args.profile == "prefill" else WORKLOADS[2]
+    L = 1 if args.profile == "prefill" else 2
     wts = alloc_and_fill(wl, n_layers=L)
     h = create_handle(wl, wts, max_tokens=wl.T, n_layers=L, prenorm=False)
     x_np = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)
@@ -292,6 +295,92 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": wl.name, "layers": L, "calls": args.warmup + args.steps}))
 
 
+def measure_prefill(wl, steps, warmup):
+    """Prefill chunk through one layer (tensor-core path); cold L2: 1.36 GB of weights per call."""
+    import torch
+    from routed_expert_ffn_07_b300 import capi, inputs
+    from routed_expert_ffn_07_b300.workloads import alloc_and_fill, create_handle, expert_bytes
+    wts = alloc_and_fill(wl)
+    h = create_handle(wl, wts)
+    T, d, f, K = wl.T, wl.d, wl.f, wl.K
+    x_np = inputs.gen_activations(wl.seed, T, d, wl.act)
+    x = torch.from_numpy(x_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    for _ in range(warmup):
+        capi.moe_layer_forward(h, 0, x, T, y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        capi.moe_layer_forward(h, 0, x, T, y)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    capi.moe_timing_enable(h, steps)
+    for _ in range(steps):
+        capi.moe_layer_forward(h, 0, x, T, y)
+    st = capi.moe_timing_read(h, steps).mean(axis=0)
+    capi.moe_timing_enable(h, 0)
+    assert capi.moe_get_device_status(h) == 0
+    n_act = int(capi.moe_get_active_counts(h, 1)[0])
+    capi.moe_destroy(h)
+    del wts
+    torch.cuda.empty_cache()
+    rows = T * K + (T if wl.shared else 0)
+    flops = 2.0 * rows * 3 * d * f
+    gemm_ms = float(st[1] + st[2])
+    pk, src = peaks()
+    peak_tf = float(pk["bf16_tflops"])  # fp16 and bf16 dense tensor rates are equal (same MMA kind)
+    wbytes = (n_act + (1 if wl.shared else 0)) * expert_bytes(d, f)
+    return {"workload": wl.name, "value": T / (ms * 1e-3), "unit": "tokens/s", "ms_per_layer": ms,
+            "stage_ms": {"route": float(st[0]), "gemm1_incl_staging": float(st[1]), "gemm2": float(st[2]),
+                         "combine": float(st[3])},
+            "grouped_gemm": {"flops": flops, "ms": gemm_ms, "tflops": flops / (gemm_ms * 1e-3) / 1e12,
+                             "frac_of_" + src + "_tensor_peak": flops / (gemm_ms * 1e-3) / 1e12 / peak_tf,
+                             "peak_tflops": peak_tf, "operands": "fp16 x fp16 -> fp32 (tcgen05 kind::f16)"},
+            "weights_gb_per_s": wbytes / (ms * 1e-3) / 1e9, "distinct_experts": n_act}
+
+
+def measure_stack(wl, steps, warmup):
+    """48-layer stack (verify / skewed decode), one CUDA graph per call."""
+    import torch
+    from routed_expert_ffn_07_b300 import capi, inputs
+    from routed_expert_ffn_07_b300.workloads import alloc_and_fill, create_handle, expert_bytes
+    wts = alloc_and_fill(wl)
+    h = create_handle(wl, wts)
+    T, d, f, L = wl.T, wl.d, wl.f, wl.layers
+    x_np = inputs.gen_activations(wl.seed, T, d, wl.act)
+    x0 = torch.from_numpy(x_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    x = x0.clone()
+    for _ in range(warmup):
+        x.copy_(x0)
+        capi.moe_stack_forward(h, x, T)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        capi.moe_stack_forward(h, x, T)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    assert capi.moe_get_device_status(h) == 0
+    x.copy_(x0)
+    capi.moe_stack_forward(h, x, T)
+    counts = capi.moe_get_active_counts(h, L)
+    capi.moe_destroy(h)
+    del wts
+    torch.cuda.empty_cache()
+    bytes_step = float(np.sum(counts + 1)) * expert_bytes(d, f) + L * 2 * T * d * 2
+    pk, src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    return {"workload": wl.name, "value": T * L / (ms * 1e-3), "unit": "MoE-layer tokens/s",
+            "ms_per_step": ms, "tokens_per_step": T,
+            "hbm": {"algorithmic_bytes_per_step": bytes_step, "gb_per_s": bytes_step / (ms * 1e-3) / 1e9,
+                    "frac_of_" + src: bytes_step / (ms * 1e-3) / 1e9 / hbm},
+            "distinct_experts_per_layer": {"mean": float(np.mean(counts)), "min": int(counts.min()),
+                                           "max": int(counts.max())}}
+
+
 def run_ours(args):
     rank, world, local = dist_init(args.gpus)
     import torch
@@ -301,7 +390,7 @@ def run_ours(args):
     barrier(world)
     from routed_expert_ffn_07_b300.workloads import WORKLOADS
     wl = WORKLOADS[2]
-    res = measure_decode_layer(wl, args.steps, args.warmup, rank, world, args.extras)
+    res = measure_decode_layer(wl, args.steps, args.warmup, rank, world)
     line = {
         "metric": METRIC,
         "value": res["value"],
@@ -325,6 +414,13 @@ def run_ours(args):
         "e2e": res["e2e"],
         "gpu_launches": res["gpu_launches"],
     }
+    if not args.no_extras:
+        steps_x = max(3, min(args.steps, 10))
+        line["workloads"] = {
+            "prefill": measure_prefill(WORKLOADS[4], steps_x, args.warmup),
+            "verify_stack": measure_stack(WORKLOADS[3], steps_x, args.warmup),
+            "skewed_stack": measure_stack(WORKLOADS[5], steps_x, args.warmup),
+        }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(wl)
     if rank == 0:
@@ -385,9 +481,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--extras", action="store_true", help="also measure the stack and prefill workloads")
+    ap.add_argument("--no-extras", action="store_true", help="skip the prefill and stack workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", action="store_true", help="small case for ncu captures (not a bench line)")
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+                    help="small case for ncu captures (not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

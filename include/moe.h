@@ -148,14 +148,15 @@ moe_status moe_get_device_status(moe_handle h, void* stream);
 /* Free the workspace and any captured graphs.  Synchronises the device first. */
 moe_status moe_destroy(moe_handle h);
 
-/* Stage timing (tracing).  moe_timing_enable(h, n) creates 4*n CUDA events; afterwards every
+/* Stage timing (tracing).  moe_timing_enable(h, n) creates 5*n CUDA events; afterwards every
  * layer enqueued by moe_layer_forward / moe_stack_forward (also inside a graph captured after
- * this call) records events before routing, after routing, after the first expert kernel and
- * after the combine, until n layer records are used.  moe_timing_read synchronises `stream`
- * and writes, for each of the *n_records recorded layers, 3 durations in milliseconds
- * (route, experts stage A = gate/up, experts stage B = down + combine) into ms[3*i .. 3*i+2]
- * (capacity: max_records records); moe_timing_rewind restarts recording at record 0 (events of
- * a captured graph keep their record indices).  moe_timing_enable(h, 0) frees the events. */
+ * this call) records events before routing, after routing, after expert stage A, after expert
+ * stage B and at the end, until n layer records are used.  Stages: decode (T <= 16) A = gate/up,
+ * B = down + combine, C = 0; prefill A = fp16 staging + tile plan + gate/up GEMM, B = down GEMM,
+ * C = combine.  moe_timing_read synchronises `stream` and writes, for each of the *n_records
+ * recorded layers, 4 durations in milliseconds (route, A, B, C) into ms[4*i .. 4*i+3]
+ * (capacity: max_records records); moe_timing_rewind restarts recording at record 0 (events of a
+ * captured graph keep their record indices).  moe_timing_enable(h, 0) frees the events. */
 moe_status moe_timing_enable(moe_handle h, int n_records);
 moe_status moe_timing_rewind(moe_handle h);
 moe_status moe_timing_read(moe_handle h, float* ms, int max_records, int* n_records, void* stream);
@@ -182,6 +183,13 @@ moe_status moe_route_noalloc(const float* router_w, const float* router_b, const
 
 const char* moe_status_str(moe_status s);
 int moe_version(void);
+
+/* The CUDA error code behind the most recent MOE_ERR_CUDA returned on this host thread (0 if none),
+ * and its text. */
+int moe_last_cuda_error(void);
+/* The CUDA runtime's pending error of this host thread (not cleared), for diagnostics. */
+int moe_peek_cuda_error(void);
+const char* moe_cuda_error_string(int code);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,11 @@ SMALL_T = 16  # T <= SMALL_T runs the split-K GEMV path
 class MoeError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+        msg = f"{fn} returned {STATUS_NAMES.get(status, status)}"
+        if status == 4:
+            code = lib.moe_last_cuda_error()
+            msg += f" (CUDA error {code}: {lib.moe_cuda_error_string(code).decode()})"
+        super().__init__(msg)
 
 
 class moe_config(ctypes.Structure):
@@ -60,6 +64,9 @@ def _load():
         "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
         "moe_status_str": ([ci], ctypes.c_char_p),
         "moe_version": ([], ci),
+        "moe_last_cuda_error": ([], ci),
+        "moe_peek_cuda_error": ([], ci),
+        "moe_cuda_error_string": ([ci], ctypes.c_char_p),
         "moe_gen_int4_planes": ([vp, ctypes.c_uint64, ci, ci, ci, ci, ctypes.c_size_t, vp], ci),
         "moe_gen_scale_planes": ([vp, ctypes.c_uint64, ci, ci, ci, ci, ctypes.c_size_t, vp], ci),
     }
@@ -164,9 +171,9 @@ def moe_timing_rewind(h):
 
 
 def moe_timing_read(h, max_records, stream=None):
-    """Returns a float32 array [n_records, 3] of (route, experts A, experts B) milliseconds."""
+    """Returns a float32 array [n_records, 4] of (route, stage A, stage B, stage C) milliseconds."""
     import numpy as np
-    ms = np.zeros((max(max_records, 1), 3), dtype=np.float32)
+    ms = np.zeros((max(max_records, 1), 4), dtype=np.float32)
     n = ctypes.c_int(0)
     _check("moe_timing_read", lib.moe_timing_read(h, ms.ctypes.data, max_records, ctypes.byref(n), _stream(stream)))
     return ms[: n.value].copy()

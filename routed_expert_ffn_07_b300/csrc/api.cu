@@ -16,7 +16,7 @@ namespace moe {
 cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t st);
 cudaError_t route_kernels_init();
 cudaError_t gemv_kernels_init(int num_sms);
-cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid);
+cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid, cudaEvent_t mid2);
 size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K);
 size_t gemv_smem_dn(int T, int K, int E);
 cudaError_t gemm_kernels_init(int num_sms);
@@ -27,8 +27,10 @@ void gemm_maps_free(void* p);
 cudaError_t gemm_build_maps(void* maps, int E, int d, int f, int has_shared, const void* gu_q, const void* gu_s,
                             const void* dn_q, const void* dn_s, const void* sh_gu_q, const void* sh_gu_s,
                             const void* sh_dn_q, const void* sh_dn_s);
-cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps, void* gemm_ws, cudaStream_t st, cudaEvent_t mid);
+cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps, void* gemm_ws, cudaStream_t st, cudaEvent_t mid,
+                                cudaEvent_t mid2);
 constexpr int kDispatchBlockHost = 256;
+constexpr int kTimingEvents = 5;  // before route, after route, after stage A, after stage B, end
 }  // namespace moe
 
 using namespace moe;
@@ -79,15 +81,26 @@ static size_t act_size(int act) { return act == MOE_ACT_BF16 ? 2 : 4; }
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 
+static thread_local int g_last_cuda_error = 0;
+
 #define CUDA_TRY(expr)                               \
   do {                                               \
     cudaError_t e_ = (expr);                         \
-    if (e_ != cudaSuccess) return MOE_ERR_CUDA;      \
+    if (e_ != cudaSuccess) {                         \
+      g_last_cuda_error = (int)e_;                   \
+      return MOE_ERR_CUDA;                           \
+    }                                                \
   } while (0)
 
 extern "C" {
 
 int moe_version(void) { return 1; }
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+int moe_peek_cuda_error(void) { return (int)cudaPeekAtLastError(); }
+
+const char* moe_cuda_error_string(int code) { return cudaGetErrorString(static_cast<cudaError_t>(code)); }
 
 const char* moe_status_str(moe_status s) {
   switch (s) {
@@ -301,26 +314,26 @@ static ExpertArgs make_expert_args(moe_ctx* h, int layer, const void* x, int T, 
 static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, void* y, const void* resid,
                                  bool prenorm, cudaStream_t st) {
   cudaEvent_t* ev = nullptr;
-  if (!h->tev.empty() && h->t_next + 4 <= (int)h->tev.size()) {
+  if (!h->tev.empty() && h->t_next + kTimingEvents <= (int)h->tev.size()) {
     ev = &h->tev[h->t_next];
-    h->t_next += 4;
-    if (h->t_next / 4 > h->t_used) h->t_used = h->t_next / 4;
+    h->t_next += kTimingEvents;
+    if (h->t_next / kTimingEvents > h->t_used) h->t_used = h->t_next / kTimingEvents;
   }
   cudaError_t e;
-  if (ev && (e = cudaEventRecordWithFlags(ev[0], st, cudaEventRecordExternal)) != cudaSuccess) return e;
+  if (ev && (e = record_timing_event(ev[0], st)) != cudaSuccess) return e;
   RouteArgs ra = make_route_args(h, layer, x, T, prenorm, h->stats + layer);
   const int nb = (T * h->cfg.top_k + kDispatchBlockHost - 1) / kDispatchBlockHost;
   e = launch_route(ra, nb, st);
   if (e != cudaSuccess) return e;
-  if (ev && (e = cudaEventRecordWithFlags(ev[1], st, cudaEventRecordExternal)) != cudaSuccess) return e;
+  if (ev && (e = record_timing_event(ev[1], st)) != cudaSuccess) return e;
   const void* xin = prenorm ? h->xnorm : x;
   ExpertArgs ea = make_expert_args(h, layer, xin, T, y, resid);
   if (T <= kSmallT)
-    e = launch_experts_gemv(ea, h->cfg.wfmt, st, ev ? ev[2] : nullptr);
+    e = launch_experts_gemv(ea, h->cfg.wfmt, st, ev ? ev[2] : nullptr, ev ? ev[3] : nullptr);
   else
-    e = launch_experts_gemm(ea, h->layers[layer].maps, h->gemm_ws, st, ev ? ev[2] : nullptr);
+    e = launch_experts_gemm(ea, h->layers[layer].maps, h->gemm_ws, st, ev ? ev[2] : nullptr, ev ? ev[3] : nullptr);
   if (e != cudaSuccess) return e;
-  if (ev && (e = cudaEventRecordWithFlags(ev[3], st, cudaEventRecordExternal)) != cudaSuccess) return e;
+  if (ev && (e = record_timing_event(ev[4], st)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -472,7 +485,8 @@ moe_status moe_timing_enable(moe_handle h, int n_records) {
   for (cudaEvent_t e : h->tev) cudaEventDestroy(e);
   h->tev.clear();
   h->t_next = h->t_used = 0;
-  for (int i = 0; i < 4 * n_records; ++i) {
+  cudaGetLastError();  // destroying an event that a live graph still records is reported here, not later
+  for (int i = 0; i < kTimingEvents * n_records; ++i) {
     cudaEvent_t e;
     CUDA_TRY(cudaEventCreate(&e));
     h->tev.push_back(e);
@@ -491,7 +505,9 @@ moe_status moe_timing_read(moe_handle h, float* ms, int max_records, int* n_reco
   CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
   const int n = h->t_used < max_records ? h->t_used : max_records;
   for (int i = 0; i < n; ++i)
-    for (int j = 0; j < 3; ++j) CUDA_TRY(cudaEventElapsedTime(&ms[3 * i + j], h->tev[4 * i + j], h->tev[4 * i + j + 1]));
+    for (int j = 0; j < kTimingEvents - 1; ++j)
+      CUDA_TRY(cudaEventElapsedTime(&ms[(kTimingEvents - 1) * i + j], h->tev[kTimingEvents * i + j],
+                                    h->tev[kTimingEvents * i + j + 1]));
   *n_records = n;
   return MOE_OK;
 }

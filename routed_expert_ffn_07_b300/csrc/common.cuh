@@ -82,6 +82,16 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Record a stage-timing event: inside stream capture it must become an external event node,
+// outside capture it is a plain record.
+inline cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, st);
+}
+
 // ------------------------------------------------------------------ launch arguments
 struct RouteArgs {
   const void* x;     // [T][d] activations (layer input)

@@ -41,7 +41,7 @@ constexpr int kBM = 128;            // weight rows per A matrix (MMA M)
 constexpr int kKS = 64;             // K per pipeline stage
 constexpr int kStages = 6;          // SMEM stages
 constexpr int kLoaders = 64;        // threads of warps 2-3
-constexpr int kLag = 2;             // cp.async stages in flight per loader before it signals
+constexpr int kLag = 4;             // cp.async stages in flight per loader before it signals
 constexpr unsigned kStatusRange = 4u;
 
 struct GemmMaps {
@@ -123,7 +123,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sA = sB + kStages * kNT * 128;           // kStages x NA x [128 rows x 32 B] int4
   uint8_t* sS = sA + kStages * NA * kBM * 32;       // 2 x NA x [128 rows x G fp16]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[8], tempty[8], acc_full[2], acc_empty[2],
-      sc_empty[2], fin;
+      sc_empty[2], fin, info_full[2], info_empty[2];
+  __shared__ int info_a[2][kNT];    // down epilogue: assignment id of each tile row
+  __shared__ float info_w[2][kNT];  // and its routing weight
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -143,6 +145,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::mbar_init(&sc_empty[b], 8);
     }
     tc::mbar_init(&fin, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&info_full[b], kLoaders);
+      tc::mbar_init(&info_empty[b], 8);
+    }
     s_abort = 0;
     tc::fence_mbar_init();
   }
@@ -243,12 +249,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp < 4) {
     // ---------------------------------------------------------------- B gather (cp.async)
     const int lt = threadIdx.x - 64;
-    uint32_t gs = 0, sig = 0;
+    uint32_t gs = 0, sig = 0, it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
       const int tile = item / nblk;
       const int n = g.tile_n[tile], nmma = (n + 15) & ~15, row0 = g.tile_row[tile];
       const int grp = g.tile_group[tile];
+      if (KIND == 1) {
+        // assignment ids and weights of the tile's rows, for this item's epilogue
+        const int ib = it & 1;
+        if (!tc::mbar_wait(&info_empty[ib], ((it >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
+        for (int r = lt; r < n; r += kLoaders) {
+          const int rr = row0 + r;
+          const int as = rr < g.n_assign ? g.perm[rr] : g.T * g.K + (rr - g.n_assign);
+          info_a[ib][r] = as;
+          info_w[ib][r] = rr < g.n_assign ? g.topk_w[as] : 1.f;
+        }
+        tc::mbar_arrive(&info_full[ib]);
+      }
       const __half* src[2];
       bool valid[2];
 #pragma unroll
@@ -304,7 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m = (warp - 4) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
-    const int swz = 0;  // int4 tiles are loaded without swizzle
+    const int swz = (row >> 2) & 1;  // 32-byte swizzle of the int4 tiles: 16-byte chunk c sits at c ^ bit 7 of the address
     uint32_t gs = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
@@ -352,6 +370,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // epilogue
       const int b = it % NB;
       if (!tc::mbar_wait(&acc_full[b], (it / NB) & 1, &s_abort)) { ok = false; break; }
+      if (KIND == 1 && !tc::mbar_wait(&info_full[it & 1], (it >> 1) & 1, &s_abort)) { ok = false; break; }
       tc::tc_fence_after();
       bool range_bad = false;
       for (int cb = m * 64; cb < m * 64 + 64 && cb < n; cb += 32) {
@@ -376,29 +395,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc::tmem_ld32(tmem + lane_base + b * 128 + cb, ov);
           tc::tmem_wait_ld();
           const int jrow = blk * kBM + row;
-#pragma unroll 4
+          const int ib = it & 1;
+#pragma unroll 8
           for (int jj = 0; jj < 32; ++jj) {
             const int nn = cb + jj;
-            if (nn < n) {
-              const int r = row0 + nn;
-              int a;
-              float w;
-              if (r < g.n_assign) {
-                a = g.perm[r];
-                w = g.topk_w[a];
-              } else {
-                a = g.T * g.K + (r - g.n_assign);
-                w = 1.f;
-              }
-              g.P[(size_t)a * g.d + jrow] = __float2bfloat16_rn(w * __uint_as_float(ov[jj]));
-            }
+            if (nn < n)
+              g.P[(size_t)info_a[ib][nn] * g.d + jrow] = __float2bfloat16_rn(info_w[ib][nn] * __uint_as_float(ov[jj]));
           }
         }
       }
       if (range_bad) atomicOr(g.status, kStatusRange);
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
+      if (lane == 0) {
+        tc::mbar_arrive(&acc_empty[b]);
+        if (KIND == 1) tc::mbar_arrive(&info_empty[it & 1]);
+      }
     }
     if (!ok) give_up();
   }
@@ -430,30 +442,62 @@ __global__ void xconv_kernel(const void* x, int act, __half* x16, int T, int d, 
 }
 
 // Tiles of <= 128 sorted rows: each active expert in ascending order, then the shared expert.
-__global__ void plan_tiles_kernel(const int32_t* offs, const int32_t* active, const int32_t* n_active, int E, int T,
-                                  int K, int has_shared, int32_t* n_tiles, int32_t* tg, int32_t* tr, int32_t* tn) {
-  if (threadIdx.x != 0) return;
-  int nt = 0;
+// One block of 1024 threads: a thread per slot (looping when there are more), block prefix sum of
+// the tiles per slot, then every slot writes its own tiles.
+__global__ void __launch_bounds__(1024) plan_tiles_kernel(const int4* slots, const int32_t* n_active, int E, int T,
+                                                          int K, int has_shared, int32_t* n_tiles, int32_t* tg,
+                                                          int32_t* tr, int32_t* tn) {
+  __shared__ int wsum[32];
+  __shared__ int carry;
   const int na = *n_active;
-  for (int s = 0; s < na; ++s) {
-    const int e = active[s];
-    const int b = offs[e], c = offs[e + 1] - b;
-    for (int o = 0; o < c; o += kNT) {
-      tg[nt] = e;
-      tr[nt] = b + o;
-      tn[nt] = min(kNT, c - o);
-      ++nt;
+  const int ns = na + (has_shared ? 1 : 0);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < ns; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    int e = 0, r0 = 0, c = 0;
+    if (s < na) {
+      const int4 sl = slots[s];
+      e = sl.x;
+      r0 = sl.y;
+      c = sl.z;
+    } else if (s < ns) {
+      e = E;
+      r0 = T * K;
+      c = T;
     }
-  }
-  if (has_shared) {
-    for (int o = 0; o < T; o += kNT) {
-      tg[nt] = E;
-      tr[nt] = T * K + o;
-      tn[nt] = min(kNT, T - o);
-      ++nt;
+    const int nt = (c + kNT - 1) / kNT;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = wsum[lane];
+      int wi = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      wsum[lane] = wi - v;
+    }
+    __syncthreads();
+    const int first = carry + wsum[warp] + incl - nt;
+    for (int i = 0; i < nt; ++i) {
+      tg[first + i] = e;
+      tr[first + i] = r0 + i * kNT;
+      tn[first + i] = min(kNT, c - i * kNT);
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = first + nt;
+    __syncthreads();
   }
-  *n_tiles = nt;
+  if (threadIdx.x == 0) *n_tiles = carry;
 }
 
 // y[t] = sum_k P[t*K + k] + P[T*K + t] (+ resid), fp32, fixed order; 8 columns per thread.
@@ -561,17 +605,17 @@ cudaError_t gemm_build_maps(void* maps, int E, int d, int f, int has_shared, con
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
-  if ((e = make_map(&mp->gu_q, gu_q, U8, d / 2, (uint64_t)E * 2 * f, d / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))) return e;
+  if ((e = make_map(&mp->gu_q, gu_q, U8, d / 2, (uint64_t)E * 2 * f, d / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
   if ((e = make_map(&mp->gu_s, gu_s, F16, Gd, (uint64_t)E * 2 * f, Gd * 2, Gd, kBM, sgu))) return e;
-  if ((e = make_map(&mp->dn_q, dn_q, U8, f / 2, (uint64_t)E * d, f / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))) return e;
+  if ((e = make_map(&mp->dn_q, dn_q, U8, f / 2, (uint64_t)E * d, f / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
   if ((e = make_map(&mp->dn_s, dn_s, F16, Gf, (uint64_t)E * d, Gf * 2, Gf, kBM, sdn))) return e;
   const void* sgq = has_shared ? sh_gu_q : gu_q;  // maps must be valid even when unused
   const void* sgs = has_shared ? sh_gu_s : gu_s;
   const void* sdq = has_shared ? sh_dn_q : dn_q;
   const void* sds = has_shared ? sh_dn_s : dn_s;
-  if ((e = make_map(&mp->sh_gu_q, sgq, U8, d / 2, 2 * f, d / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))) return e;
+  if ((e = make_map(&mp->sh_gu_q, sgq, U8, d / 2, 2 * f, d / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
   if ((e = make_map(&mp->sh_gu_s, sgs, F16, Gd, 2 * f, Gd * 2, Gd, kBM, sgu))) return e;
-  if ((e = make_map(&mp->sh_dn_q, sdq, U8, f / 2, d, f / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))) return e;
+  if ((e = make_map(&mp->sh_dn_q, sdq, U8, f / 2, d, f / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
   if ((e = make_map(&mp->sh_dn_s, sds, F16, Gf, d, Gf * 2, Gf, kBM, sdn))) return e;
   return cudaSuccess;
 }
@@ -580,14 +624,15 @@ void* gemm_maps_new() { return aligned_alloc(64, (sizeof(GemmMaps) + 63) & ~size
 void gemm_maps_free(void* p) { free(p); }
 
 // Launches: x -> fp16, tile plan, GEMM1, [mid event], GEMM2, combine.
-cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, void* ws, cudaStream_t st, cudaEvent_t mid) {
+cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, void* ws, cudaStream_t st, cudaEvent_t mid,
+                                cudaEvent_t mid2) {
   const GemmMaps& mp = *static_cast<const GemmMaps*>(maps_v);
   const int T = a.T, d = a.d, f = a.f, E = a.E, K = a.K;
   GemmWs w = carve(ws, T, d, f, E, K);
   const size_t nblk8 = (size_t)T * d / 8;
   xconv_kernel<<<(unsigned)((nblk8 + 255) / 256), 256, 0, st>>>(a.x, a.act, w.x16, T, d, a.status);
-  plan_tiles_kernel<<<1, 32, 0, st>>>(a.offs, a.active, a.n_active, E, T, K, a.has_shared, w.n_tiles, w.tile_group,
-                                      w.tile_row, w.tile_n);
+  plan_tiles_kernel<<<1, 1024, 0, st>>>(a.slots, a.n_active, E, T, K, a.has_shared, w.n_tiles, w.tile_group,
+                                        w.tile_row, w.tile_n);
   GemmArgs g;
   g.T = T;
   g.d = d;
@@ -608,9 +653,10 @@ cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, void* w
   g.status = a.status;
   g.sc_sw128 = mp.gu_s_sw128;
   gemm_kernel<0><<<g_sms, kGemmThreads, gemm_smem_bytes(0, d, f), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s);
-  if (mid) cudaEventRecordWithFlags(mid, st, cudaEventRecordExternal);
+  if (mid) record_timing_event(mid, st);
   g.sc_sw128 = mp.dn_s_sw128;
   gemm_kernel<1><<<g_sms, kGemmThreads, gemm_smem_bytes(1, d, f), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s);
+  if (mid2) record_timing_event(mid2, st);
   combine_kernel<<<(unsigned)((nblk8 + 255) / 256), 256, 0, st>>>(w.P, T, d, K, a.has_shared, a.resid, a.y, a.act);
   return cudaGetLastError();
 }

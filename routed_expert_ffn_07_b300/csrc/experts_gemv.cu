@@ -486,7 +486,7 @@ size_t gemv_smem_dn(int T, int K, int E) {
 }
 
 // Launches gate/up then down+combine for T <= kSmallT tokens.
-cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid) {
+cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid, cudaEvent_t mid2) {
   const int dn_grid = (a.d + kDnRows - 1) / kDnRows;
   const size_t sm_gu = gemv_smem_gu(wfmt, a.T, a.d, a.E, a.K);
   const size_t sm_dn = gemv_smem_dn(a.T, a.K, a.E);
@@ -501,12 +501,14 @@ cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, 
       case 4: gu_int4_kernel<4><<<grid, kGuThreads, sm_gu, st>>>(a); break;
       default: return cudaErrorInvalidValue;
     }
-    if (mid) cudaEventRecordWithFlags(mid, st, cudaEventRecordExternal);
+    if (mid) record_timing_event(mid, st);
     dn_int4_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
+    if (mid2) record_timing_event(mid2, st);
   } else {
     gu_f32_kernel<<<g_num_sms, 256, sm_gu, st>>>(a);
-    if (mid) cudaEventRecordWithFlags(mid, st, cudaEventRecordExternal);
+    if (mid) record_timing_event(mid, st);
     dn_f32_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
+    if (mid2) record_timing_event(mid2, st);
   }
   return cudaGetLastError();
 }
