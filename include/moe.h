@@ -148,6 +148,13 @@ moe_status moe_get_device_status(moe_handle h, void* stream);
 /* Free the workspace and any captured graphs.  Synchronises the device first. */
 moe_status moe_destroy(moe_handle h);
 
+/* Options.  MOE_OPT_GEMV_MAX_TOKENS: calls with T <= value run the split-K GEMV experts, larger T
+ * the tensor-core grouped GEMM (value 0..16; default 16; the grouped GEMM needs INT4 weights with
+ * d % 256 == 0 and f % 256 == 0, otherwise the value is clamped to 16).  Returns the option's
+ * value in effect, or a negative moe_status on error. */
+enum { MOE_OPT_GEMV_MAX_TOKENS = 1 };
+int moe_set_option(moe_handle h, int option, int value);
+
 /* Stage timing (tracing).  moe_timing_enable(h, n) creates 5*n CUDA events; afterwards every
  * layer enqueued by moe_layer_forward / moe_stack_forward (also inside a graph captured after
  * this call) records events before routing, after routing, after expert stage A, after expert

@@ -17,7 +17,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_NOT_SET", 7: "MOE_ERR_DEVICE"}
 MOE_ACT_F32, MOE_ACT_BF16 = 0, 1
 MOE_W_F32, MOE_W_INT4_G32 = 0, 1
-SMALL_T = 16  # T <= SMALL_T runs the split-K GEMV path
+SMALL_T = 16  # T <= SMALL_T can run the split-K GEMV path
+MOE_OPT_GEMV_MAX_TOKENS = 1
 
 
 class MoeError(RuntimeError):
@@ -59,6 +60,7 @@ def _load():
         "moe_get_device_status": ([vp, vp], ci),
         "moe_destroy": ([vp], ci),
         "moe_route_noalloc": ([vp, vp, vp, ci, ci, ci, ci, ci, i32p, vp, i32p, i32p, vp], ci),
+        "moe_set_option": ([vp, ci, ci], ci),
         "moe_timing_enable": ([vp, ci], ci),
         "moe_timing_rewind": ([vp], ci),
         "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
@@ -160,6 +162,13 @@ def moe_get_device_status(h, stream=None):
 
 def moe_destroy(h):
     _check("moe_destroy", lib.moe_destroy(h))
+
+
+def moe_set_option(h, option, value):
+    r = lib.moe_set_option(h, option, value)
+    if r < 0:
+        raise MoeError("moe_set_option", -r)
+    return r
 
 
 def moe_timing_enable(h, n_records):

@@ -27,8 +27,10 @@ void gemm_maps_free(void* p);
 cudaError_t gemm_build_maps(void* maps, int E, int d, int f, int has_shared, const void* gu_q, const void* gu_s,
                             const void* dn_q, const void* dn_s, const void* sh_gu_q, const void* sh_gu_s,
                             const void* sh_dn_q, const void* sh_dn_s);
-cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps, void* gemm_ws, cudaStream_t st, cudaEvent_t mid,
-                                cudaEvent_t mid2);
+cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps, const void* act_maps, void* gemm_ws,
+                                cudaStream_t st, cudaEvent_t mid, cudaEvent_t mid2);
+cudaError_t gemm_build_act_maps(void* ws, int T, int d, int f, int E, int K, void* out);
+size_t gemm_act_maps_bytes();
 constexpr int kDispatchBlockHost = 256;
 constexpr int kTimingEvents = 5;  // before route, after route, after stage A, after stage B, end
 }  // namespace moe
@@ -71,6 +73,9 @@ struct moe_ctx {
   int nblocks_max;
   cudaStream_t cap_stream = nullptr;
   std::map<int, cudaGraphExec_t> graphs;
+  bool gemm_ok = false;          // tensor-core path available for this config
+  void* act_maps = nullptr;      // TMA descriptors of the workspace activation buffers
+  int gemv_max_tokens = kSmallT; // T <= this runs the GEMV experts
   // stage timing
   std::vector<cudaEvent_t> tev;
   int t_next = 0;
@@ -131,7 +136,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   if (c.wfmt == MOE_W_INT4_G32) {
     if (c.d % 128 || c.f % 128) return MOE_ERR_UNSUPPORTED;
     if (c.d > 4096 || c.f > 1024) return MOE_ERR_UNSUPPORTED;  // GEMV lane mapping limits
-    if (c.max_tokens > kSmallT && !gemm_shape_ok(c.d, c.f)) return MOE_ERR_UNSUPPORTED;  // tensor-core path
+    if (c.max_tokens > kSmallT && !gemm_shape_ok(c.d, c.f)) return MOE_ERR_UNSUPPORTED;  // tensor-core path needed
   } else {
     if (c.max_tokens > kSmallT) return MOE_ERR_UNSUPPORTED;   // fp32 experts: GEMV path only
   }
@@ -146,8 +151,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
     return MOE_ERR_CUDA;
   }
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  h->gemm_ok = c.wfmt == MOE_W_INT4_G32 && gemm_shape_ok(c.d, c.f);
   if (route_kernels_init() != cudaSuccess || gemv_kernels_init(h->num_sms) != cudaSuccess ||
-      (c.max_tokens > kSmallT && gemm_kernels_init(h->num_sms) != cudaSuccess)) {
+      (h->gemm_ok && gemm_kernels_init(h->num_sms) != cudaSuccess)) {
     delete h;
     return MOE_ERR_CUDA;
   }
@@ -172,7 +178,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   sz[n++] = up256((size_t)h->nblocks_max * E * 4);    // blockhist
   const int TS = T < kSmallT ? T : kSmallT;
   sz[n++] = up256((size_t)(TS * K + TS) * f * 4);     // h (GEMV path)
-  sz[n++] = (T > kSmallT) ? up256(gemm_workspace_bytes(T, d, f, E, K)) : 0;
+  sz[n++] = h->gemm_ok ? up256(gemm_workspace_bytes(T, d, f, E, K)) : 0;
   sz[n++] = up256((size_t)T * d * as);                // xnorm
   sz[n++] = up256((size_t)T * d * as);                // stack x
   sz[n++] = up256((size_t)T * d * as);                // host x
@@ -211,6 +217,15 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
     delete h;
     return MOE_ERR_CUDA;
   }
+  if (h->gemm_ok) {
+    h->act_maps = gemm_maps_new();
+    if (!h->act_maps || gemm_build_act_maps(h->gemm_ws, T, d, f, E, K, h->act_maps) != cudaSuccess) {
+      if (h->act_maps) gemm_maps_free(h->act_maps);
+      cudaFree(h->slab);
+      delete h;
+      return MOE_ERR_CUDA;
+    }
+  }
   *out = h;
   return MOE_OK;
 }
@@ -229,7 +244,7 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
       return MOE_ERR_INVALID_ARG;
   }
   LayerW& L = h->layers[layer];
-  if (h->cfg.max_tokens > kSmallT) {
+  if (h->gemm_ok) {
     if (!L.maps) L.maps = gemm_maps_new();
     if (!L.maps) return MOE_ERR_OOM;
     if (gemm_build_maps(L.maps, h->cfg.n_experts, h->cfg.d, h->cfg.f, h->cfg.has_shared, w->gu_q, w->gu_s, w->dn_q,
@@ -288,6 +303,7 @@ static ExpertArgs make_expert_args(moe_ctx* h, int layer, const void* x, int T, 
   a.K = c.top_k;
   a.act = c.act;
   a.has_shared = c.has_shared;
+  a.max_tokens = c.max_tokens;
   a.x = x;
   a.gu_q = w.gu_q;
   a.gu_s = static_cast<const __half*>(w.gu_s);
@@ -328,10 +344,11 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
   if (ev && (e = record_timing_event(ev[1], st)) != cudaSuccess) return e;
   const void* xin = prenorm ? h->xnorm : x;
   ExpertArgs ea = make_expert_args(h, layer, xin, T, y, resid);
-  if (T <= kSmallT)
+  if (T <= h->gemv_max_tokens || !h->gemm_ok)
     e = launch_experts_gemv(ea, h->cfg.wfmt, st, ev ? ev[2] : nullptr, ev ? ev[3] : nullptr);
   else
-    e = launch_experts_gemm(ea, h->layers[layer].maps, h->gemm_ws, st, ev ? ev[2] : nullptr, ev ? ev[3] : nullptr);
+    e = launch_experts_gemm(ea, h->layers[layer].maps, h->act_maps, h->gemm_ws, st, ev ? ev[2] : nullptr,
+                            ev ? ev[3] : nullptr);
   if (e != cudaSuccess) return e;
   if (ev && (e = record_timing_event(ev[4], st)) != cudaSuccess) return e;
   return cudaSuccess;
@@ -480,6 +497,18 @@ moe_status moe_get_device_status(moe_handle h, void* stream) {
   return MOE_OK;
 }
 
+int moe_set_option(moe_handle h, int option, int value) {
+  if (!h) return -(int)MOE_ERR_INVALID_ARG;
+  if (option == MOE_OPT_GEMV_MAX_TOKENS) {
+    if (value < 0 || value > kSmallT) return -(int)MOE_ERR_INVALID_ARG;
+    h->gemv_max_tokens = h->gemm_ok ? value : kSmallT;
+    for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);  // captured graphs used the old path
+    h->graphs.clear();
+    return h->gemv_max_tokens;
+  }
+  return -(int)MOE_ERR_INVALID_ARG;
+}
+
 moe_status moe_timing_enable(moe_handle h, int n_records) {
   if (!h || n_records < 0 || n_records > (1 << 20)) return MOE_ERR_INVALID_ARG;
   for (cudaEvent_t e : h->tev) cudaEventDestroy(e);
@@ -518,6 +547,7 @@ moe_status moe_destroy(moe_handle h) {
   for (cudaEvent_t ev : h->tev) cudaEventDestroy(ev);
   for (LayerW& L : h->layers)
     if (L.maps) gemm_maps_free(L.maps);
+  if (h->act_maps) gemm_maps_free(h->act_maps);
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->slab) cudaFree(h->slab);

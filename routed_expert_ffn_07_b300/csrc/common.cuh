@@ -118,6 +118,7 @@ struct RouteArgs {
 
 struct ExpertArgs {
   int T, d, f, E, K, act, has_shared;
+  int max_tokens;         // the handle's max_tokens (fixes the workspace layout)
   const void* x;          // [T][d] expert input (normalised input in the stack)
   const void* gu_q;       // [E][2f][..] routed gate/up
   const __half* gu_s;

@@ -11,10 +11,18 @@
 //
 // Per CTA (one per SM, persistent over work items = (tile, 128-row block)):
 //   warp 0     : allocates 512 TMEM columns; one thread issues tcgen05.mma (A from TMEM, B from SMEM)
-//   warp 1     : one thread issues TMA loads of the int4 weight tiles and their fp16 scales
-//   warps 2-3  : gather the tile's activation rows into 128B-swizzled SMEM with cp.async
-//   warps 4-11 : dequantise int4 -> fp16 (q * scale, one rounding) straight into TMEM (tcgen05.st),
-//                then the epilogue (tcgen05.ld of the fp32 accumulators)
+//   warp 1     : one thread issues the TMA loads of the int4 weights (128 rows x 128 bytes = 256 K
+//                per stage, 128B swizzle) and of each item's fp16 scales
+//   warp 18    : one thread issues the TMA loads of the tile's activation rows (128 rows x 64
+//                columns per stage, 128B swizzle)
+//   warps 2-17 : dequantise int4 -> fp16 (q * scale, one rounding) straight into TMEM (tcgen05.st),
+//                then the epilogue (tcgen05.ld of the fp32 accumulators).  Warp w reaches TMEM lanes
+//                32*(w%4).. of the 128 weight rows.  Two teams of eight warps take alternate pipeline
+//                stages, so two stages are being dequantised at once; inside a team the warps split
+//                the stage's K columns (and the two matrices of the gate/up GEMM).  All sixteen warps
+//                share the epilogue, four groups of 32 token columns.
+// The activation rows of each expert are contiguous because a staging kernel first writes the
+// chunk's tokens in dispatch order (fp16, K-permuted), so every B tile is one TMA box.
 // The weights are the MMA M side (128 rows), the tile's tokens the N side (16..128, padded to 16),
 // so ~80-token groups are not padded to 128.  The dequantised A operand never touches shared
 // memory, which keeps SMEM traffic to the B tiles.  mbarrier pipelines: SMEM stages (TMA + cp.async
@@ -35,13 +43,17 @@
 
 namespace moe {
 
-constexpr int kGemmThreads = 384;
+constexpr int kGemmThreads = 608;  // warps: 0 MMA, 1 TMA (weights), 2-17 dequant + epilogue, 18 TMA (activations)
+constexpr int kDqWarps = 16;
+constexpr int kBWarp = 18;
+constexpr int kDqWarp0 = 2;
 constexpr int kNT = 128;            // max token rows per tile (MMA N)
 constexpr int kBM = 128;            // weight rows per A matrix (MMA M)
-constexpr int kKS = 64;             // K per pipeline stage
-constexpr int kStages = 6;          // SMEM stages
-constexpr int kLoaders = 64;        // threads of warps 2-3
-constexpr int kLag = 4;             // cp.async stages in flight per loader before it signals
+constexpr int kKS = 64;             // K per MMA / activation stage
+constexpr int kKA = 256;            // K per weight stage (128-byte int4 rows)
+constexpr int kSub = kKA / kKS;     // MMA stages per weight stage
+constexpr int kAStages = 3;         // weight stages in SMEM
+constexpr int kBStages = 4;         // activation stages in SMEM
 constexpr unsigned kStatusRange = 4u;
 
 struct GemmMaps {
@@ -49,8 +61,13 @@ struct GemmMaps {
   int gu_s_sw128, dn_s_sw128;
 };
 
+// Maps of the workspace activation buffers (fixed per handle).
+struct GemmActMaps {
+  CUtensorMap xs, hs;
+};
+
 struct GemmWs {
-  __half* x16;          // [T][d] fp16, K-permuted
+  __half* x16;          // [T*K + T][d] fp16, K-permuted, rows in dispatch order
   __half* h16;          // [T*K + T][f] fp16, K-permuted
   __nv_bfloat16* P;     // [T*K + T][d] weighted per-assignment partials
   int32_t* n_tiles;     // [1]
@@ -63,7 +80,6 @@ struct GemmArgs {
   int T, d, f, E, K, n_assign, has_shared, sc_sw128;
   const int32_t* perm;
   const float* topk_w;
-  const __half* x16;
   __half* h16;
   __nv_bfloat16* P;
   const int32_t* n_tiles;
@@ -103,12 +119,21 @@ __device__ __forceinline__ void dequant32(const uint4 q, const __half2 s2, uint3
   }
 }
 
+// 16 int4 values (8 bytes) -> 8 words of fp16 pairs, same order as dequant32.
+__device__ __forceinline__ void dequant16(const uint2 q, const __half2 s2, uint32_t* v) {
+  uint32_t t[16];
+  dequant32(make_uint4(q.x, q.y, 0u, 0u), s2, t);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = t[i];
+}
+
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 template <int KIND>  // 0: gate/up + SwiGLU, 1: down + weighted partials
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const GemmArgs g, const __grid_constant__ CUtensorMap mq_r, const __grid_constant__ CUtensorMap ms_r,
-                const __grid_constant__ CUtensorMap mq_s, const __grid_constant__ CUtensorMap ms_s) {
+                const __grid_constant__ CUtensorMap mq_s, const __grid_constant__ CUtensorMap ms_s,
+                const __grid_constant__ CUtensorMap mb) {
   constexpr int NA = KIND == 0 ? 2 : 1;  // A matrices per tile
   constexpr int NB = KIND == 0 ? 1 : 2;  // accumulator buffers
   constexpr int J = KIND == 0 ? 4 : 8;   // TMEM A stages
@@ -119,36 +144,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = smem;                               // kStages x [128 rows x 128 B]
-  uint8_t* sA = sB + kStages * kNT * 128;           // kStages x NA x [128 rows x 32 B] int4
-  uint8_t* sS = sA + kStages * NA * kBM * 32;       // 2 x NA x [128 rows x G fp16]
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[8], tempty[8], acc_full[2], acc_empty[2],
-      sc_empty[2], fin, info_full[2], info_empty[2];
-  __shared__ int info_a[2][kNT];    // down epilogue: assignment id of each tile row
-  __shared__ float info_w[2][kNT];  // and its routing weight
+  uint8_t* sB = smem;                               // kBStages x [128 rows x 128 B] fp16
+  uint8_t* sA = sB + kBStages * kNT * 128;          // kAStages x NA x [128 rows x 128 B] int4
+  uint8_t* sS = sA + kAStages * NA * kBM * 128;     // 2 x NA x [128 rows x G fp16]
+  __shared__ __align__(8) uint64_t fa[kAStages], ea[kAStages], fb[kBStages], eb[kBStages], tfull[8], tempty[8],
+      acc_full[2], acc_empty[2], sc_full[2], sc_empty[2], fin;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], 1 + kLoaders);
-      tc::mbar_init(&empty[s], 1 + 8);
+    for (int s = 0; s < kAStages; ++s) {
+      tc::mbar_init(&fa[s], 1);
+      tc::mbar_init(&ea[s], kDqWarps);  // every dequant warp, after its last sub-stage of the weight stage
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      tc::mbar_init(&fb[s], 1);
+      tc::mbar_init(&eb[s], 1);
     }
     for (int j = 0; j < J; ++j) {
-      tc::mbar_init(&tfull[j], 8);
+      tc::mbar_init(&tfull[j], kDqWarps / 2);
       tc::mbar_init(&tempty[j], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 8);
-      tc::mbar_init(&sc_empty[b], 8);
+      tc::mbar_init(&acc_empty[b], kDqWarps);
+      tc::mbar_init(&sc_empty[b], kDqWarps);
+      tc::mbar_init(&sc_full[b], 1);
     }
     tc::mbar_init(&fin, 1);
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&info_full[b], kLoaders);
-      tc::mbar_init(&info_empty[b], 8);
-    }
     s_abort = 0;
     tc::fence_mbar_init();
   }
@@ -179,9 +203,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!tc::mbar_wait(&acc_empty[b], ((it / NB) & 1) ^ 1, &s_abort)) { ok = false; break; }
         tc::tc_fence_after();
         for (int s = 0; s < KS; ++s, ++gs) {
-          const int slot = gs % kStages, j = gs % J;
-          if (!tc::mbar_wait(&full[slot], (gs / kStages) & 1, &s_abort) ||
-              !tc::mbar_wait(&tfull[j], (gs / J) & 1, &s_abort)) {
+          const int slot = gs % kBStages, j = gs % J;
+          if (!tc::mbar_wait(&fb[slot], (gs / kBStages) & 1, &s_abort)) { ok = false; break; }
+          if (!tc::mbar_wait(&tfull[j], (gs / J) & 1, &s_abort)) {
             ok = false;
             break;
           }
@@ -197,7 +221,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tc::mma_ts(tmem + dcol, tmem + acol, bd, idesc, (s > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          tc::mma_commit(&empty[slot]);
+          tc::mma_commit(&eb[slot]);
           tc::mma_commit(&tempty[j]);
         }
         if (!ok) break;
@@ -216,9 +240,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::prefetch_tmap(&ms_r);
       tc::prefetch_tmap(&mq_s);
       tc::prefetch_tmap(&ms_s);
-      uint32_t gs = 0, it = 0;
+      uint32_t as = 0, it = 0;
       bool ok = true;
       const int rows_per_expert = KIND == 0 ? 2 * g.f : g.d;
+      const int KAS = Kdim / kKA;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
         const int tile = item / nblk, blk = item % nblk;
         const int grp = g.tile_group[tile];
@@ -227,102 +252,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const CUtensorMap* ms = sh ? &ms_s : &ms_r;
         const int r0 = (sh ? 0 : grp * rows_per_expert) + blk * kBM;
         const int sb = it & 1;
-        for (int s = 0; s < KS; ++s, ++gs) {
-          const int slot = gs % kStages;
-          if (!tc::mbar_wait(&empty[slot], ((gs / kStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
-          uint32_t bytes = NA * kBM * 32;
-          if (s == 0) {
-            if (!tc::mbar_wait(&sc_empty[sb], ((it >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
-            bytes += NA * kBM * G * 2;
-          }
-          tc::mbar_arrive_expect_tx(&full[slot], bytes);
+        // the item's scales: their own barrier, since one dequant team never waits on the first stage
+        if (!tc::mbar_wait(&sc_empty[sb], ((it >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
+        tc::mbar_arrive_expect_tx(&sc_full[sb], NA * kBM * G * 2);
 #pragma unroll
-          for (int m = 0; m < NA; ++m) {
-            tc::tma_load_2d(sA + (slot * NA + m) * kBM * 32, mq, s * 32, r0 + m * g.f, &full[slot]);
-            if (s == 0) tc::tma_load_2d(sS + (sb * NA + m) * kBM * G * 2, ms, 0, r0 + m * g.f, &full[slot]);
-          }
+        for (int m = 0; m < NA; ++m)
+          tc::tma_load_2d(sS + (sb * NA + m) * kBM * G * 2, ms, 0, r0 + m * g.f, &sc_full[sb]);
+        for (int a = 0; a < KAS; ++a, ++as) {
+          const int slot = as % kAStages;
+          if (!tc::mbar_wait(&ea[slot], ((as / kAStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&fa[slot], NA * kBM * 128);
+#pragma unroll
+          for (int m = 0; m < NA; ++m)
+            tc::tma_load_2d(sA + (slot * NA + m) * kBM * 128, mq, a * 128, r0 + m * g.f, &fa[slot]);
         }
       }
       if (!ok) give_up();
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ---------------------------------------------------------------- B gather (cp.async)
-    const int lt = threadIdx.x - 64;
-    uint32_t gs = 0, sig = 0, it = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-      const int tile = item / nblk;
-      const int n = g.tile_n[tile], nmma = (n + 15) & ~15, row0 = g.tile_row[tile];
-      const int grp = g.tile_group[tile];
-      if (KIND == 1) {
-        // assignment ids and weights of the tile's rows, for this item's epilogue
-        const int ib = it & 1;
-        if (!tc::mbar_wait(&info_empty[ib], ((it >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
-        for (int r = lt; r < n; r += kLoaders) {
-          const int rr = row0 + r;
-          const int as = rr < g.n_assign ? g.perm[rr] : g.T * g.K + (rr - g.n_assign);
-          info_a[ib][r] = as;
-          info_w[ib][r] = rr < g.n_assign ? g.topk_w[as] : 1.f;
-        }
-        tc::mbar_arrive(&info_full[ib]);
-      }
-      const __half* src[2];
-      bool valid[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int r = lt + 64 * i;
-        valid[i] = r < n;
-        src[i] = g.x16;
-        if (valid[i]) {
-          if (KIND == 0) {
-            const int tok = grp < g.E ? g.perm[row0 + r] / g.K : row0 + r - g.n_assign;
-            src[i] = g.x16 + (size_t)tok * g.d;
-          } else {
-            src[i] = g.h16 + (size_t)(row0 + r) * g.f;
-          }
+  } else if (warp == kBWarp) {
+    // ---------------------------------------------------------------- TMA producer (activations)
+    if (lane == 0) {
+      tc::prefetch_tmap(&mb);
+      uint32_t gs = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int tile = item / nblk;
+        const int brow = g.tile_row[tile];
+        for (int s = 0; s < KS; ++s, ++gs) {
+          const int slot = gs % kBStages;
+          if (!tc::mbar_wait(&eb[slot], ((gs / kBStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&fb[slot], kNT * 128);
+          tc::tma_load_2d(sB + slot * kNT * 128, &mb, s * kKS, brow, &fb[slot]);
         }
       }
-      for (int s = 0; s < KS; ++s, ++gs) {
-        const int slot = gs % kStages;
-        if (!tc::mbar_wait(&empty[slot], ((gs / kStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
-        const uint32_t base = tc::smem_u32(sB + slot * kNT * 128);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = lt + 64 * i;
-          if (r < nmma) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t dst = base + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-              tc::cp_async16(dst, valid[i] ? src[i] + s * kKS + c * 8 : g.x16, valid[i] ? 16u : 0u);
-            }
-          }
-        }
-        tc::cp_async_commit();
-        if (gs + 1 - sig > (uint32_t)kLag) {
-          tc::cp_async_wait<kLag>();
-          tc::fence_proxy_async_smem();
-          while (gs + 1 - sig > (uint32_t)kLag) {
-            tc::mbar_arrive(&full[sig % kStages]);
-            ++sig;
-          }
-        }
-      }
+      if (!ok) give_up();
     }
-    tc::cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    while (sig < gs) {
-      tc::mbar_arrive(&full[sig % kStages]);
-      ++sig;
-    }
-    if (!ok) give_up();
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- dequant + epilogue
-    const int q = warp & 3;
-    const int m = (warp - 4) >> 2;
+    const int q = warp & 3;                      // TMEM lane quarter
+    const int grp = (warp - kDqWarp0) >> 2;      // 0..3 (epilogue token-column group)
+    const int team = grp >> 1;                   // stages with gs % 2 == team
+    const int sub = grp & 1;                     // gate/up: matrix; down: 16-byte chunk of the stage
+    const int m = KIND == 0 ? sub : 0;
     const int row = q * 32 + lane;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
-    const int swz = (row >> 2) & 1;  // 32-byte swizzle of the int4 tiles: 16-byte chunk c sits at c ^ bit 7 of the address
+    const int swz = row & 7;  // 128-byte swizzle of the int4 rows: 16-byte chunk c sits at c ^ (row % 8)
     uint32_t gs = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
@@ -330,14 +306,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int n = g.tile_n[tile], row0 = g.tile_row[tile];
       const int sb = it & 1;
       const uint8_t* srow = sS + ((sb * NA + (KIND == 0 ? m : 0)) * kBM + row) * G * 2;
+      if (!tc::mbar_wait(&sc_full[sb], (it >> 1) & 1, &s_abort)) {
+        ok = false;
+        break;
+      }
       for (int s = 0; s < KS; ++s, ++gs) {
-        const int slot = gs % kStages, j = gs % J;
-        if (!tc::mbar_wait(&full[slot], (gs / kStages) & 1, &s_abort) ||
-            !tc::mbar_wait(&tempty[j], ((gs / J) & 1) ^ 1, &s_abort)) {
+        if ((int)(gs & 1) != team) {
+          if (s == KS - 1 && lane == 0) tc::mbar_arrive(&sc_empty[sb]);  // done with this item's scales
+          continue;
+        }
+        const uint32_t as = gs / kSub;  // weight stage (continuous across items: K % 256 == 0)
+        const int sub_k = gs % kSub;   // which 64-K part of it
+        const int aslot = as % kAStages, j = gs % J;
+        if (!tc::mbar_wait(&fa[aslot], (as / kAStages) & 1, &s_abort)) { ok = false; break; }
+        if (!tc::mbar_wait(&tempty[j], ((gs / J) & 1) ^ 1, &s_abort)) {
           ok = false;
           break;
         }
-        const uint8_t* arow = sA + ((slot * NA + (KIND == 0 ? m : 0)) * kBM + row) * 32;
+        const uint8_t* arow = sA + ((aslot * NA + m) * kBM + row) * 128;
         auto scale_at = [&](int grp_idx) -> __half2 {
           const int o = grp_idx * 2;
           const int off = g.sc_sw128 ? ((((o >> 4) ^ (row & 7)) << 4) | (o & 15)) : o;
@@ -345,24 +331,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           return __halves2half2(s1, s1);
         };
         if (KIND == 0) {
+          // the whole 64-K stage of matrix m: two 16-byte chunks
           uint32_t v[32];
-          const uint4 q0 = *reinterpret_cast<const uint4*>(arow + ((0 ^ swz) << 4));
-          const uint4 q1 = *reinterpret_cast<const uint4*>(arow + ((1 ^ swz) << 4));
+          const uint4 q0 = *reinterpret_cast<const uint4*>(arow + (((2 * sub_k) ^ swz) << 4));
+          const uint4 q1 = *reinterpret_cast<const uint4*>(arow + (((2 * sub_k + 1) ^ swz) << 4));
           dequant32(q0, scale_at(2 * s), v);
           dequant32(q1, scale_at(2 * s + 1), v + 16);
           tc::tmem_st32(tmem + lane_base + 256 + j * (NA * 32) + m * 32, v);
         } else {
+          // one 16-byte chunk (32 K) of the stage
           uint32_t v[16];
-          const uint4 qq = *reinterpret_cast<const uint4*>(arow + ((m ^ swz) << 4));
-          dequant32(qq, scale_at(2 * s + m), v);
-          tc::tmem_st16(tmem + lane_base + 256 + j * 32 + m * 16, v);
+          const uint4 qq = *reinterpret_cast<const uint4*>(arow + (((2 * sub_k + sub) ^ swz) << 4));
+          dequant32(qq, scale_at(2 * s + sub), v);
+          tc::tmem_st16(tmem + lane_base + 256 + j * 32 + sub * 16, v);
         }
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           tc::mbar_arrive(&tfull[j]);
-          tc::mbar_arrive(&empty[slot]);
+          if (sub_k >= kSub - 2) tc::mbar_arrive(&ea[aslot]);  // this warp's last part of the weight stage
           if (s == KS - 1) tc::mbar_arrive(&sc_empty[sb]);
         }
       }
@@ -370,10 +358,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // epilogue
       const int b = it % NB;
       if (!tc::mbar_wait(&acc_full[b], (it / NB) & 1, &s_abort)) { ok = false; break; }
-      if (KIND == 1 && !tc::mbar_wait(&info_full[it & 1], (it >> 1) & 1, &s_abort)) { ok = false; break; }
       tc::tc_fence_after();
       bool range_bad = false;
-      for (int cb = m * 64; cb < m * 64 + 64 && cb < n; cb += 32) {
+      for (int cb = grp * 32; cb < grp * 32 + 32 && cb < n; cb += 32) {
         if (KIND == 0) {
           uint32_t gv[32], uv[32];
           tc::tmem_ld32(tmem + lane_base + cb, gv);
@@ -391,26 +378,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         } else {
+          // assignment id and weight of token column cb + lane, shared with the warp by shuffles
+          const int rr = row0 + cb + lane;
+          int my_a = 0;
+          float my_w = 0.f;
+          if (cb + lane < n) {
+            my_a = rr < g.n_assign ? g.perm[rr] : g.T * g.K + (rr - g.n_assign);
+            my_w = rr < g.n_assign ? g.topk_w[my_a] : 1.f;
+          }
           uint32_t ov[32];
           tc::tmem_ld32(tmem + lane_base + b * 128 + cb, ov);
           tc::tmem_wait_ld();
           const int jrow = blk * kBM + row;
-          const int ib = it & 1;
-#pragma unroll 8
+#pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int nn = cb + jj;
-            if (nn < n)
-              g.P[(size_t)info_a[ib][nn] * g.d + jrow] = __float2bfloat16_rn(info_w[ib][nn] * __uint_as_float(ov[jj]));
+            const int a_jj = __shfl_sync(0xffffffffu, my_a, jj);
+            const float w_jj = __shfl_sync(0xffffffffu, my_w, jj);
+            if (cb + jj < n) g.P[(size_t)a_jj * g.d + jrow] = __float2bfloat16_rn(w_jj * __uint_as_float(ov[jj]));
           }
         }
       }
       if (range_bad) atomicOr(g.status, kStatusRange);
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&acc_empty[b]);
-        if (KIND == 1) tc::mbar_arrive(&info_empty[it & 1]);
-      }
+      if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
     }
     if (!ok) give_up();
   }
@@ -421,13 +412,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ------------------------------------------------------------------ helper kernels
-// x (act type) -> fp16, K-permuted within 8-column blocks; flags values outside the fp16 range.
-__global__ void xconv_kernel(const void* x, int act, __half* x16, int T, int d, unsigned* status) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // one 8-column block
-  if (i >= (size_t)T * d / 8) return;
+// Activations of the routed rows in dispatch order, fp16, K-permuted within 8-column blocks:
+// row r < T*K holds token perm[r] / K, row T*K + t holds token t (shared expert).  One thread per
+// 8-column block; flags values outside the fp16 range.
+__global__ void xgather_kernel(const void* x, int act, const int32_t* perm, __half* xs, int T, int K, int d,
+                               int has_shared, unsigned* status) {
+  const int rows = T * K + (has_shared ? T : 0);
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)rows * d / 8) return;
+  const int r = (int)(i / (d / 8)), c = (int)(i % (d / 8));
+  const int tok = r < T * K ? perm[r] / K : r - T * K;
   float v[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) v[p] = load_act(x, act, i * 8 + p);
+  load8_act(x, act, (size_t)tok * d + c * 8, v);
   const int sig[8] = {0, 4, 1, 5, 2, 6, 3, 7};
   __align__(16) __half o[8];
   bool bad = false;
@@ -437,7 +433,7 @@ __global__ void xconv_kernel(const void* x, int act, __half* x16, int T, int d, 
     bad |= !(fabsf(t) <= 65504.f);
     o[p] = __float2half_rn(t);
   }
-  *reinterpret_cast<uint4*>(x16 + i * 8) = *reinterpret_cast<const uint4*>(o);
+  *reinterpret_cast<uint4*>(xs + (size_t)r * d + c * 8) = *reinterpret_cast<const uint4*>(o);
   if (bad) atomicOr(status, kStatusRange);
 }
 
@@ -528,12 +524,12 @@ __global__ void combine_kernel(const __nv_bfloat16* P, int T, int d, int K, int 
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static int g_sms = 148;
 
-constexpr int kGemmSmemMax = 220 * 1024;
+constexpr int kGemmSmemMax = 226 * 1024;
 
 static size_t gemm_smem_bytes(int kind, int d, int f) {
   const int NA = kind == 0 ? 2 : 1;
   const int G = (kind == 0 ? d : f) / 32;
-  return 1024 + (size_t)kStages * kNT * 128 + (size_t)kStages * NA * kBM * 32 + (size_t)2 * NA * kBM * G * 2;
+  return 1024 + (size_t)kBStages * kNT * 128 + (size_t)kAStages * NA * kBM * 128 + (size_t)2 * NA * kBM * G * 2;
 }
 
 cudaError_t gemm_kernels_init(int num_sms) {
@@ -552,7 +548,7 @@ cudaError_t gemm_kernels_init(int num_sms) {
 }
 
 bool gemm_shape_ok(int d, int f) {
-  return d % 256 == 0 && f % 256 == 0 && d / 32 <= 256 && f / 32 <= 256 &&
+  return d % kKA == 0 && f % kKA == 0 && d / 32 <= 256 && f / 32 <= 256 &&
          gemm_smem_bytes(0, d, f) <= kGemmSmemMax && gemm_smem_bytes(1, d, f) <= kGemmSmemMax;
 }
 
@@ -560,7 +556,8 @@ size_t gemm_workspace_bytes(int T, int d, int f, int E, int K) {
   const size_t rows = (size_t)T * K + T;
   const size_t max_tiles = (size_t)(T * K) / kNT + E + (T + kNT - 1) / kNT + 2;
   auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
-  return up((size_t)T * d * 2) + up(rows * f * 2) + up(rows * d * 2) + up(4) + 3 * up(max_tiles * 4);
+  return up(rows * d * 2) + up(rows * f * 2) + up(rows * d * 2) + up(4) + 3 * up(max_tiles * 4) +
+         up(sizeof(GemmActMaps) + 64);
 }
 
 static GemmWs carve(void* ws, int T, int d, int f, int E, int K) {
@@ -569,7 +566,7 @@ static GemmWs carve(void* ws, int T, int d, int f, int E, int K) {
   auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
   char* p = static_cast<char*>(ws);
   GemmWs w;
-  w.x16 = reinterpret_cast<__half*>(p); p += up((size_t)T * d * 2);
+  w.x16 = reinterpret_cast<__half*>(p); p += up(rows * d * 2);
   w.h16 = reinterpret_cast<__half*>(p); p += up(rows * f * 2);
   w.P = reinterpret_cast<__nv_bfloat16*>(p); p += up(rows * d * 2);
   w.n_tiles = reinterpret_cast<int32_t*>(p); p += up(4);
@@ -605,32 +602,51 @@ cudaError_t gemm_build_maps(void* maps, int E, int d, int f, int has_shared, con
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
-  if ((e = make_map(&mp->gu_q, gu_q, U8, d / 2, (uint64_t)E * 2 * f, d / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
+  if ((e = make_map(&mp->gu_q, gu_q, U8, d / 2, (uint64_t)E * 2 * f, d / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
   if ((e = make_map(&mp->gu_s, gu_s, F16, Gd, (uint64_t)E * 2 * f, Gd * 2, Gd, kBM, sgu))) return e;
-  if ((e = make_map(&mp->dn_q, dn_q, U8, f / 2, (uint64_t)E * d, f / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
+  if ((e = make_map(&mp->dn_q, dn_q, U8, f / 2, (uint64_t)E * d, f / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
   if ((e = make_map(&mp->dn_s, dn_s, F16, Gf, (uint64_t)E * d, Gf * 2, Gf, kBM, sdn))) return e;
   const void* sgq = has_shared ? sh_gu_q : gu_q;  // maps must be valid even when unused
   const void* sgs = has_shared ? sh_gu_s : gu_s;
   const void* sdq = has_shared ? sh_dn_q : dn_q;
   const void* sds = has_shared ? sh_dn_s : dn_s;
-  if ((e = make_map(&mp->sh_gu_q, sgq, U8, d / 2, 2 * f, d / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
+  if ((e = make_map(&mp->sh_gu_q, sgq, U8, d / 2, 2 * f, d / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
   if ((e = make_map(&mp->sh_gu_s, sgs, F16, Gd, 2 * f, Gd * 2, Gd, kBM, sgu))) return e;
-  if ((e = make_map(&mp->sh_dn_q, sdq, U8, f / 2, d, f / 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_32B))) return e;
+  if ((e = make_map(&mp->sh_dn_q, sdq, U8, f / 2, d, f / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
   if ((e = make_map(&mp->sh_dn_s, sds, F16, Gf, d, Gf * 2, Gf, kBM, sdn))) return e;
   return cudaSuccess;
 }
 
+// Tensor maps of the workspace's sorted activation rows (GEMM1 B) and h rows (GEMM2 B):
+// box 128 rows x 64 fp16 columns, 128-byte swizzle.
+cudaError_t gemm_build_act_maps(void* ws, int T, int d, int f, int E, int K, void* out) {
+  if (!g_encode) return cudaErrorNotSupported;
+  GemmWs w = carve(ws, T, d, f, E, K);
+  GemmActMaps* am = static_cast<GemmActMaps*>(out);
+  const uint64_t rows = (uint64_t)T * K + T;
+  cudaError_t e = make_map(&am->xs, w.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d, rows, (uint64_t)d * 2, kKS, kNT,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  return make_map(&am->hs, w.h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, f, rows, (uint64_t)f * 2, kKS, kNT,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+size_t gemm_act_maps_bytes() { return sizeof(GemmActMaps); }
+
 void* gemm_maps_new() { return aligned_alloc(64, (sizeof(GemmMaps) + 63) & ~size_t(63)); }
 void gemm_maps_free(void* p) { free(p); }
 
-// Launches: x -> fp16, tile plan, GEMM1, [mid event], GEMM2, combine.
-cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, void* ws, cudaStream_t st, cudaEvent_t mid,
-                                cudaEvent_t mid2) {
+// Launches: sorted fp16 activations, tile plan, GEMM1, [mid event], GEMM2, [mid2 event], combine.
+cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, const void* act_maps_v, void* ws,
+                                cudaStream_t st, cudaEvent_t mid, cudaEvent_t mid2) {
   const GemmMaps& mp = *static_cast<const GemmMaps*>(maps_v);
+  const GemmActMaps& am = *static_cast<const GemmActMaps*>(act_maps_v);
   const int T = a.T, d = a.d, f = a.f, E = a.E, K = a.K;
-  GemmWs w = carve(ws, T, d, f, E, K);
-  const size_t nblk8 = (size_t)T * d / 8;
-  xconv_kernel<<<(unsigned)((nblk8 + 255) / 256), 256, 0, st>>>(a.x, a.act, w.x16, T, d, a.status);
+  GemmWs w = carve(ws, a.max_tokens, d, f, E, K);  // layout fixed by max_tokens (the TMA maps point into it)
+  const size_t rows = (size_t)T * K + (a.has_shared ? T : 0);
+  const size_t nch = rows * d / 8;
+  xgather_kernel<<<(unsigned)((nch + 255) / 256), 256, 0, st>>>(a.x, a.act, a.perm, w.x16, T, K, d, a.has_shared,
+                                                                a.status);
   plan_tiles_kernel<<<1, 1024, 0, st>>>(a.slots, a.n_active, E, T, K, a.has_shared, w.n_tiles, w.tile_group,
                                         w.tile_row, w.tile_n);
   GemmArgs g;
@@ -643,7 +659,6 @@ cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, void* w
   g.has_shared = a.has_shared;
   g.perm = a.perm;
   g.topk_w = a.topk_w;
-  g.x16 = w.x16;
   g.h16 = w.h16;
   g.P = w.P;
   g.n_tiles = w.n_tiles;
@@ -652,13 +667,17 @@ cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, void* w
   g.tile_n = w.tile_n;
   g.status = a.status;
   g.sc_sw128 = mp.gu_s_sw128;
-  gemm_kernel<0><<<g_sms, kGemmThreads, gemm_smem_bytes(0, d, f), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s);
+  gemm_kernel<0><<<g_sms, kGemmThreads, gemm_smem_bytes(0, d, f), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s,
+                                                                        am.xs);
   if (mid) record_timing_event(mid, st);
   g.sc_sw128 = mp.dn_s_sw128;
-  gemm_kernel<1><<<g_sms, kGemmThreads, gemm_smem_bytes(1, d, f), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s);
+  gemm_kernel<1><<<g_sms, kGemmThreads, gemm_smem_bytes(1, d, f), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s,
+                                                                        am.hs);
   if (mid2) record_timing_event(mid2, st);
+  const size_t nblk8 = (size_t)T * d / 8;
   combine_kernel<<<(unsigned)((nblk8 + 255) / 256), 256, 0, st>>>(w.P, T, d, K, a.has_shared, a.resid, a.y, a.act);
   return cudaGetLastError();
 }
 
 }  // namespace moe
+

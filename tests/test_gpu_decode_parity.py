@@ -163,12 +163,14 @@ def test_decode_layer_batch_sizes(decode_layer):
         run_layer(h, wl, wts, x[:T], T, layer=1, gen_layer=1)
 
 
-def _stack_parity(wl, sample_layers):
+def _stack_parity(wl, sample_layers, gemv_max=None):
     torch = _torch()
     from routed_expert_ffn_07_b300 import capi
     wts = alloc_and_fill(wl)
     L, T, d, K, E = wl.layers, wl.T, wl.d, wl.K, wl.E
     h = create_handle(wl, wts)
+    if gemv_max is not None:
+        capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gemv_max)
     try:
         x0 = inputs.gen_activations(wl.seed, T, d, "bf16")
         xa = to_torch_act(x0)
@@ -266,3 +268,26 @@ def test_invalid_arguments_rejected():
         assert capi.moe_get_device_status(h) == 0
     finally:
         capi.moe_destroy(h)
+
+
+@pytest.mark.parametrize("gemv_max", [0, 16])
+def test_decode_sizes_on_both_expert_paths(decode_layer, gemv_max):
+    """T <= 16 through the split-K GEMV experts and through the tensor-core grouped GEMM."""
+    from routed_expert_ffn_07_b300 import capi
+    wl, wts, h = decode_layer
+    capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gemv_max)
+    try:
+        x = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=9)
+        for T in (1, 4, 16):
+            run_layer(h, wl, wts, x[:T], T, layer=2, gen_layer=2)
+    finally:
+        capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 16)
+
+
+def test_skewed_stack_on_tensor_core_path():
+    from routed_expert_ffn_07_b300 import capi
+    wl = WORKLOADS[5]
+    import dataclasses
+    wl_small = dataclasses.replace(wl, layers=8)
+    counts, flagged, worst = _stack_parity(wl_small, sample_layers=[0, 3, 7], gemv_max=0)
+    assert all(10 <= c <= 160 for c in counts)
