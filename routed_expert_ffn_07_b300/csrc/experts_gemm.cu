@@ -52,13 +52,18 @@ constexpr int kBM = 128;            // weight rows per A matrix (MMA M)
 constexpr int kKS = 64;             // K per MMA / activation stage
 constexpr int kKA = 256;            // K per weight stage (128-byte int4 rows)
 constexpr int kSub = kKA / kKS;     // MMA stages per weight stage
-constexpr int kAStages = 3;         // weight stages in SMEM
-constexpr int kBStages = 4;         // activation stages in SMEM
+constexpr int kAStages = 3;         // weight stages in SMEM (int4 rows + their fp16 scales)
+constexpr int kScB = kKA / 32 * 2;  // scale bytes per weight row per weight stage (8 groups)
+// activation stages in SMEM and dequantised A stages in TMEM, per kind (0 gate/up, 1 down)
+template <int KIND> struct Stages {
+  static constexpr int NA = KIND == 0 ? 2 : 1;   // A matrices per tile
+  static constexpr int B = KIND == 0 ? 7 : 10;   // activation stages: deep, the TMA latency is long
+  static constexpr int J = KIND == 0 ? 4 : 8;    // TMEM A stages (NA*32 columns each, 256 columns in all)
+};
 constexpr unsigned kStatusRange = 4u;
 
 struct GemmMaps {
   CUtensorMap gu_q, gu_s, sh_gu_q, sh_gu_s, dn_q, dn_s, sh_dn_q, sh_dn_s;
-  int gu_s_sw128, dn_s_sw128;
 };
 
 // Maps of the workspace activation buffers (fixed per handle).
@@ -77,7 +82,7 @@ struct GemmWs {
 };
 
 struct GemmArgs {
-  int T, d, f, E, K, n_assign, has_shared, sc_sw128;
+  int T, d, f, E, K, n_assign, has_shared;
   const int32_t* perm;
   const float* topk_w;
   __half* h16;
@@ -134,21 +139,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const GemmArgs g, const __grid_constant__ CUtensorMap mq_r, const __grid_constant__ CUtensorMap ms_r,
                 const __grid_constant__ CUtensorMap mq_s, const __grid_constant__ CUtensorMap ms_s,
                 const __grid_constant__ CUtensorMap mb) {
-  constexpr int NA = KIND == 0 ? 2 : 1;  // A matrices per tile
+  constexpr int NA = Stages<KIND>::NA;
   constexpr int NB = KIND == 0 ? 1 : 2;  // accumulator buffers
-  constexpr int J = KIND == 0 ? 4 : 8;   // TMEM A stages
+  constexpr int BS = Stages<KIND>::B;
+  constexpr int J = Stages<KIND>::J;
+  static_assert(J <= BS && 256 + J * NA * 32 <= 512, "TMEM budget");
   const int Kdim = KIND == 0 ? g.d : g.f;
   const int KS = Kdim / kKS;
-  const int G = Kdim / 32;
   const int nblk = (KIND == 0 ? g.f : g.d) / kBM;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = smem;                               // kBStages x [128 rows x 128 B] fp16
-  uint8_t* sA = sB + kBStages * kNT * 128;          // kAStages x NA x [128 rows x 128 B] int4
-  uint8_t* sS = sA + kAStages * NA * kBM * 128;     // 2 x NA x [128 rows x G fp16]
-  __shared__ __align__(8) uint64_t fa[kAStages], ea[kAStages], fb[kBStages], eb[kBStages], tfull[8], tempty[8],
-      acc_full[2], acc_empty[2], sc_full[2], sc_empty[2], fin;
+  uint8_t* sB = smem;                               // BS x [128 rows x 128 B] fp16
+  uint8_t* sA = sB + BS * kNT * 128;                // kAStages x NA x [128 rows x 128 B] int4
+  uint8_t* sS = sA + kAStages * NA * kBM * 128;     // kAStages x NA x [128 rows x 8 fp16]
+  // fa/ea: weight stages; fb: activation stages; tfull: stage gs dequantised into TMEM A stage
+  // gs % J and its activations seen by the dequant warps; sdone: the MMAs of stage gs finished,
+  // which frees activation slot gs % BS and (J stages later) TMEM A stage gs % J
+  __shared__ __align__(8) uint64_t fa[kAStages], ea[kAStages], fb[BS], tfull[BS], sdone[BS], acc_full[2],
+      acc_empty[2], fin;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -158,19 +167,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc::mbar_init(&fa[s], 1);
       tc::mbar_init(&ea[s], kDqWarps);  // every dequant warp, after its last sub-stage of the weight stage
     }
-    for (int s = 0; s < kBStages; ++s) {
+    for (int s = 0; s < BS; ++s) {
       tc::mbar_init(&fb[s], 1);
-      tc::mbar_init(&eb[s], 1);
-    }
-    for (int j = 0; j < J; ++j) {
-      tc::mbar_init(&tfull[j], kDqWarps / 2);
-      tc::mbar_init(&tempty[j], 1);
+      tc::mbar_init(&tfull[s], kDqWarps / 2);
+      tc::mbar_init(&sdone[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
       tc::mbar_init(&acc_empty[b], kDqWarps);
-      tc::mbar_init(&sc_empty[b], kDqWarps);
-      tc::mbar_init(&sc_full[b], 1);
     }
     tc::mbar_init(&fin, 1);
     s_abort = 0;
@@ -192,43 +196,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t gs = 0, it = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        const int tile = item / nblk;
-        const int nmma = (g.tile_n[tile] + 15) & ~15;
-        const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
-        const int b = it % NB;
-        if (!tc::mbar_wait(&acc_empty[b], ((it / NB) & 1) ^ 1, &s_abort)) { ok = false; break; }
-        tc::tc_fence_after();
-        for (int s = 0; s < KS; ++s, ++gs) {
-          const int slot = gs % kBStages, j = gs % J;
-          if (!tc::mbar_wait(&fb[slot], (gs / kBStages) & 1, &s_abort)) { ok = false; break; }
-          if (!tc::mbar_wait(&tfull[j], (gs / J) & 1, &s_abort)) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint32_t bbase = tc::smem_u32(sB + slot * kNT * 128);
-#pragma unroll
-          for (int kk = 0; kk < kKS / 16; ++kk) {
-            const uint64_t bd = tc::sdesc_sw128(bbase + kk * 32);
-#pragma unroll
-            for (int m = 0; m < NA; ++m) {
-              const uint32_t dcol = KIND == 0 ? m * 128 : b * 128;
-              const uint32_t acol = 256 + j * (NA * 32) + m * 32 + kk * 8;
-              tc::mma_ts(tmem + dcol, tmem + acol, bd, idesc, (s > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          tc::mma_commit(&eb[slot]);
-          tc::mma_commit(&tempty[j]);
+    // The whole warp runs this loop converged (all values warp-uniform); one elected lane issues.
+    uint32_t gs = 0, it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      const int tile = item / nblk;
+      const int nmma = (g.tile_n[tile] + 15) & ~15;
+      const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
+      const int b = it % NB;
+      if (!tc::mbar_wait_warp(&acc_empty[b], ((it / NB) & 1) ^ 1, &s_abort)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t dcol0 = KIND == 0 ? 0u : (uint32_t)b * 128u;
+      for (int s = 0; s < KS; ++s, ++gs) {
+        const int slot = gs % BS;
+        const uint32_t ph = (gs / BS) & 1;
+        // tfull completes after the dequant warps also saw this stage's activations arrive; the
+        // second wait then returns at once but keeps the TMA -> MMA ordering explicit
+        if (!tc::mbar_wait_warp(&tfull[slot], ph, &s_abort) || !tc::mbar_wait_warp(&fb[slot], ph, &s_abort)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc::mma_commit(&acc_full[b]);
+        tc::tc_fence_after();
+        const uint64_t bd0 = tc::sdesc_sw128(tc::smem_u32(sB + slot * kNT * 128));
+        const uint32_t a0 = tmem + 256 + (gs % J) * (NA * 32);
+#pragma unroll
+        for (int kk = 0; kk < kKS / 16; ++kk) {
+#pragma unroll
+          for (int m = 0; m < NA; ++m)
+            tc::mma_ts_elect(tmem + dcol0 + (KIND == 0 ? m * 128 : 0), a0 + m * 32 + kk * 8,
+                             bd0 + (uint64_t)(kk * 2), idesc, (s > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit_elect(&sdone[slot]);
       }
-      if (!ok) give_up();
-      tc::mma_commit(&fin);  // completes when every MMA issued above has finished
+      if (!ok) break;
+      tc::mma_commit_elect(&acc_full[b]);
+    }
+    if (!ok && lane == 0) give_up();
+    __syncwarp();
+    tc::mma_commit_elect(&fin);  // completes when every MMA issued above has finished
+    if (lane == 0) {
       volatile int never = 0;
       tc::mbar_wait(&fin, 0, &never, 2000000000ll);
     }
@@ -251,20 +257,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const CUtensorMap* mq = sh ? &mq_s : &mq_r;
         const CUtensorMap* ms = sh ? &ms_s : &ms_r;
         const int r0 = (sh ? 0 : grp * rows_per_expert) + blk * kBM;
-        const int sb = it & 1;
-        // the item's scales: their own barrier, since one dequant team never waits on the first stage
-        if (!tc::mbar_wait(&sc_empty[sb], ((it >> 1) & 1) ^ 1, &s_abort)) { ok = false; break; }
-        tc::mbar_arrive_expect_tx(&sc_full[sb], NA * kBM * G * 2);
-#pragma unroll
-        for (int m = 0; m < NA; ++m)
-          tc::tma_load_2d(sS + (sb * NA + m) * kBM * G * 2, ms, 0, r0 + m * g.f, &sc_full[sb]);
         for (int a = 0; a < KAS; ++a, ++as) {
           const int slot = as % kAStages;
           if (!tc::mbar_wait(&ea[slot], ((as / kAStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(&fa[slot], NA * kBM * 128);
+          tc::mbar_arrive_expect_tx(&fa[slot], NA * kBM * (128 + kScB));
 #pragma unroll
-          for (int m = 0; m < NA; ++m)
+          for (int m = 0; m < NA; ++m) {
             tc::tma_load_2d(sA + (slot * NA + m) * kBM * 128, mq, a * 128, r0 + m * g.f, &fa[slot]);
+            tc::tma_load_2d(sS + (slot * NA + m) * kBM * kScB, ms, a * (kKA / 32), r0 + m * g.f, &fa[slot]);
+          }
         }
       }
       if (!ok) give_up();
@@ -280,8 +281,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int tile = item / nblk;
         const int brow = g.tile_row[tile];
         for (int s = 0; s < KS; ++s, ++gs) {
-          const int slot = gs % kBStages;
-          if (!tc::mbar_wait(&eb[slot], ((gs / kBStages) & 1) ^ 1, &s_abort)) { ok = false; break; }
+          const int slot = gs % BS;
+          if (!tc::mbar_wait(&sdone[slot], ((gs / BS) & 1) ^ 1, &s_abort)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&fb[slot], kNT * 128);
           tc::tma_load_2d(sB + slot * kNT * 128, &mb, s * kKS, brow, &fb[slot]);
         }
@@ -299,110 +300,147 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     const int swz = row & 7;  // 128-byte swizzle of the int4 rows: 16-byte chunk c sits at c ^ (row % 8)
-    uint32_t gs = 0, it = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+    // Epilogue of one finished item: accumulators -> registers, release them to the MMA, then the
+    // math and the global stores.  (a, w) of this thread's token column (down GEMM) were loaded
+    // when the item started.
+    auto epilogue = [&](int item, uint32_t eit, int ea_id, float ew) -> bool {
       const int tile = item / nblk, blk = item % nblk;
       const int n = g.tile_n[tile], row0 = g.tile_row[tile];
-      const int sb = it & 1;
-      const uint8_t* srow = sS + ((sb * NA + (KIND == 0 ? m : 0)) * kBM + row) * G * 2;
-      if (!tc::mbar_wait(&sc_full[sb], (it >> 1) & 1, &s_abort)) {
-        ok = false;
-        break;
+      const int b = eit % NB;
+      if (!tc::mbar_wait_warp(&acc_full[b], (eit / NB) & 1, &s_abort)) return false;
+      tc::tc_fence_after();
+      const int cb = grp * 32;
+      if (KIND == 0) {
+        // h = silu(gate) * up for 32 token columns, in two halves of 16 to bound register use
+        __half hv[32];
+        bool range_bad = false;
+        if (cb < n) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t gv[16], uv[16];
+            tc::tmem_ld16(tmem + lane_base + cb + hh * 16, gv);
+            tc::tmem_ld16(tmem + lane_base + 128 + cb + hh * 16, uv);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const float h = silu_fast(__uint_as_float(gv[jj])) * __uint_as_float(uv[jj]);
+              range_bad |= !(fabsf(h) <= 65504.f) && cb + hh * 16 + jj < n;
+              hv[hh * 16 + jj] = __float2half_rn(h);
+            }
+          }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
+        if (cb < n) {
+          const int fidx = blk * kBM + row;
+          const int fpos = (fidx & ~7) | inv_perm8(fidx & 7);
+          __half* hp = g.h16 + (size_t)(row0 + cb) * g.f + fpos;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            if (cb + jj < n) hp[(size_t)jj * g.f] = hv[jj];
+          if (range_bad) atomicOr(g.status, kStatusRange);
+        }
+      } else {
+        uint32_t ov[32];
+        if (cb < n) {
+          tc::tmem_ld32(tmem + lane_base + b * 128 + cb, ov);
+          tc::tmem_wait_ld();
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
+        if (cb < n) {
+          const int jrow = blk * kBM + row;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int a_jj = __shfl_sync(0xffffffffu, ea_id, jj);
+            const float w_jj = __shfl_sync(0xffffffffu, ew, jj);
+            if (cb + jj < n) g.P[(size_t)a_jj * g.d + jrow] = __float2bfloat16_rn(w_jj * __uint_as_float(ov[jj]));
+          }
+        }
+      }
+      return true;
+    };
+
+    uint32_t gs = 0, it = 0;
+    bool ok = true;
+    // the finished item whose epilogue is still due: it runs once the dequant is `lag` stages into
+    // the next item, by which time the item's MMAs are (nearly) done and the MMA has stages queued.
+    // With one accumulator buffer the lag must not exceed J, or the dequant would wait on TMEM A
+    // stages that only the next item's MMAs (blocked on this epilogue) can free.
+    const uint32_t lag = (uint32_t)min(J, KS - 1);  // KS - 1: the epilogue always falls inside the next item
+    int p_item = -1, p_a = 0;
+    uint32_t p_it = 0, p_end = 0;
+    float p_w = 0.f;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      const int tile = item / nblk;
+      int c_a = 0;
+      float c_w = 0.f;
+      if (KIND == 1) {
+        // assignment id and weight of this thread's token column, for the epilogue
+        const int n = g.tile_n[tile], rr = g.tile_row[tile] + grp * 32 + lane;
+        if (grp * 32 + lane < n) {
+          c_a = rr < g.n_assign ? g.perm[rr] : g.T * g.K + (rr - g.n_assign);
+          c_w = rr < g.n_assign ? g.topk_w[c_a] : 1.f;
+        }
       }
       for (int s = 0; s < KS; ++s, ++gs) {
-        if ((int)(gs & 1) != team) {
-          if (s == KS - 1 && lane == 0) tc::mbar_arrive(&sc_empty[sb]);  // done with this item's scales
-          continue;
+        if (p_item >= 0 && gs >= p_end + lag) {
+          if (!epilogue(p_item, p_it, p_a, p_w)) { ok = false; break; }
+          p_item = -1;
         }
+        if ((int)(gs & 1) != team) continue;
         const uint32_t as = gs / kSub;  // weight stage (continuous across items: K % 256 == 0)
         const int sub_k = gs % kSub;   // which 64-K part of it
-        const int aslot = as % kAStages, j = gs % J;
-        if (!tc::mbar_wait(&fa[aslot], (as / kAStages) & 1, &s_abort)) { ok = false; break; }
-        if (!tc::mbar_wait(&tempty[j], ((gs / J) & 1) ^ 1, &s_abort)) {
+        const int aslot = as % kAStages, slot = gs % BS, j = gs % J;
+        // TMEM A stage j is free once the MMAs of stage gs - J have finished
+        if (!tc::mbar_wait(&fa[aslot], (as / kAStages) & 1, &s_abort) ||
+            (gs >= (uint32_t)J && !tc::mbar_wait(&sdone[(gs - J) % BS], ((gs - J) / BS) & 1, &s_abort))) {
           ok = false;
           break;
         }
         const uint8_t* arow = sA + ((aslot * NA + m) * kBM + row) * 128;
-        auto scale_at = [&](int grp_idx) -> __half2 {
-          const int o = grp_idx * 2;
-          const int off = g.sc_sw128 ? ((((o >> 4) ^ (row & 7)) << 4) | (o & 15)) : o;
-          const __half s1 = *reinterpret_cast<const __half*>(srow + off);
-          return __halves2half2(s1, s1);
-        };
+        // this row's two scales of the stage's 64 K (groups 2*sub_k, 2*sub_k + 1 of the weight stage)
+        const uint32_t sc2 = *reinterpret_cast<const uint32_t*>(sS + ((aslot * NA + m) * kBM + row) * kScB + sub_k * 4);
+        const __half2 scp = *reinterpret_cast<const __half2*>(&sc2);
         if (KIND == 0) {
           // the whole 64-K stage of matrix m: two 16-byte chunks
           uint32_t v[32];
           const uint4 q0 = *reinterpret_cast<const uint4*>(arow + (((2 * sub_k) ^ swz) << 4));
           const uint4 q1 = *reinterpret_cast<const uint4*>(arow + (((2 * sub_k + 1) ^ swz) << 4));
-          dequant32(q0, scale_at(2 * s), v);
-          dequant32(q1, scale_at(2 * s + 1), v + 16);
+          dequant32(q0, __low2half2(scp), v);
+          dequant32(q1, __high2half2(scp), v + 16);
           tc::tmem_st32(tmem + lane_base + 256 + j * (NA * 32) + m * 32, v);
         } else {
           // one 16-byte chunk (32 K) of the stage
           uint32_t v[16];
           const uint4 qq = *reinterpret_cast<const uint4*>(arow + (((2 * sub_k + sub) ^ swz) << 4));
-          dequant32(qq, scale_at(2 * s + sub), v);
+          dequant32(qq, sub ? __high2half2(scp) : __low2half2(scp), v);
           tc::tmem_st16(tmem + lane_base + 256 + j * 32 + sub * 16, v);
         }
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
+        int fb_ok = 1;
         if (lane == 0) {
-          tc::mbar_arrive(&tfull[j]);
+          fb_ok = tc::mbar_wait(&fb[slot], (gs / BS) & 1, &s_abort) ? 1 : 0;  // activations landed too
+          tc::mbar_arrive(&tfull[slot]);
           if (sub_k >= kSub - 2) tc::mbar_arrive(&ea[aslot]);  // this warp's last part of the weight stage
-          if (s == KS - 1) tc::mbar_arrive(&sc_empty[sb]);
+        }
+        if (!__shfl_sync(0xffffffffu, fb_ok, 0)) {  // keep the warp converged for the .aligned ops
+          ok = false;
+          break;
         }
       }
       if (!ok) break;
-      // epilogue
-      const int b = it % NB;
-      if (!tc::mbar_wait(&acc_full[b], (it / NB) & 1, &s_abort)) { ok = false; break; }
-      tc::tc_fence_after();
-      bool range_bad = false;
-      for (int cb = grp * 32; cb < grp * 32 + 32 && cb < n; cb += 32) {
-        if (KIND == 0) {
-          uint32_t gv[32], uv[32];
-          tc::tmem_ld32(tmem + lane_base + cb, gv);
-          tc::tmem_ld32(tmem + lane_base + 128 + cb, uv);
-          tc::tmem_wait_ld();
-          const int fidx = blk * kBM + row;
-          const int fpos = (fidx & ~7) | inv_perm8(fidx & 7);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int nn = cb + jj;
-            if (nn < n) {
-              const float hv = silu_fast(__uint_as_float(gv[jj])) * __uint_as_float(uv[jj]);
-              range_bad |= !(fabsf(hv) <= 65504.f);
-              g.h16[(size_t)(row0 + nn) * g.f + fpos] = __float2half_rn(hv);
-            }
-          }
-        } else {
-          // assignment id and weight of token column cb + lane, shared with the warp by shuffles
-          const int rr = row0 + cb + lane;
-          int my_a = 0;
-          float my_w = 0.f;
-          if (cb + lane < n) {
-            my_a = rr < g.n_assign ? g.perm[rr] : g.T * g.K + (rr - g.n_assign);
-            my_w = rr < g.n_assign ? g.topk_w[my_a] : 1.f;
-          }
-          uint32_t ov[32];
-          tc::tmem_ld32(tmem + lane_base + b * 128 + cb, ov);
-          tc::tmem_wait_ld();
-          const int jrow = blk * kBM + row;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int a_jj = __shfl_sync(0xffffffffu, my_a, jj);
-            const float w_jj = __shfl_sync(0xffffffffu, my_w, jj);
-            if (cb + jj < n) g.P[(size_t)a_jj * g.d + jrow] = __float2bfloat16_rn(w_jj * __uint_as_float(ov[jj]));
-          }
-        }
-      }
-      if (range_bad) atomicOr(g.status, kStatusRange);
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
+      p_item = item;
+      p_it = it;
+      p_end = gs;
+      p_a = c_a;
+      p_w = c_w;
     }
+    if (ok && p_item >= 0) ok = epilogue(p_item, p_it, p_a, p_w);
     if (!ok) give_up();
   }
   tc::tc_fence_before();
@@ -526,11 +564,11 @@ static int g_sms = 148;
 
 constexpr int kGemmSmemMax = 226 * 1024;
 
-static size_t gemm_smem_bytes(int kind, int d, int f) {
-  const int NA = kind == 0 ? 2 : 1;
-  const int G = (kind == 0 ? d : f) / 32;
-  return 1024 + (size_t)kBStages * kNT * 128 + (size_t)kAStages * NA * kBM * 128 + (size_t)2 * NA * kBM * G * 2;
+template <int KIND>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 + (size_t)Stages<KIND>::B * kNT * 128 + (size_t)kAStages * Stages<KIND>::NA * kBM * (128 + kScB);
 }
+static_assert(gemm_smem_bytes<0>() <= kGemmSmemMax && gemm_smem_bytes<1>() <= kGemmSmemMax, "shared memory");
 
 cudaError_t gemm_kernels_init(int num_sms) {
   g_sms = num_sms;
@@ -541,15 +579,14 @@ cudaError_t gemm_kernels_init(int num_sms) {
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  // the largest dynamic size any supported shape needs (d <= 8192, f <= 8192 keep it under the limit)
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemMax);
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem_bytes<0>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemMax);
+  return cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem_bytes<1>());
 }
 
 bool gemm_shape_ok(int d, int f) {
-  return d % kKA == 0 && f % kKA == 0 && d / 32 <= 256 && f / 32 <= 256 &&
-         gemm_smem_bytes(0, d, f) <= kGemmSmemMax && gemm_smem_bytes(1, d, f) <= kGemmSmemMax;
+  return d % kKA == 0 && f % kKA == 0;
 }
 
 size_t gemm_workspace_bytes(int T, int d, int f, int E, int K) {
@@ -587,33 +624,31 @@ static cudaError_t make_map(CUtensorMap* m, const void* base, CUtensorMapDataTyp
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tensor maps of one layer's int4 planes (box: 128 rows x 32 bytes) and fp16 scale planes
-// (box: 128 rows x the whole row of scales).
+// Tensor maps of one layer's int4 planes (box: 128 rows x 128 bytes = 256 K, 128-byte swizzle) and
+// fp16 scale planes (box: 128 rows x the 8 scales of the same 256 K, no swizzle).
 cudaError_t gemm_build_maps(void* maps, int E, int d, int f, int has_shared, const void* gu_q, const void* gu_s,
                             const void* dn_q, const void* dn_s, const void* sh_gu_q, const void* sh_gu_s,
                             const void* sh_dn_q, const void* sh_dn_s) {
   if (!g_encode) return cudaErrorNotSupported;
   GemmMaps* mp = static_cast<GemmMaps*>(maps);
   const int Gd = d / 32, Gf = f / 32;
-  const CUtensorMapSwizzle sgu = Gd * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  const CUtensorMapSwizzle sdn = Gf * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  mp->gu_s_sw128 = sgu == CU_TENSOR_MAP_SWIZZLE_128B;
-  mp->dn_s_sw128 = sdn == CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle sgu = CU_TENSOR_MAP_SWIZZLE_NONE, sdn = CU_TENSOR_MAP_SWIZZLE_NONE;
+  const uint32_t sbox = kScB / 2;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
   if ((e = make_map(&mp->gu_q, gu_q, U8, d / 2, (uint64_t)E * 2 * f, d / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
-  if ((e = make_map(&mp->gu_s, gu_s, F16, Gd, (uint64_t)E * 2 * f, Gd * 2, Gd, kBM, sgu))) return e;
+  if ((e = make_map(&mp->gu_s, gu_s, F16, Gd, (uint64_t)E * 2 * f, Gd * 2, sbox, kBM, sgu))) return e;
   if ((e = make_map(&mp->dn_q, dn_q, U8, f / 2, (uint64_t)E * d, f / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
-  if ((e = make_map(&mp->dn_s, dn_s, F16, Gf, (uint64_t)E * d, Gf * 2, Gf, kBM, sdn))) return e;
+  if ((e = make_map(&mp->dn_s, dn_s, F16, Gf, (uint64_t)E * d, Gf * 2, sbox, kBM, sdn))) return e;
   const void* sgq = has_shared ? sh_gu_q : gu_q;  // maps must be valid even when unused
   const void* sgs = has_shared ? sh_gu_s : gu_s;
   const void* sdq = has_shared ? sh_dn_q : dn_q;
   const void* sds = has_shared ? sh_dn_s : dn_s;
   if ((e = make_map(&mp->sh_gu_q, sgq, U8, d / 2, 2 * f, d / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
-  if ((e = make_map(&mp->sh_gu_s, sgs, F16, Gd, 2 * f, Gd * 2, Gd, kBM, sgu))) return e;
+  if ((e = make_map(&mp->sh_gu_s, sgs, F16, Gd, 2 * f, Gd * 2, sbox, kBM, sgu))) return e;
   if ((e = make_map(&mp->sh_dn_q, sdq, U8, f / 2, d, f / 2, kKA / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B))) return e;
-  if ((e = make_map(&mp->sh_dn_s, sds, F16, Gf, d, Gf * 2, Gf, kBM, sdn))) return e;
+  if ((e = make_map(&mp->sh_dn_s, sds, F16, Gf, d, Gf * 2, sbox, kBM, sdn))) return e;
   return cudaSuccess;
 }
 
@@ -666,12 +701,10 @@ cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, const v
   g.tile_row = w.tile_row;
   g.tile_n = w.tile_n;
   g.status = a.status;
-  g.sc_sw128 = mp.gu_s_sw128;
-  gemm_kernel<0><<<g_sms, kGemmThreads, gemm_smem_bytes(0, d, f), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s,
+  gemm_kernel<0><<<g_sms, kGemmThreads, gemm_smem_bytes<0>(), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s,
                                                                         am.xs);
   if (mid) record_timing_event(mid, st);
-  g.sc_sw128 = mp.dn_s_sw128;
-  gemm_kernel<1><<<g_sms, kGemmThreads, gemm_smem_bytes(1, d, f), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s,
+  gemm_kernel<1><<<g_sms, kGemmThreads, gemm_smem_bytes<1>(), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s,
                                                                         am.hs);
   if (mid2) record_timing_event(mid2, st);
   const size_t nblk8 = (size_t)T * d / 8;
@@ -680,4 +713,3 @@ cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, const v
 }
 
 }  // namespace moe
-
