@@ -148,11 +148,16 @@ moe_status moe_get_device_status(moe_handle h, void* stream);
 /* Free the workspace and any captured graphs.  Synchronises the device first. */
 moe_status moe_destroy(moe_handle h);
 
-/* Options.  MOE_OPT_GEMV_MAX_TOKENS: calls with T <= value run the split-K GEMV experts, larger T
- * the tensor-core grouped GEMM (value 0..16; default 16; the grouped GEMM needs INT4 weights with
- * d % 256 == 0 and f % 256 == 0, otherwise the value is clamped to 16).  Returns the option's
- * value in effect, or a negative moe_status on error. */
-enum { MOE_OPT_GEMV_MAX_TOKENS = 1 };
+/* Options (each returns the value in effect, or a negative moe_status on error; changing one
+ * drops the handle's captured stack graphs).
+ * MOE_OPT_FUSED_MAX_TOKENS: calls with T <= value run the whole layer (router, selection,
+ *   dispatch, experts, combine) as one cooperative kernel with grid-wide barriers (value 0..8,
+ *   0 = off; default 4; INT4 weights with d % 256 == 0, f % 256 == 0, f <= 1024, d <= 4096; the
+ *   value in effect is clamped to what the shared-memory plan of the shape allows).
+ * MOE_OPT_GEMV_MAX_TOKENS: other calls with T <= value run the split-K GEMV experts, larger T the
+ *   tensor-core grouped GEMM (value 0..16; default 4; the grouped GEMM needs INT4 weights with
+ *   d % 256 == 0 and f % 256 == 0, otherwise the value is clamped to 16). */
+enum { MOE_OPT_GEMV_MAX_TOKENS = 1, MOE_OPT_FUSED_MAX_TOKENS = 2 };
 int moe_set_option(moe_handle h, int option, int value);
 
 /* Stage timing (tracing).  moe_timing_enable(h, n) creates 5*n CUDA events; afterwards every

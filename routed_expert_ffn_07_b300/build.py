@@ -12,8 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe_b300.so")
-SOURCES = ["api.cu", "router.cu", "experts_gemv.cu", "experts_gemm.cu", "gen.cu"]
-HEADERS = ["common.cuh", "tc_ptx.cuh"]
+SOURCES = ["api.cu", "router.cu", "experts_gemv.cu", "experts_gemm.cu", "decode_fused.cu", "gen.cu"]
+HEADERS = ["common.cuh", "tc_ptx.cuh", "topk.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

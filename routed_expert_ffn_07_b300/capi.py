@@ -19,6 +19,7 @@ MOE_ACT_F32, MOE_ACT_BF16 = 0, 1
 MOE_W_F32, MOE_W_INT4_G32 = 0, 1
 SMALL_T = 16  # T <= SMALL_T can run the split-K GEMV path
 MOE_OPT_GEMV_MAX_TOKENS = 1
+MOE_OPT_FUSED_MAX_TOKENS = 2
 
 
 class MoeError(RuntimeError):

@@ -20,6 +20,10 @@ cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, 
 size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K);
 size_t gemv_smem_dn(int T, int K, int E);
 cudaError_t gemm_kernels_init(int num_sms);
+cudaError_t fused_kernels_init(int num_sms);
+bool fused_shape_ok(int T, int d, int f, int E, int K);
+cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, unsigned long long* grid_bar,
+                                cudaStream_t st);
 size_t gemm_workspace_bytes(int max_tokens, int d, int f, int E, int K);
 bool gemm_shape_ok(int d, int f);
 void* gemm_maps_new();
@@ -33,6 +37,8 @@ cudaError_t gemm_build_act_maps(void* ws, int T, int d, int f, int E, int K, voi
 size_t gemm_act_maps_bytes();
 constexpr int kDispatchBlockHost = 256;
 constexpr int kTimingEvents = 5;  // before route, after route, after stage A, after stage B, end
+constexpr int kFusedMaxTokensHost = 8;    // the one-launch decode layer's limit
+constexpr int kFusedDefaultTokens = 4;    // decode and 1 + 3 verify
 }  // namespace moe
 
 using namespace moe;
@@ -75,7 +81,9 @@ struct moe_ctx {
   std::map<int, cudaGraphExec_t> graphs;
   bool gemm_ok = false;          // tensor-core path available for this config
   void* act_maps = nullptr;      // TMA descriptors of the workspace activation buffers
-  int gemv_max_tokens = kSmallT; // T <= this runs the GEMV experts
+  int gemv_max_tokens = 4;       // T <= this runs the GEMV experts (when the grouped GEMM is available)
+  int fused_max_tokens = 0;      // T <= this runs the one-launch decode layer (0: off)
+  unsigned long long* grid_bar = nullptr;  // grid-barrier counter of the one-launch decode layer
   // stage timing
   std::vector<cudaEvent_t> tev;
   int t_next = 0;
@@ -83,6 +91,15 @@ struct moe_ctx {
 };
 
 static size_t act_size(int act) { return act == MOE_ACT_BF16 ? 2 : 4; }
+
+// Largest T <= want (and <= max_tokens) that the one-launch decode layer serves for this config.
+static int fused_limit(const moe_config& c, int want) {
+  int best = 0;
+  if (c.wfmt == MOE_W_INT4_G32)
+    for (int t = 1; t <= want && t <= c.max_tokens; ++t)
+      if (fused_shape_ok(t, c.d, c.f, c.n_experts, c.top_k)) best = t;
+  return best;
+}
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 
@@ -152,11 +169,14 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   }
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   h->gemm_ok = c.wfmt == MOE_W_INT4_G32 && gemm_shape_ok(c.d, c.f);
+  if (!h->gemm_ok) h->gemv_max_tokens = kSmallT;
   if (route_kernels_init() != cudaSuccess || gemv_kernels_init(h->num_sms) != cudaSuccess ||
-      (h->gemm_ok && gemm_kernels_init(h->num_sms) != cudaSuccess)) {
+      (h->gemm_ok && gemm_kernels_init(h->num_sms) != cudaSuccess) ||
+      (c.wfmt == MOE_W_INT4_G32 && fused_kernels_init(h->num_sms) != cudaSuccess)) {
     delete h;
     return MOE_ERR_CUDA;
   }
+  h->fused_max_tokens = fused_limit(c, kFusedDefaultTokens);
 
   const int T = c.max_tokens, E = c.n_experts, K = c.top_k, d = c.d, f = c.f;
   const size_t as = act_size(c.act);
@@ -175,6 +195,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   sz[n++] = up256((size_t)E * 16);                    // slot table
   sz[n++] = up256(4);                                 // ticket
   sz[n++] = up256(4);                                 // status
+  sz[n++] = up256(8);                                 // grid barrier
   sz[n++] = up256((size_t)h->nblocks_max * E * 4);    // blockhist
   const int TS = T < kSmallT ? T : kSmallT;
   sz[n++] = up256((size_t)(TS * K + TS) * f * 4);     // h (GEMV path)
@@ -205,6 +226,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   h->slots = reinterpret_cast<int4*>(p); p += sz[i++];
   h->ticket = reinterpret_cast<unsigned*>(p); p += sz[i++];
   h->status = reinterpret_cast<unsigned*>(p); p += sz[i++];
+  h->grid_bar = reinterpret_cast<unsigned long long*>(p); p += sz[i++];
   h->blockhist = reinterpret_cast<int32_t*>(p); p += sz[i++];
   h->h = reinterpret_cast<float*>(p); p += sz[i++];
   h->gemm_ws = sz[i] ? p : nullptr; p += sz[i++];
@@ -338,6 +360,15 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
   cudaError_t e;
   if (ev && (e = record_timing_event(ev[0], st)) != cudaSuccess) return e;
   RouteArgs ra = make_route_args(h, layer, x, T, prenorm, h->stats + layer);
+  if (T <= h->fused_max_tokens) {
+    // one launch for the whole layer; its stages are not separated (all of it counts as "route")
+    ExpertArgs ea = make_expert_args(h, layer, x, T, y, resid);
+    e = launch_decode_fused(ra, ea, h->grid_bar, st);
+    if (e != cudaSuccess) return e;
+    for (int k = 1; ev && k < kTimingEvents; ++k)
+      if ((e = record_timing_event(ev[k], st)) != cudaSuccess) return e;
+    return cudaSuccess;
+  }
   const int nb = (T * h->cfg.top_k + kDispatchBlockHost - 1) / kDispatchBlockHost;
   e = launch_route(ra, nb, st);
   if (e != cudaSuccess) return e;
@@ -492,7 +523,11 @@ moe_status moe_get_device_status(moe_handle h, void* stream) {
   unsigned v = 0;
   CUDA_TRY(cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
   if (v) CUDA_TRY(cudaMemset(h->status, 0, 4));
-  if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kStatusTimeout) {
+    // a grid barrier that gave up may hold a partial count: start the next launch from zero
+    CUDA_TRY(cudaMemset(h->grid_bar, 0, 8));
+    return MOE_ERR_TIMEOUT;
+  }
   if (v) return MOE_ERR_DEVICE;
   return MOE_OK;
 }
@@ -505,6 +540,13 @@ int moe_set_option(moe_handle h, int option, int value) {
     for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);  // captured graphs used the old path
     h->graphs.clear();
     return h->gemv_max_tokens;
+  }
+  if (option == MOE_OPT_FUSED_MAX_TOKENS) {
+    if (value < 0 || value > kFusedMaxTokensHost) return -(int)MOE_ERR_INVALID_ARG;
+    h->fused_max_tokens = fused_limit(h->cfg, value);
+    for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+    h->graphs.clear();
+    return h->fused_max_tokens;
   }
   return -(int)MOE_ERR_INVALID_ARG;
 }

@@ -82,6 +82,13 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// int4 code byte b (0..3) of `lo` (offset-binary nibbles o = q + 8, one per byte) as the fp32
+// value 0.5 + o/256: the byte lands in bits 16..23 under the exponent of 0.5, and o < 16 only
+// touches mantissa bits 16..19.
+__device__ __forceinline__ float v_lo(uint32_t lo, int b) {
+  return __int_as_float(__byte_perm(lo, 0x3F000000u, 0x7054u | (b << 8)));
+}
+
 // Record a stage-timing event: inside stream capture it must become an external event node,
 // outside capture it is a plain record.
 inline cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t st) {

@@ -67,9 +67,6 @@ __device__ __forceinline__ SlotInfo slot_tokens(const ExpertArgs& a, int s, int 
   return si;
 }
 
-__device__ __forceinline__ float v_lo(uint32_t lo, int b) {
-  return __int_as_float(__byte_perm(lo, 0x3F000000u, 0x7054u | (b << 8)));
-}
 
 // ------------------------------------------------------------------ gate/up, int4
 // Persistent: one block per SM, 16 warps.  The (gate row, up row) pairs of all slots are numbered

@@ -15,6 +15,7 @@
 
 #include "../../include/moe.h"
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -112,27 +113,6 @@ __device__ void topk_warp(const float* lg, int E, int K, int32_t* out_idx, float
     out_w[lane] = sp[lane] / s;
   }
   __syncwarp();
-}
-
-// Descending bitonic sort of the first N entries of kv (N a power of two), fully unrolled.
-template <int N>
-__device__ __forceinline__ void bitonic_desc(uint64_t (&kv)[32]) {
-#pragma unroll
-  for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-#pragma unroll
-      for (int i = 0; i < N; ++i) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t x0 = kv[i], x1 = kv[ixj];
-          const bool sw = ((i & k) == 0) ? (x0 < x1) : (x0 > x1);
-          kv[i] = sw ? x1 : x0;
-          kv[ixj] = sw ? x0 : x1;
-        }
-      }
-    }
-  }
 }
 
 // ------------------------------------------------------------------ small T (fused, one launch)
@@ -270,58 +250,15 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  // ---- last block: softmax + top-K per token, one warp per token.  Each lane sorts its (up to 32)
-  // logits once; a round then takes the warp maximum of the lanes' heads with two redux
-  // reductions (largest order-preserving key, then lowest expert index among equal keys).
+  // ---- last block: softmax + top-K per token, one warp per token (logits held in registers).
   for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
   for (int t = warp; t < T; t += kRouterWarps) {
-    uint64_t kv[32];  // (order-preserving key of the logit) << 32 | (31 - j); larger = better
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int ej = lane + 32 * j;
-      const float v = ej < E ? __ldcg(a.logits + (size_t)t * E + ej) : -INFINITY;
-      m = fmaxf(m, v);
-      const uint32_t u = __float_as_uint(v);
-      const uint32_t key = ej < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-      kv[j] = ((uint64_t)key << 32) | (uint32_t)(31 - j);
-    }
-    m = warp_max(m);
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int ej = lane + 32 * j;
-      if (ej < E) z += expf(__ldcg(a.logits + (size_t)t * E + ej) - m);
-    }
-    z = warp_sum(z);
-    // descending sort of the lane's keys (bitonic network; 16 keys per lane when E <= 512)
-    if (E <= 512)
-      bitonic_desc<16>(kv);
-    else
-      bitonic_desc<32>(kv);
-    int head = 0;
-    int my_i = 0;
-    for (int k = 0; k < K; ++k) {
-      uint64_t hk = 0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j == head) hk = kv[j];
-      const uint32_t key = (uint32_t)(hk >> 32);
-      const uint32_t best = __reduce_max_sync(0xffffffffu, key);
-      const int e_mine = lane + 32 * (31 - (int)(hk & 31u));
-      const uint32_t cand = (key == best && key != 0u) ? (uint32_t)e_mine : 0xffffffffu;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-      if (lane == (int)(win & 31u)) ++head;
-      if (lane == k) my_i = (int)win;
-    }
-    // probabilities of the kept experts, renormalised in ascending k
-    float my_p = 0.f;
-    if (lane < K) my_p = expf(__ldcg(a.logits + (size_t)t * E + my_i) - m) / z;
-    float psum = 0.f;
-    for (int k = 0; k < K; ++k) psum += __shfl_sync(0xffffffffu, my_p, k);
+    int my_i;
+    float my_w;
+    topk_token(a.logits + (size_t)t * E, E, K, my_i, my_w);
     if (lane < K) {
       a.idx[(size_t)t * K + lane] = my_i;
-      a.w[(size_t)t * K + lane] = my_p / psum;
+      a.w[(size_t)t * K + lane] = my_w;
       idx_s[t * K + lane] = my_i;
     }
   }

@@ -20,16 +20,19 @@ def run_layer(h, wl, weights, x_np, T, layer=0, gen_layer=0):
     torch = _torch()
     from routed_expert_ffn_07_b300 import capi
     K, E = wl.K, wl.E
+    n_layers = weights["router"].shape[0]
     x = to_torch_act(x_np)
     idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
     w = torch.empty(T * K, dtype=torch.float32, device="cuda")
     offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
-    capi.moe_route(h, layer, x, T, idx, w, offs, perm)
     y = torch.empty_like(x)
     capi.moe_layer_forward(h, layer, x, T, y)
     torch.cuda.synchronize()
     assert capi.moe_get_device_status(h) == 0
+    n_active_fwd = int(capi.moe_get_active_counts(h, n_layers)[layer])  # from the forward's own routing
+    capi.moe_route(h, layer, x, T, idx, w, offs, perm)
+    torch.cuda.synchronize()
     Wr = weights["router"][layer].cpu().numpy()
     bias = None if weights["bias"] is None else weights["bias"][layer].cpu().numpy()
     logits, idx_ref, w_ref, gap = oracle.route(x_np, Wr, bias, K)
@@ -39,6 +42,8 @@ def run_layer(h, wl, weights, x_np, T, layer=0, gen_layer=0):
     w_exp = oracle.weights_for(logits, idx_g)
     np.testing.assert_allclose(w.cpu().numpy().reshape(T, K), w_exp, rtol=0, atol=W_ATOL)
     used = sorted(set(idx_g.ravel().tolist()))
+    if not flagged:
+        assert n_active_fwd == len(used), "the forward pass routed differently"
     ex = host_experts(wl, gen_layer, used + ([E] if wl.shared else []))
     sh = ex.pop(E) if wl.shared else None
     y_ref, _, _ = oracle.layer(x_np, Wr, bias, ex, E, K, shared=sh, idx=idx_g)
@@ -163,7 +168,7 @@ def test_decode_layer_batch_sizes(decode_layer):
         run_layer(h, wl, wts, x[:T], T, layer=1, gen_layer=1)
 
 
-def _stack_parity(wl, sample_layers, gemv_max=None):
+def _stack_parity(wl, sample_layers, gemv_max=None, fused_max=None):
     torch = _torch()
     from routed_expert_ffn_07_b300 import capi
     wts = alloc_and_fill(wl)
@@ -171,6 +176,8 @@ def _stack_parity(wl, sample_layers, gemv_max=None):
     h = create_handle(wl, wts)
     if gemv_max is not None:
         capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gemv_max)
+    if fused_max is not None:
+        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, fused_max)
     try:
         x0 = inputs.gen_activations(wl.seed, T, d, "bf16")
         xa = to_torch_act(x0)
@@ -270,24 +277,67 @@ def test_invalid_arguments_rejected():
         capi.moe_destroy(h)
 
 
-@pytest.mark.parametrize("gemv_max", [0, 16])
-def test_decode_sizes_on_both_expert_paths(decode_layer, gemv_max):
-    """T <= 16 through the split-K GEMV experts and through the tensor-core grouped GEMM."""
+PATHS = {  # decode path -> (MOE_OPT_FUSED_MAX_TOKENS, MOE_OPT_GEMV_MAX_TOKENS)
+    "one_launch": (8, 16),
+    "gemv": (0, 16),
+    "tensor_core": (0, 0),
+}
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_decode_sizes_on_every_expert_path(decode_layer, path):
+    """T <= 16 through the one-launch layer (T <= 8), the split-K GEMV experts and the grouped GEMM."""
     from routed_expert_ffn_07_b300 import capi
     wl, wts, h = decode_layer
-    capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gemv_max)
+    fz, gv = PATHS[path]
+    got = capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, fz)
+    assert (got >= 4) if fz else (got == 0)  # the one-launch layer serves at least decode and 1 + 3 verify
+    capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gv)
     try:
         x = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=9)
-        for T in (1, 4, 16):
+        for T in (1, 2, 3, 4, 5, 8, 16):
             run_layer(h, wl, wts, x[:T], T, layer=2, gen_layer=2)
     finally:
-        capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 16)
+        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)
+        capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 4)
 
 
-def test_skewed_stack_on_tensor_core_path():
+def test_one_launch_layer_matches_gemv_path_closely(decode_layer):
+    """Same routing, same per-product arithmetic: the two decode paths agree to fp32 rounding."""
+    torch = _torch()
     from routed_expert_ffn_07_b300 import capi
+    wl, wts, h = decode_layer
+    x = to_torch_act(inputs.gen_activations(wl.seed, 4, wl.d, "bf16", layer=11))
+    out = {}
+    try:
+        for path in ("one_launch", "gemv"):
+            fz, gv = PATHS[path]
+            capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, fz)
+            capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gv)
+            y = torch.empty_like(x)
+            capi.moe_layer_forward(h, 1, x, 4, y)
+            torch.cuda.synchronize()
+            assert capi.moe_get_device_status(h) == 0
+            out[path] = y.float()
+    finally:
+        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)
+        capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 4)
+    a, b = out["one_launch"], out["gemv"]
+    # both round once to bf16 from fp32 sums taken in different orders: at most 2 bf16 ulps apart
+    assert torch.all((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-6)
+
+
+def test_verify_stack_on_gemv_path():
+    wl = WORKLOADS[3]
+    import dataclasses
+    wl_small = dataclasses.replace(wl, layers=8)
+    counts, flagged, worst = _stack_parity(wl_small, sample_layers=[0, 3, 7], fused_max=0, gemv_max=16)
+    assert all(10 <= c <= 40 for c in counts)
+
+
+def test_skewed_stack_on_gemv_path():
     wl = WORKLOADS[5]
     import dataclasses
     wl_small = dataclasses.replace(wl, layers=8)
-    counts, flagged, worst = _stack_parity(wl_small, sample_layers=[0, 3, 7], gemv_max=0)
+    counts, flagged, worst = _stack_parity(wl_small, sample_layers=[0, 3, 7], gemv_max=16)
     assert all(10 <= c <= 160 for c in counts)
