@@ -30,6 +30,34 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Sums N values (N = 2, 4 or 8) over the warp in five dependent shuffle steps in all: the first
+// log2(N) steps exchange halves of the value list (each lane keeps the half its lane bit selects),
+// the rest are a plain butterfly.  On return every lane holds the total of value index
+// (lane >> 2) & (N - 1) when N == 8, (lane >> 3) & 3 when N == 4, (lane >> 4) & 1 when N == 2,
+// i.e. value i's total sits in the lanes whose bits [5 - log2(N), 5) spell i.
+template <int N>
+__device__ __forceinline__ float warp_sum_multi(float (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+  float w[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = v[i];
+  int n = N;
+  int off = 16;
+#pragma unroll
+  for (; n > 1; n >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;  // keep the upper half of the list
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? w[i] : w[i + n / 2];
+      const float keep = up ? w[i + n / 2] : w[i];
+      w[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+#pragma unroll
+  for (; off > 0; off >>= 1) w[0] += __shfl_xor_sync(0xffffffffu, w[0], off);
+  return w[0];
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

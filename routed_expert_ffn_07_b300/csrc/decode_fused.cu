@@ -42,6 +42,8 @@ constexpr int kFzMaxT = 8;
 constexpr int kFzMaxStages = 8;
 constexpr int kFzSmemMax = 227 * 1024;
 constexpr unsigned kFzSpinLimit = 1u << 24;      // grid-barrier polls, at least 32 ns apart
+constexpr unsigned kFzProducerSleep = 200;        // ns between polls of the producer's waits
+constexpr unsigned kFzConsumerSleep = 64;         // ns between polls of a waiting consumer warp
 
 struct FusedArgs {
   const void* x;
@@ -100,14 +102,15 @@ __device__ __forceinline__ bool consumers_all(bool v) {
   return r != 0;
 }
 
-// Grid barrier on a 64-bit arrival counter that only ever increases.  One thread per CTA, after
-// the CTA's writes (consumers_sync): arrive returns the count that marks this barrier instance as
-// complete (all gridDim.x arrivals of one instance fall in one block of gridDim.x consecutive
-// values, since no CTA can arrive at the next instance before this one completes).
-__device__ __forceinline__ unsigned long long grid_arrive(unsigned long long* bar) {
+// Grid barrier on a 64-bit arrival counter that only ever increases.  At the start (after
+// griddepcontrol.wait) one thread per CTA reads the counter and rounds it down to a multiple of
+// gridDim.x: the previous launch's barriers are complete and fewer than gridDim.x arrivals of this
+// launch's first barrier can precede the read, so every CTA gets the same base.  Barrier i of the launch is
+// complete when the counter reaches base + (i + 1) * gridDim.x.  Arrival is a release reduction
+// (no reply awaited); the wait polls with acquire loads.
+__device__ __forceinline__ void grid_arrive(unsigned long long* bar) {
   __threadfence();
-  const unsigned long long old = atomicAdd(bar, 1ull);
-  return (old / gridDim.x + 1) * gridDim.x;
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
 }
 __device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigned long long target,
                                           volatile int* abort) {
@@ -119,13 +122,15 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigne
 }
 
 // ------------------------------------------------------------------ gate/up dot products
-// ROWS int4 rows (codes at q[r], fp16 scales at sc[r], all in shared memory) against TB tokens of
-// x' (group-interleaved [t][8][G] float4): lane-partial sums acc[r][tt], each x' load shared by
-// all ROWS rows.  Lane = 32-column groups lane, lane+32, ...
-template <int NG, int TB, int ROWS>
-__device__ __forceinline__ void rows_dot(const uint8_t* const (&q)[ROWS], const __half* const (&sc)[ROWS], int G,
-                                         const float4* xq, const float* xs136, const int (&tok)[TB],
-                                         float (&acc)[ROWS][TB], int lane) {
+// 2*NP int4 rows against TB tokens of x' (group-interleaved [t][8][G] float4), all in shared memory:
+// rows r < NP are gate rows p = r, rows r >= NP up rows p = r - NP, at gq/uq + min-clamped p*qrow
+// (rows p >= np repeat row 0), scales at gs/us + p*G.  Lane-partial sums acc[r][tt]; each x' load
+// is shared by all rows.  Lane = 32-column groups lane, lane+32, ...
+template <int NG, int TB, int NP>
+__device__ __forceinline__ void pairs_dot(const uint8_t* gq, const uint8_t* uq, const __half* gs, const __half* us,
+                                          size_t qrow, int np, int G, const float4* xq, const float* xs136,
+                                          const int (&tok)[TB], float (&acc)[2 * NP][TB], int lane) {
+  constexpr int ROWS = 2 * NP;
 #pragma unroll
   for (int r = 0; r < ROWS; ++r)
 #pragma unroll
@@ -136,7 +141,11 @@ __device__ __forceinline__ void rows_dot(const uint8_t* const (&q)[ROWS], const 
     if (g >= G) continue;
     uint4 wq[ROWS];
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) wq[r] = *reinterpret_cast<const uint4*>(q[r] + g * 16);
+    for (int r = 0; r < ROWS; ++r) {
+      const int p = r < NP ? r : r - NP;
+      const int pp = p < np ? p : 0;
+      wq[r] = *reinterpret_cast<const uint4*>((r < NP ? gq : uq) + pp * qrow + g * 16);
+    }
     float part[ROWS][TB];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r)
@@ -177,15 +186,20 @@ __device__ __forceinline__ void rows_dot(const uint8_t* const (&q)[ROWS], const 
     for (int tt = 0; tt < TB; ++tt) {
       const float x136 = xs136[tok[tt] * G + g];
 #pragma unroll
-      for (int r = 0; r < ROWS; ++r) acc[r][tt] = fmaf(__half2float(sc[r][g]), part[r][tt] - x136, acc[r][tt]);
+      for (int r = 0; r < ROWS; ++r) {
+        const int p = r < NP ? r : r - NP;
+        const int pp = p < np ? p : 0;
+        const float sc = __half2float((r < NP ? gs : us)[(size_t)pp * G + g]);
+        acc[r][tt] = fmaf(sc, part[r][tt] - x136, acc[r][tt]);
+      }
     }
   }
 }
 
-// h[asg][i0 + p] = silu(gate_p . x) * (up_p . x), p < np <= 4, for the n tokens of one slot (the
+// h[asg][i0 + p] = silu(gate_p . x) * (up_p . x), p < np <= NP, for the n tokens of one slot (the
 // assignments at perm_s[pbase..], or all T tokens of the shared expert).  Gate rows at gq +
 // p*qrow, up rows at uq + p*qrow, their scales at gs + p*G / us + p*G (shared memory).
-template <int NG, int TB>
+template <int NG, int TB, int NP>
 __device__ __forceinline__ void quad_h(const FusedArgs& a, const uint8_t* gq, const uint8_t* uq, const __half* gs,
                                        const __half* us, size_t qrow, int i0, int np, int n, int pbase, bool shared,
                                        const int* perm_s, const float4* xq, const float* xs136, int lane) {
@@ -197,65 +211,41 @@ __device__ __forceinline__ void quad_h(const FusedArgs& a, const uint8_t* gq, co
       const int ti = t0 + tt < n ? t0 + tt : t0;
       tok[tt] = shared ? ti : perm_s[pbase + ti] / a.K;
     }
-    float hv[4][TB];
-    if (TB == 1) {
-      // all eight rows share each x' load
-      const uint8_t* q[8];
-      const __half* sc[8];
+    // pairs per pass: all NP for one token, half as many for two (register budget)
+    constexpr int NPC = TB == 1 ? NP : (NP > 1 ? NP / 2 : 1);
+    constexpr int NV = 2 * NPC * TB;                 // values reduced together: gate rows, then up rows
+    constexpr int SH = NV == 8 ? 2 : NV == 4 ? 3 : 4;  // value i's total sits in lanes with (lane >> SH) == i
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int pp = p < np ? p : 0;
-        q[p] = gq + pp * qrow;
-        q[4 + p] = uq + pp * qrow;
-        sc[p] = gs + (size_t)pp * G;
-        sc[4 + p] = us + (size_t)pp * G;
-      }
-      float acc[8][TB];
-      rows_dot<NG, TB, 8>(q, sc, G, xq, xs136, tok, acc, lane);
+    for (int p0 = 0; p0 < NP; p0 += NPC) {
+      float acc[2 * NPC][TB];
+      const int npc = min(NPC, np - p0);
+      pairs_dot<NG, TB, NPC>(gq + p0 * qrow, uq + p0 * qrow, gs + (size_t)p0 * G, us + (size_t)p0 * G, qrow,
+                             npc > 0 ? npc : 1, G, xq, xs136, tok, acc, lane);
+      float vals[NV];
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
+      for (int r = 0; r < 2 * NPC; ++r)
 #pragma unroll
-        for (int tt = 0; tt < TB; ++tt) hv[p][tt] = silu(warp_sum(acc[p][tt])) * warp_sum(acc[4 + p][tt]);
-    } else {
-      const uint8_t* qg[4];
-      const uint8_t* qu[4];
-      const __half* sg[4];
-      const __half* su[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int pp = p < np ? p : 0;
-        qg[p] = gq + pp * qrow;
-        qu[p] = uq + pp * qrow;
-        sg[p] = gs + (size_t)pp * G;
-        su[p] = us + (size_t)pp * G;
-      }
-      float ag[4][TB], au[4][TB];
-      rows_dot<NG, TB, 4>(qg, sg, G, xq, xs136, tok, ag, lane);
-      rows_dot<NG, TB, 4>(qu, su, G, xq, xs136, tok, au, lane);
-#pragma unroll
-      for (int p = 0; p < 4; ++p)
-#pragma unroll
-        for (int tt = 0; tt < TB; ++tt) hv[p][tt] = silu(warp_sum(ag[p][tt])) * warp_sum(au[p][tt]);
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int tt = 0; tt < TB; ++tt) {
-        if (t0 + tt >= n) continue;
+        for (int tt = 0; tt < TB; ++tt) vals[r * TB + tt] = acc[r][tt];
+      const float g = warp_sum_multi<NV>(vals);
+      const float u = __shfl_down_sync(0xffffffffu, g, 16);  // the up row of the same pair and token
+      const int vi = lane >> SH;                              // < NV / 2 for lanes < 16
+      const int p = p0 + vi / TB, tt = vi % TB;
+      if (lane < 16 && (lane & ((1 << SH) - 1)) == 0 && p - p0 < npc && t0 + tt < n) {
         const int as = shared ? a.T * a.K + (t0 + tt) : perm_s[pbase + t0 + tt];
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          if (p < np) a.h[(size_t)as * a.f + i0 + p] = hv[p][tt];
+        a.h[(size_t)as * a.f + i0 + p] = silu(g) * u;
       }
     }
   }
 }
 
-// All nr down rows of one expert (codes at q, scales at sc, row stride f/2 bytes and f/32 scales, in
-// shared memory) for the tokens [t_beg, t_end) of one slot: P[asg][r] = sum_f W[r][f] h[asg][f].
-// Lane = one 32-column group of h (f <= 1024); two rows at a time.  h is read through L1: each
-// lane's 128 contiguous bytes are one line, fetched once.
-__device__ __forceinline__ void dn_slot(const FusedArgs& a, const uint8_t* q, const __half* sc, int nr, int t_beg,
-                                        int t_end, int pbase, bool shared, const int* perm_s, float* P, int lane) {
+// Down rows [r_beg, r_end) of one expert (codes at q, scales at sc, row stride f/2 bytes and f/32
+// scales, in shared memory) for the tokens [t_beg, t_end) of one slot:
+// P[asg][r] = sum_f W[r][f] h[asg][f].  Lane = one 32-column group of h (f <= 1024); rows in
+// batches of eight, each batch reduced over the warp in one multi-value reduction.  h is read
+// through L1: each lane's 128 contiguous bytes are one line, fetched once.
+__device__ __forceinline__ void dn_slot(const FusedArgs& a, const uint8_t* q, const __half* sc, int r_beg, int r_end,
+                                        int t_beg, int t_end, int pbase, bool shared, const int* perm_s, float* P,
+                                        int lane) {
   const int f = a.f, Gf = f / 32;
   const bool on = lane < Gf;
   for (int ti = t_beg; ti < t_end; ++ti) {
@@ -274,48 +264,35 @@ __device__ __forceinline__ void dn_slot(const FusedArgs& a, const uint8_t* q, co
       hv[m].w *= 256.f;
     }
     const float h136 = hsum * 136.0f;
-    for (int r = 0; r < nr; r += 2) {
-      const bool two = r + 1 < nr;
-      const uint4 w0 = on ? *reinterpret_cast<const uint4*>(q + (size_t)r * (f / 2) + lane * 16) : make_uint4(0, 0, 0, 0);
-      const uint4 w1 = on && two ? *reinterpret_cast<const uint4*>(q + (size_t)(r + 1) * (f / 2) + lane * 16)
-                                 : make_uint4(0, 0, 0, 0);
-      float p0 = 0.f, p1 = 0.f;
+    for (int r0 = r_beg; r0 < r_end; r0 += 8) {
+      float pr[8];
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        const float4 xa = hv[2 * wd], xb = hv[2 * wd + 1];
-        {
-          const uint32_t w32 = wd == 0 ? w0.x : wd == 1 ? w0.y : wd == 2 ? w0.z : w0.w;
-          const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-          p0 = fmaf(v_lo(lo, 0), xa.x, p0);
-          p0 = fmaf(v_lo(hi, 0), xa.y, p0);
-          p0 = fmaf(v_lo(lo, 1), xa.z, p0);
-          p0 = fmaf(v_lo(hi, 1), xa.w, p0);
-          p0 = fmaf(v_lo(lo, 2), xb.x, p0);
-          p0 = fmaf(v_lo(hi, 2), xb.y, p0);
-          p0 = fmaf(v_lo(lo, 3), xb.z, p0);
-          p0 = fmaf(v_lo(hi, 3), xb.w, p0);
+      for (int i = 0; i < 8; ++i) {
+        const int r = r0 + i;
+        float pv = 0.f;
+        if (on && r < r_end) {
+          const uint4 w = *reinterpret_cast<const uint4*>(q + (size_t)r * (f / 2) + lane * 16);
+#pragma unroll
+          for (int wd = 0; wd < 4; ++wd) {
+            const float4 xa = hv[2 * wd], xb = hv[2 * wd + 1];
+            const uint32_t w32 = wd == 0 ? w.x : wd == 1 ? w.y : wd == 2 ? w.z : w.w;
+            const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+            pv = fmaf(v_lo(lo, 0), xa.x, pv);
+            pv = fmaf(v_lo(hi, 0), xa.y, pv);
+            pv = fmaf(v_lo(lo, 1), xa.z, pv);
+            pv = fmaf(v_lo(hi, 1), xa.w, pv);
+            pv = fmaf(v_lo(lo, 2), xb.x, pv);
+            pv = fmaf(v_lo(hi, 2), xb.y, pv);
+            pv = fmaf(v_lo(lo, 3), xb.z, pv);
+            pv = fmaf(v_lo(hi, 3), xb.w, pv);
+          }
+          pv = __half2float(sc[(size_t)r * Gf + lane]) * (pv - h136);
         }
-        {
-          const uint32_t w32 = wd == 0 ? w1.x : wd == 1 ? w1.y : wd == 2 ? w1.z : w1.w;
-          const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-          p1 = fmaf(v_lo(lo, 0), xa.x, p1);
-          p1 = fmaf(v_lo(hi, 0), xa.y, p1);
-          p1 = fmaf(v_lo(lo, 1), xa.z, p1);
-          p1 = fmaf(v_lo(hi, 1), xa.w, p1);
-          p1 = fmaf(v_lo(lo, 2), xb.x, p1);
-          p1 = fmaf(v_lo(hi, 2), xb.y, p1);
-          p1 = fmaf(v_lo(lo, 3), xb.z, p1);
-          p1 = fmaf(v_lo(hi, 3), xb.w, p1);
-        }
+        pr[i] = pv;
       }
-      const float s0 = on ? __half2float(sc[(size_t)r * Gf + lane]) : 0.f;
-      const float s1 = on && two ? __half2float(sc[(size_t)(r + 1) * Gf + lane]) : 0.f;
-      const float o0 = warp_sum(s0 * (p0 - h136));
-      const float o1 = warp_sum(s1 * (p1 - h136));
-      if (lane == 0) {
-        P[(size_t)as * a.dn_rows_max + r] = o0;
-        if (two) P[(size_t)as * a.dn_rows_max + r + 1] = o1;
-      }
+      const float o = warp_sum_multi<8>(pr);
+      const int r = r0 + (lane >> 2);
+      if ((lane & 3) == 0 && r < r_end) P[(size_t)as * a.dn_rows_max + r] = o;
     }
   }
 }
@@ -374,17 +351,19 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   int* perm_s = reinterpret_cast<int*>(slot_s + E);
   int* idx_s = perm_s + T * K;
   float* w_s = reinterpret_cast<float*>(idx_s + T * K);
-  int* cnt = reinterpret_cast<int*>(w_s + T * K);
-  int* offv = cnt + E;                                        // [E + 1]
 
   __shared__ __align__(8) uint64_t full[kFzMaxStages], empty[kFzMaxStages], shg_full, shd_full, route_ready;
-  __shared__ uint64_t s_tkc[2 * kFzWarps];
+  __shared__ uint64_t s_tkc[kFzWarps * kMaxK];
   __shared__ float s_tkf[2 * kFzWarps];
-  __shared__ int s_wsum[kFzWarps], s_wact[kFzWarps];
+  __shared__ int s_srt[kFzMaxT * kMaxK];
   __shared__ volatile int s_abort;
   __shared__ int s_nact, s_issued, s_ok;
   __shared__ float inv_s[kFzMaxT];
 
+  // This launch may start while the previous layer's kernel is still finishing (programmatic
+  // dependent launch): everything before griddepcontrol.wait touches only this CTA's shared memory
+  // and read-only weights; the activations, the workspace and the barrier counter come after it.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(&full[s], 1);
@@ -420,16 +399,17 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
         tc::bulk_g2s(shd, a.sh_dn_q + (size_t)j0 * dq, (uint32_t)(nr * dq), &shd_full);
         tc::bulk_g2s(shd + nr * dq, a.sh_dn_s + (size_t)j0 * Gf, (uint32_t)(nr * ds), &shd_full);
       }
-      bool ok = tc::mbar_wait(&route_ready, 0, &s_abort);
+      bool ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, kFzProducerSleep);
       int k = 0;
       if (ok) {
         const int n_act = s_nact;
+
         const long long U = (long long)n_act * f;
         PairRange pr{(int)(U * c / nc), (int)(U * (c + 1) / nc)};
         int s, i0, n;
         while (ok && next_pairs(pr, f, s, i0, n)) {
           const int st = ring_stage(k, SG);
-          if (!tc::mbar_wait(&empty[st], ring_phase(k, SG) ^ 1u, &s_abort)) { ok = false; break; }
+          if (!tc::mbar_wait_sleepy(&empty[st], ring_phase(k, SG) ^ 1u, &s_abort, kFzProducerSleep)) { ok = false; break; }
           const int e = slot_s[s].x;
           uint8_t* dst = ring + (size_t)st * SB;
           const size_t rg = (size_t)e * 2 * f + i0, ru = rg + f;
@@ -440,10 +420,18 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
           tc::bulk_g2s(dst + 2 * kFzPairs * qrow + kFzPairs * srow, a.gu_s + ru * G, (uint32_t)(n * srow), &full[st]);
           s_issued = ++k;
         }
+        // the down rows are needed only after the second barrier: start their way into L2 now (after
+        // the gate/up requests), so their copies into the ring, which wait for the gate/up stages,
+        // are short
+        for (int jj = 0; ok && jj < n_act && nr > 0; ++jj) {
+          const int e = slot_s[jj].x;
+          tc::bulk_prefetch_l2(a.dn_q + ((size_t)e * d + j0) * dq, (uint32_t)(nr * dq));
+          tc::bulk_prefetch_l2(a.dn_s + ((size_t)e * d + j0) * Gf, (uint32_t)(nr * ds));
+        }
         // then this CTA's down rows of every routed expert, kFzDnSlots experts per chunk
         for (int p0 = 0; ok && nr > 0 && p0 < n_act; p0 += kFzDnSlots) {
           const int st = ring_stage(k, SG);
-          if (!tc::mbar_wait(&empty[st], ring_phase(k, SG) ^ 1u, &s_abort)) { ok = false; break; }
+          if (!tc::mbar_wait_sleepy(&empty[st], ring_phase(k, SG) ^ 1u, &s_abort, kFzProducerSleep)) { ok = false; break; }
           const int cntp = min(kFzDnSlots, n_act - p0);
           uint8_t* dst = ring + (size_t)st * SB;
           tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(cntp * nr * (dq + ds)));
@@ -481,6 +469,11 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       const int cc = cb + lane + 32 * i;
       wv[i] = cc < ce ? __ldg(wr + cc) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are visible
+    // the barrier counter's base: the previous launch's barriers are complete and fewer than
+    // gridDim.x arrivals of this launch's first barrier can precede this read
+    unsigned long long bar_base = 0;
+    if (ctid == 0) bar_base = ld_acquire_gpu(a.grid_bar) / gridDim.x * gridDim.x;
     if (a.prenorm) {
       for (int t = warp; t < T; t += kFzWarps) {
         float ss = 0.f;
@@ -565,20 +558,20 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       a.logits[(size_t)t * E + e0 + le] = v * (1.0f / 256.0f) + (a.bias ? a.bias[e0 + le] : 0.f);
     }
     consumers_sync();
-    unsigned long long target = 0;
-    if (ctid == 0) target = grid_arrive(a.grid_bar);
+    if (ctid == 0) grid_arrive(a.grid_bar);
 
     // ---- shared expert gate/up while the other CTAs finish their logits
     if (sh_gu_on) {
-      ok = tc::mbar_wait_warp(&shg_full, 0, &s_abort);
+      ok = tc::mbar_wait_warp(&shg_full, 0, &s_abort, kFzConsumerSleep);
       const int n = sh1 - sh0;
-      for (int p0 = 4 * warp; ok && p0 < n; p0 += 4 * kFzWarps)
-        quad_h<NG, TB>(a, shg + p0 * qrow, shg + SR * qrow + p0 * qrow,
-                       reinterpret_cast<const __half*>(shg + 2 * SR * qrow) + (size_t)p0 * G,
-                       reinterpret_cast<const __half*>(shg + 2 * SR * qrow + SR * srow) + (size_t)p0 * G, qrow,
-                       sh0 + p0, min(4, n - p0), T, 0, true, perm_s, xq, xs136, lane);
+      // one pair per warp: this runs while the barrier waits, so spread it out
+      for (int p0 = warp; ok && p0 < n; p0 += kFzWarps)
+        quad_h<NG, TB, 1>(a, shg + p0 * qrow, shg + SR * qrow + p0 * qrow,
+                          reinterpret_cast<const __half*>(shg + 2 * SR * qrow) + (size_t)p0 * G,
+                          reinterpret_cast<const __half*>(shg + 2 * SR * qrow + SR * srow) + (size_t)p0 * G, qrow,
+                          sh0 + p0, 1, T, 0, true, perm_s, xq, xs136, lane);
     }
-    if (ctid == 0) s_ok = grid_wait(a.grid_bar, target, &s_abort) ? 1 : 0;
+    if (ctid == 0) s_ok = grid_wait(a.grid_bar, bar_base + nc, &s_abort) ? 1 : 0;
     consumers_sync();
     ok = consumers_all(ok && s_ok && !s_abort);
     if (!ok && ctid == 0) s_abort = 1;  // the producer stops waiting for the routing
@@ -587,79 +580,66 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     int k = 0;
     if (ok) {
       topk_group(a.logits, T, E, K, kFzWarps, warp, s_tkf, s_tkc, idx_s, w_s, [] { consumers_sync(); });
-      for (int i = ctid; i < E; i += kFzWarps * 32) cnt[i] = 0;
       if (c == 0)
         for (int i = ctid; i < T * K; i += kFzWarps * 32) {
           a.idx[i] = idx_s[i];
           a.w[i] = w_s[i];
         }
-      consumers_sync();
-      for (int i = ctid; i < T * K; i += kFzWarps * 32) atomicAdd(&cnt[idx_s[i]], 1);
-      consumers_sync();
       {
-        // exclusive scans of the counts and of the "expert is used" flags: each consumer thread
-        // owns `per` consecutive experts, then warp scans, then a scan of the warp totals
-        const int per = (E + kFzWarps * 32 - 1) / (kFzWarps * 32), b = ctid * per;
-        int sum = 0, act = 0;
-        for (int i = b; i < min(b + per, E); ++i) {
-          sum += cnt[i];
-          act += cnt[i] > 0;
-        }
-        int isum = sum, iact = act;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y1 = __shfl_up_sync(0xffffffffu, isum, o), y2 = __shfl_up_sync(0xffffffffu, iact, o);
-          if (lane >= o) {
-            isum += y1;
-            iact += y2;
+        // dispatch by counting, one thread per assignment i (n <= 256): its place in the stable
+        // counting sort is the number of smaller (expert, i) keys; the distinct experts below its
+        // own give its slot
+        const int n = T * K;
+        int e_i = 0, start = 0, cnt_i = 0, first = 0;
+        if (ctid < n) {
+          e_i = idx_s[ctid];
+          int pos = 0, before = 0;
+          for (int j = 0; j < n; ++j) {
+            const int ej = idx_s[j];
+            start += ej < e_i;
+            cnt_i += ej == e_i;
+            pos += ej < e_i || (ej == e_i && j < ctid);
+            before += ej == e_i && j < ctid;
           }
-        }
-        if (lane == 31) {
-          s_wsum[warp] = isum;
-          s_wact[warp] = iact;
+          perm_s[pos] = ctid;
+          first = before == 0;
+          s_srt[ctid] = first;
         }
         consumers_sync();
-        int wsum = 0, wact = 0;  // totals of the warps before this one
-        for (int q = 0; q < warp; ++q) {
-          wsum += s_wsum[q];
-          wact += s_wact[q];
+        if (ctid < n && first) {
+          int slot = 0;
+          for (int j = 0; j < n; ++j) slot += s_srt[j] && idx_s[j] < e_i;
+          slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
         }
-        int run = wsum + isum - sum, ar = wact + iact - act;
-        for (int i = b; i < min(b + per, E); ++i) {
-          offv[i] = run;
-          if (cnt[i] > 0) {
-            slot_s[ar] = make_int4(i, run, cnt[i], 0);
-            if (c == 0) {
-              a.active[ar] = i;
-              a.slots[ar] = make_int4(i, run, cnt[i], 0);
+        if (ctid == 0) {
+          int na = 0;
+          for (int j = 0; j < n; ++j) na += s_srt[j];
+          s_nact = na;
+        }
+        consumers_sync();
+        if (c == 0) {
+          // the full outputs: offs[e] = assignments with an expert below e
+          const int na = s_nact;
+          for (int e = ctid; e <= E; e += kFzWarps * 32) {
+            int o = 0, ce = 0;
+            for (int q = 0; q < n; ++q) {
+              o += idx_s[q] < e;
+              ce += idx_s[q] == e;
             }
-            ++ar;
+            a.offs[e] = o;
+            if (e < E) a.counts[e] = ce;
           }
-          if (c == 0) {
-            a.counts[i] = cnt[i];
-            a.offs[i] = run;
+          for (int q = ctid; q < na; q += kFzWarps * 32) {
+            a.active[q] = slot_s[q].x;
+            a.slots[q] = slot_s[q];
           }
-          run += cnt[i];
-        }
-        if (ctid == kFzWarps * 32 - 1) {
-          offv[E] = run;
-          s_nact = ar;
-          if (c == 0) {
-            a.offs[E] = run;
-            *a.n_active = ar;
-            if (a.stat) *a.stat = ar;
+          for (int q = ctid; q < n; q += kFzWarps * 32) a.perm[q] = perm_s[q];
+          if (ctid == 0) {
+            *a.n_active = na;
+            if (a.stat) *a.stat = na;
           }
         }
       }
-      consumers_sync();
-      for (int i = ctid; i < T * K; i += kFzWarps * 32) {
-        const int ei = idx_s[i];
-        int r = 0;
-        for (int jj = 0; jj < i; ++jj) r += (idx_s[jj] == ei);
-        perm_s[offv[ei] + r] = i;
-        if (c == 0) a.perm[offv[ei] + r] = i;
-      }
-      consumers_sync();
       if (ctid == 0) tc::mbar_arrive(&route_ready);  // the producer may now stream routed experts
     }
     const int n_act = ok ? s_nact : 0;
@@ -672,13 +652,13 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       while (next_pairs(pr, f, s, i0, n)) {
         if (k % kFzGroups == grp) {
           const int st = ring_stage(k, SG);
-          ok = tc::mbar_wait_warp(&full[st], ring_phase(k, SG), &s_abort);
+          ok = tc::mbar_wait_warp(&full[st], ring_phase(k, SG), &s_abort, kFzConsumerSleep);
           if (!ok) break;
           const int p0 = 4 * wg;
           if (p0 < n) {
             const uint8_t* base = ring + (size_t)st * SB;
             const int4 sl = slot_s[s];
-            quad_h<NG, TB>(a, base + p0 * qrow, base + kFzPairs * qrow + p0 * qrow,
+            quad_h<NG, TB, 4>(a, base + p0 * qrow, base + kFzPairs * qrow + p0 * qrow,
                            reinterpret_cast<const __half*>(base + 2 * kFzPairs * qrow) + (size_t)p0 * G,
                            reinterpret_cast<const __half*>(base + 2 * kFzPairs * qrow + kFzPairs * srow) + (size_t)p0 * G,
                            qrow, i0 + p0, min(4, n - p0), sl.z, sl.y, false, perm_s, xq, xs136, lane);
@@ -692,33 +672,35 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     if (!ok && lane == 0) s_abort = 1;
     consumers_sync();
     if (ctid == 0) {
-      const unsigned long long t2 = grid_arrive(a.grid_bar);  // always arrive: the other CTAs must not wait
-      s_ok = (!s_abort && grid_wait(a.grid_bar, t2, &s_abort)) ? 1 : 0;
+      grid_arrive(a.grid_bar);  // always arrive: the other CTAs must not wait on this one
+      s_ok = (!s_abort && grid_wait(a.grid_bar, bar_base + 2ull * nc, &s_abort)) ? 1 : 0;
     }
     consumers_sync();
     ok = consumers_all(ok && s_ok && !s_abort);
     if (!ok && ctid == 0) s_abort = 1;
 
     // ---- phase 4: this CTA's down rows of every expert, then the combine
-    if (ok && sh_dn_on && grp == kFzGroups - 1) {
-      // the shared expert: one warp per token of the last group
-      ok = tc::mbar_wait_warp(&shd_full, 0, &s_abort);
-      for (int t = wg; ok && t < T; t += kFzGroupWarps)
-        dn_slot(a, shd, reinterpret_cast<const __half*>(shd + nr * dq), nr, t, t + 1, 0, true, perm_s, P, lane);
-    }
-    for (int p0 = 0; ok && nr > 0 && p0 < n_act; p0 += kFzDnSlots, ++k) {
-      if (k % kFzGroups != grp) continue;
-      const int st = ring_stage(k, SG);
-      ok = tc::mbar_wait_warp(&full[st], ring_phase(k, SG), &s_abort);
-      if (!ok) break;
-      const int cntp = min(kFzDnSlots, n_act - p0);
-      if (wg < cntp) {
-        const int4 sl = slot_s[p0 + wg];
-        const uint8_t* q = ring + (size_t)st * SB + (size_t)wg * DR * (dq + ds);
-        dn_slot(a, q, reinterpret_cast<const __half*>(q + DR * dq), nr, 0, sl.z, sl.y, false, perm_s, P, lane);
+    {
+      if (ok && sh_dn_on && grp == kFzGroups - 1) {
+        // the shared expert: one warp per token of the last group
+        ok = tc::mbar_wait_warp(&shd_full, 0, &s_abort, kFzConsumerSleep);
+        for (int t = wg; ok && t < T; t += kFzGroupWarps)
+          dn_slot(a, shd, reinterpret_cast<const __half*>(shd + nr * dq), 0, nr, t, t + 1, 0, true, perm_s, P, lane);
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&empty[st]);
+      for (int p0 = 0; ok && nr > 0 && p0 < n_act; p0 += kFzDnSlots, ++k) {
+        if (k % kFzGroups != grp) continue;
+        const int st = ring_stage(k, SG);
+        ok = tc::mbar_wait_warp(&full[st], ring_phase(k, SG), &s_abort, kFzConsumerSleep);
+        if (!ok) break;
+        const int cntp = min(kFzDnSlots, n_act - p0);
+        if (wg < cntp) {
+          const int4 sl = slot_s[p0 + wg];
+          const uint8_t* q = ring + (size_t)st * SB + (size_t)wg * DR * (dq + ds);
+          dn_slot(a, q, reinterpret_cast<const __half*>(q + DR * dq), 0, nr, 0, sl.z, sl.y, false, perm_s, P, lane);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[st]);
+      }
     }
     if (!ok && lane == 0) s_abort = 1;
     ok = consumers_all(ok && !s_abort);
@@ -766,7 +748,7 @@ static FusedPlan fused_plan(int T, int d, int f, int E, int K, int nsm) {
   size_t fixed = (size_t)p.shg_rows * 2 * (d / 2 + G * 2) + (size_t)p.dn_rows_max * (f / 2 + Gf * 2);
   fixed += (size_t)T * d * 4 + (size_t)T * G * 4 + kFzWarps * kFzMaxT * 4;
   fixed += ((size_t)(T * K + T) * p.dn_rows_max * 4 + 15) & ~size_t(15);
-  fixed += (size_t)E * 16 + (size_t)T * K * 12 + (size_t)E * 4 + (size_t)(E + 1) * 4 + 64;
+  fixed += (size_t)E * 16 + (size_t)T * K * 12 + 64;
   const long long room = (long long)kFzSmemMax - (long long)fixed - kFzStaticSlack;
   p.ns = room > 0 ? (int)std::min<long long>(kFzMaxStages, room / p.stage_bytes) : 0;
   p.ns -= p.ns % kFzGroups;  // whole stages per consumer group
@@ -775,7 +757,6 @@ static FusedPlan fused_plan(int T, int d, int f, int E, int K, int nsm) {
 }
 
 static int g_fz_sms = 0;
-static bool g_fz_coop = false;
 
 template <int NG, int TB>
 static const void* fused_fn() {
@@ -784,10 +765,6 @@ static const void* fused_fn() {
 
 cudaError_t fused_kernels_init(int num_sms) {
   g_fz_sms = num_sms;
-  int coop = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  g_fz_coop = coop != 0;
   const void* fns[6] = {fused_fn<1, 1>(), fused_fn<2, 1>(), fused_fn<4, 1>(),
                         fused_fn<1, 2>(), fused_fn<2, 2>(), fused_fn<4, 2>()};
   for (const void* fn : fns) {
@@ -862,11 +839,15 @@ cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, unsigne
   cfg.blockDim = dim3(kFzThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
+  // One CTA per SM (shared memory and registers allow no second), grid = #SMs, and nothing else
+  // in the stream runs beside it, so all CTAs are resident; the grid barriers are bounded anyway.
+  // The launch may overlap the tail of the previous kernel in the stream (its prologue only reads
+  // weights); griddepcontrol.wait orders everything else.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = g_fz_coop ? 1 : 0;
+  cfg.numAttrs = 1;
   void* args[1] = {&a};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
