@@ -315,45 +315,89 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const void* x, void* xnorm
 }
 
 // logits[T][E] = X[T][d] * Wr[E][d]^T (+ bias), fp32 FMA in ascending k per output.
-// Tile 64 tokens x 64 experts x 16 k, 256 threads, 4x4 outputs per thread.
+// Register-blocked SIMT GEMM: CTA tile 128 tokens x 128 experts, k-step 8, 256 threads, 8 x 8
+// outputs per thread held in registers (rows ty*4 + {0..3, 64..67}, columns tx*4 + {0..3, 64..67},
+// so every shared-memory read is a conflict-free 16-byte load).  Both operands are staged k-major
+// in shared memory, double-buffered; the next k-step's global loads are in flight while the current
+// one is multiplied.  Activations are widened from bf16 as they are staged.
+constexpr int kRlBM = 128, kRlBN = 128, kRlBK = 8;
 __global__ void __launch_bounds__(256) router_logits_kernel(const void* x, int act, const float* Wr, const float* bias,
                                                             float* logits, int T, int d, int E) {
-  __shared__ float As[16][64 + 4];
-  __shared__ float Bs[16][64 + 4];
-  const int tid = threadIdx.x;
-  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
-  const int tx = tid & 15, ty = tid >> 4;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < d; k0 += 16) {
-    for (int i = tid; i < 64 * 16; i += 256) {
-      const int r = i >> 4, kk = i & 15;
-      const int t = t0 + r, e = e0 + r;
-      As[kk][r] = (t < T) ? load_act(x, act, (size_t)t * d + k0 + kk) : 0.f;
-      Bs[kk][r] = (e < E) ? Wr[(size_t)e * d + k0 + kk] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        av[i] = As[kk][ty * 4 + i];
-        bv[i] = Bs[kk][tx * 4 + i];
+  __shared__ __align__(16) float As[2][kRlBK][kRlBM];
+  __shared__ __align__(16) float Bs[2][kRlBK][kRlBN];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.y * kRlBM, e0 = blockIdx.x * kRlBN;
+  // staging: thread tid loads row (tid >> 1) and 4 consecutive k (tid & 1) * 4 of each operand
+  const int lr = tid >> 1, lk = (tid & 1) * 4;
+  const int ta = t0 + lr, eb = e0 + lr;
+  const bool a_on = ta < T, b_on = eb < E;
+  float ra[4], rb[4];
+  auto load = [&](int k0) {
+    if (a_on) {
+      if (act == kActBf16) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(x) + (size_t)ta * d + k0 + lk));
+        ra[0] = __uint_as_float(u.x << 16);
+        ra[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        ra[2] = __uint_as_float(u.y << 16);
+        ra[3] = __uint_as_float(u.y & 0xFFFF0000u);
+      } else {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)ta * d + k0 + lk));
+        ra[0] = v.x; ra[1] = v.y; ra[2] = v.z; ra[3] = v.w;
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    } else {
+      ra[0] = ra[1] = ra[2] = ra[3] = 0.f;
     }
-    __syncthreads();
+    if (b_on) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(Wr + (size_t)eb * d + k0 + lk));
+      rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
+    } else {
+      rb[0] = rb[1] = rb[2] = rb[3] = 0.f;
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      As[buf][lk + i][lr] = ra[i];
+      Bs[buf][lk + i][lr] = rb[i];
+    }
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  load(0);
+  store(0);
+  __syncthreads();
+  const int nk = d / kRlBK;
+  for (int kt = 0; kt < nk; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nk) load((kt + 1) * kRlBK);
+#pragma unroll
+    for (int k = 0; k < kRlBK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4 + 64]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4 + 64]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (kt + 1 < nk) {
+      store(buf ^ 1);
+      __syncthreads();
+    }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 4 + (i & 3) + (i >> 2) * 64;
     if (t >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + tx * 4 + (j & 3) + (j >> 2) * 64;
       if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
     }
   }
@@ -462,7 +506,7 @@ cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t 
     rmsnorm_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a.x, a.xnorm, a.act, a.T, a.d, a.eps);
     xin = a.xnorm;
   }
-  dim3 g((a.E + 63) / 64, (a.T + 63) / 64);
+  dim3 g((a.E + kRlBN - 1) / kRlBN, (a.T + kRlBM - 1) / kRlBM);
   router_logits_kernel<<<g, 256, 0, st>>>(xin, a.act, a.Wr, a.bias, a.logits, a.T, a.d, a.E);
   topk_kernel<<<(a.T + kRouterWarps - 1) / kRouterWarps, 256, (size_t)kRouterWarps * a.E * sizeof(float), st>>>(a);
   dispatch_hist_kernel<<<nblocks_dispatch, kDispatchBlock, 0, st>>>(a);
