@@ -148,6 +148,14 @@ moe_status moe_get_device_status(moe_handle h, void* stream);
 /* Free the workspace and any captured graphs.  Synchronises the device first. */
 moe_status moe_destroy(moe_handle h);
 
+/* Self-test of the device-side bounded waits that every layer kernel uses (no model data, no
+ * handle).  One small kernel waits on an mbarrier nobody arrives at and polls a counter nobody
+ * bumps, each with a budget of `budget_cycles` SM clocks (1000 .. 2e9).  Returns MOE_ERR_TIMEOUT
+ * when both waits gave up and recorded "timeout" (the expected outcome), MOE_ERR_DEVICE if a wait
+ * reported success, MOE_ERR_CUDA on a CUDA error.  Synchronises `stream`; the GPU context stays
+ * usable afterwards. */
+moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream);
+
 /* Options (each returns the value in effect, or a negative moe_status on error; changing one
  * drops the handle's captured stack graphs).
  * MOE_OPT_FUSED_MAX_TOKENS: calls with T <= value run the whole layer (router, selection,

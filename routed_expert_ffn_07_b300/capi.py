@@ -62,6 +62,7 @@ def _load():
         "moe_destroy": ([vp], ci),
         "moe_route_noalloc": ([vp, vp, vp, ci, ci, ci, ci, ci, i32p, vp, i32p, i32p, vp], ci),
         "moe_set_option": ([vp, ci, ci], ci),
+        "moe_selftest_bounded_waits": ([ctypes.c_longlong, vp], ci),
         "moe_timing_enable": ([vp, ci], ci),
         "moe_timing_rewind": ([vp], ci),
         "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
@@ -163,6 +164,11 @@ def moe_get_device_status(h, stream=None):
 
 def moe_destroy(h):
     _check("moe_destroy", lib.moe_destroy(h))
+
+
+def moe_selftest_bounded_waits(budget_cycles=2_000_000, stream=None):
+    """Run the device self-test of the bounded waits; returns the raw moe_status (5 = timeout, expected)."""
+    return lib.moe_selftest_bounded_waits(budget_cycles, _stream(stream))
 
 
 def moe_set_option(h, option, value):

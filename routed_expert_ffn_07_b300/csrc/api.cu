@@ -21,6 +21,8 @@ size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K);
 size_t gemv_smem_dn(int T, int K, int E);
 cudaError_t gemm_kernels_init(int num_sms);
 cudaError_t fused_kernels_init(int num_sms);
+cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
+                                         cudaStream_t st);
 bool fused_shape_ok(int T, int d, int f, int E, int K);
 cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, unsigned long long* grid_bar,
                                 cudaStream_t st);
@@ -530,6 +532,35 @@ moe_status moe_get_device_status(moe_handle h, void* stream) {
   }
   if (v) return MOE_ERR_DEVICE;
   return MOE_OK;
+}
+
+moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream) {
+  if (budget_cycles < 1000 || budget_cycles > 2000000000ll) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned long long* counter = nullptr;
+  unsigned* res = nullptr;
+  CUDA_TRY(cudaMalloc(&counter, 8));
+  cudaError_t e = cudaMalloc(&res, 8);
+  if (e != cudaSuccess) {
+    cudaFree(counter);
+    g_last_cuda_error = (int)e;
+    return MOE_ERR_CUDA;
+  }
+  unsigned hres[2] = {0, 0};
+  e = cudaMemsetAsync(counter, 0, 8, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(res, 0, 8, st);
+  if (e == cudaSuccess) e = launch_bounded_wait_selftest(counter, budget_cycles, res, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(hres, res, 8, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(counter);
+  cudaFree(res);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = (int)e;
+    return MOE_ERR_CUDA;
+  }
+  if (hres[0] & 4u) return MOE_ERR_DEVICE;            // a wait that cannot succeed returned success
+  if ((hres[0] & 3u) == 3u && (hres[1] & kStatusTimeout)) return MOE_ERR_TIMEOUT;
+  return MOE_ERR_DEVICE;
 }
 
 int moe_set_option(moe_handle h, int option, int value) {

@@ -731,6 +731,41 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   }
 }
 
+// ------------------------------------------------------------------ self-test of the bounded waits
+// One CTA: thread 0 waits on an mbarrier nobody arrives at and on a barrier counter nobody bumps,
+// each with a small budget, exactly as the layer kernels wait.  Bit 0 of *result: the mbarrier
+// wait gave up; bit 1: the counter wait gave up; bit 2: a wait returned success (a bug).
+__global__ void bounded_wait_selftest_kernel(unsigned long long* counter, long long budget, unsigned* result) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int never;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    never = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned r = 0;
+    if (!tc::mbar_wait(&bar, 0, &never, budget)) r |= 1u; else r |= 4u;
+    // the counter never reaches this target; the poll limit bounds the wait
+    const unsigned long long target = ld_acquire_gpu(counter) + (1ull << 40);
+    bool ok = true;
+    for (unsigned n = 0; ok && ld_acquire_gpu(counter) < target; ++n) {
+      if (n > (unsigned)(budget >> 6)) ok = false;
+      __nanosleep(32);
+    }
+    r |= ok ? 4u : 2u;
+    *result = r;
+    if (r & 3u) atomicOr(result + 1, kStatusTimeout);
+  }
+}
+
+cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
+                                         cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(counter, budget, result);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ host side
 struct FusedPlan {
   int ns, stage_bytes, shg_rows, dn_rows_max;

@@ -94,3 +94,8 @@ def test_noalloc_route_validates_before_touching_the_device(lib):
     assert L.moe_route_noalloc(p + 2, None, p, 1, 4, 256, 8, 2, None, None, None, None, None) == 1
     assert L.moe_route_noalloc(p, None, p, 1, 4, 250, 8, 2, None, None, None, None, None) == 1
     assert L.moe_route_noalloc(p, None, p, 7, 4, 256, 8, 2, None, None, None, None, None) == 1
+
+
+def test_selftest_rejects_bad_budget_before_the_device(lib):
+    assert lib.lib.moe_selftest_bounded_waits(10, None) == 1
+    assert lib.lib.moe_selftest_bounded_waits(10 ** 12, None) == 1

@@ -323,8 +323,12 @@ def test_one_launch_layer_matches_gemv_path_closely(decode_layer):
         capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)
         capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 4)
     a, b = out["one_launch"], out["gemv"]
-    # both round once to bf16 from fp32 sums taken in different orders: at most 2 bf16 ulps apart
-    assert torch.all((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-6)
+    # Both sum the same fp32 products in different orders, then round once to bf16: they may differ
+    # by the bf16 rounding of each (2 ulps, 2^-7 relative) plus fp32 reassociation error, which
+    # scales with the size of the summed terms (the layer's output scale), not with a result that
+    # happens to cancel to near zero: 2^-16 of max|y| covers it with room to spare.
+    tol = 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 2.0 ** -16 * b.abs().max()
+    assert torch.all((a - b).abs() <= tol)
 
 
 def test_verify_stack_on_gemv_path():
@@ -341,3 +345,13 @@ def test_skewed_stack_on_gemv_path():
     wl_small = dataclasses.replace(wl, layers=8)
     counts, flagged, worst = _stack_parity(wl_small, sample_layers=[0, 3, 7], gemv_max=16)
     assert all(10 <= c <= 160 for c in counts)
+
+
+def test_bounded_waits_give_up_and_the_context_survives(decode_layer):
+    """A wait that nothing can satisfy (an mbarrier nobody arrives at, a barrier counter nobody
+    bumps) gives up within its budget and reports a timeout; the library keeps working after it."""
+    from routed_expert_ffn_07_b300 import capi
+    assert capi.moe_selftest_bounded_waits(2_000_000) == 5  # MOE_ERR_TIMEOUT
+    wl, wts, h = decode_layer
+    x = inputs.gen_activations(wl.seed, 1, wl.d, "bf16", layer=3)
+    run_layer(h, wl, wts, x, 1, layer=0, gen_layer=0)
