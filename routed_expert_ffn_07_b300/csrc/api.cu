@@ -24,7 +24,9 @@ cudaError_t fused_kernels_init(int num_sms);
 cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
                                          cudaStream_t st);
 bool fused_shape_ok(int T, int d, int f, int E, int K);
-cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, unsigned long long* grid_bar,
+cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const FusedExtra& fx, cudaStream_t st);
+size_t fused_down_copy_bytes(int n_exp, int d, int f);
+cudaError_t repack_down_blocked(const void* dn_q, const void* dn_s, int n_exp, int d, int f, void* out_q, void* out_s,
                                 cudaStream_t st);
 size_t gemm_workspace_bytes(int max_tokens, int d, int f, int E, int K);
 bool gemm_shape_ok(int d, int f);
@@ -49,6 +51,7 @@ struct LayerW {
   moe_layer_weights w;
   bool set = false;
   void* maps = nullptr;  // TMA descriptors of the layer's planes (tensor-core path only)
+  void* dnb = nullptr;   // K-blocked copy of the down planes (one-launch decode path only)
 };
 
 struct moe_ctx {
@@ -86,6 +89,8 @@ struct moe_ctx {
   int gemv_max_tokens = 4;       // T <= this runs the GEMV experts (when the grouped GEMM is available)
   int fused_max_tokens = 0;      // T <= this runs the one-launch decode layer (0: off)
   unsigned long long* grid_bar = nullptr;  // grid-barrier counter of the one-launch decode layer
+  bool fused_capable = false;    // the one-launch decode layer serves this config (T = 1 at least)
+  float* part = nullptr;         // its per-CTA partial outputs [#SM][min(max_tokens, 8)][d]
   // stage timing
   std::vector<cudaEvent_t> tev;
   int t_next = 0;
@@ -179,11 +184,12 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
     return MOE_ERR_CUDA;
   }
   h->fused_max_tokens = fused_limit(c, kFusedDefaultTokens);
+  h->fused_capable = fused_limit(c, 1) == 1;
 
   const int T = c.max_tokens, E = c.n_experts, K = c.top_k, d = c.d, f = c.f;
   const size_t as = act_size(c.act);
   h->nblocks_max = (T * K + kDispatchBlockHost - 1) / kDispatchBlockHost;
-  size_t sz[20];
+  size_t sz[24];
   int n = 0;
   sz[n++] = up256((size_t)T * E * 4);                 // logits
   sz[n++] = up256((size_t)T * K * 4);                 // idx
@@ -206,6 +212,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   sz[n++] = up256((size_t)T * d * as);                // stack x
   sz[n++] = up256((size_t)T * d * as);                // host x
   sz[n++] = up256((size_t)T * d * as);                // host y
+  const int TF = T < kFusedMaxTokensHost ? T : kFusedMaxTokensHost;
+  sz[n++] = h->fused_capable ? up256((size_t)h->num_sms * TF * d * 4) : 0;  // one-launch partials
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += sz[i];
   if (cudaMalloc(&h->slab, total) != cudaSuccess) {
@@ -236,6 +244,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   h->stack_x = p; p += sz[i++];
   h->host_x = p; p += sz[i++];
   h->host_y = p; p += sz[i++];
+  h->part = sz[i] ? reinterpret_cast<float*>(p) : nullptr; p += sz[i++];
   if (cudaMemset(h->slab, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->slab);
     delete h;
@@ -275,6 +284,32 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
                         w->dn_s, w->sh_gu_q, w->sh_gu_s, w->sh_dn_q, w->sh_dn_s) != cudaSuccess) {
       L.set = false;
       return MOE_ERR_INVALID_ARG;
+    }
+  }
+  if (h->fused_capable) {
+    // the one-launch decode layer reads the down planes K-blocked: copy them once, here
+    const moe_config& c = h->cfg;
+    const size_t rb = fused_down_copy_bytes(c.n_experts, c.d, c.f);
+    const size_t sb = c.has_shared ? fused_down_copy_bytes(1, c.d, c.f) : 0;
+    if (!L.dnb && cudaMalloc(&L.dnb, rb + sb) != cudaSuccess) {
+      cudaGetLastError();
+      L.dnb = nullptr;
+      L.set = false;
+      return MOE_ERR_OOM;
+    }
+    char* base = static_cast<char*>(L.dnb);
+    const size_t rq = ((size_t)c.n_experts * c.d * (c.f / 2) + 255) & ~size_t(255);
+    const size_t sq = ((size_t)c.d * (c.f / 2) + 255) & ~size_t(255);
+    // the weights may have been written on any stream: wait for the device before reading them
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = repack_down_blocked(w->dn_q, w->dn_s, c.n_experts, c.d, c.f, base, base + rq, nullptr);
+    if (e == cudaSuccess && c.has_shared)
+      e = repack_down_blocked(w->sh_dn_q, w->sh_dn_s, 1, c.d, c.f, base + rb, base + rb + sq, nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+    if (e != cudaSuccess) {
+      g_last_cuda_error = (int)e;
+      L.set = false;
+      return MOE_ERR_CUDA;
     }
   }
   L.w = *w;
@@ -362,10 +397,22 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
   cudaError_t e;
   if (ev && (e = record_timing_event(ev[0], st)) != cudaSuccess) return e;
   RouteArgs ra = make_route_args(h, layer, x, T, prenorm, h->stats + layer);
-  if (T <= h->fused_max_tokens) {
+  if (T <= h->fused_max_tokens && h->layers[layer].dnb) {
     // one launch for the whole layer; its stages are not separated (all of it counts as "route")
     ExpertArgs ea = make_expert_args(h, layer, x, T, y, resid);
-    e = launch_decode_fused(ra, ea, h->grid_bar, st);
+    const moe_config& c = h->cfg;
+    char* base = static_cast<char*>(h->layers[layer].dnb);
+    const size_t rb = fused_down_copy_bytes(c.n_experts, c.d, c.f);
+    const size_t rq = ((size_t)c.n_experts * c.d * (c.f / 2) + 255) & ~size_t(255);
+    const size_t sq = ((size_t)c.d * (c.f / 2) + 255) & ~size_t(255);
+    FusedExtra fx;
+    fx.dnb_q = base;
+    fx.dnb_s = base + rq;
+    fx.sh_dnb_q = c.has_shared ? base + rb : nullptr;
+    fx.sh_dnb_s = c.has_shared ? base + rb + sq : nullptr;
+    fx.part = h->part;
+    fx.grid_bar = h->grid_bar;
+    e = launch_decode_fused(ra, ea, fx, st);
     if (e != cudaSuccess) return e;
     for (int k = 1; ev && k < kTimingEvents; ++k)
       if ((e = record_timing_event(ev[k], st)) != cudaSuccess) return e;
@@ -618,8 +665,10 @@ moe_status moe_destroy(moe_handle h) {
   if (!h) return MOE_ERR_INVALID_ARG;
   cudaError_t e = cudaDeviceSynchronize();
   for (cudaEvent_t ev : h->tev) cudaEventDestroy(ev);
-  for (LayerW& L : h->layers)
+  for (LayerW& L : h->layers) {
     if (L.maps) gemm_maps_free(L.maps);
+    if (L.dnb) cudaFree(L.dnb);
+  }
   if (h->act_maps) gemm_maps_free(h->act_maps);
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);

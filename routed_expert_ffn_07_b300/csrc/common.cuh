@@ -175,4 +175,14 @@ struct ExpertArgs {
   unsigned* status;
 };
 
+// Extra arguments of the one-launch decode layer.
+struct FusedExtra {
+  const void* dnb_q;     // [E][f/8][d] uint32: K-blocked routed down codes (8 columns of one row per word)
+  const void* dnb_s;     // [E][f/32][d] fp16: their scales
+  const void* sh_dnb_q;  // the shared expert's, same layout (E = 1), or null
+  const void* sh_dnb_s;
+  float* part;           // [#SM][T][d] per-CTA partial outputs
+  unsigned long long* grid_bar;
+};
+
 }  // namespace moe

@@ -85,6 +85,86 @@ __device__ __forceinline__ void topk_token(const float* lg, int E, int K, int& m
   my_w = lane < K ? my_p / psum : 0.f;
 }
 
+// Order-preserving u32 key of a logit (larger logit, larger key; never 0) and its inverse.
+__device__ __forceinline__ uint32_t topk_order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float topk_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// The same selection and weights as topk_token, in compact code for kernels where it runs once per
+// launch, from keys already in shared memory: s_key[32 j + lane] = topk_order_key(logit of expert
+// lane + 32 j), 0 past E (E <= 1024); taken keys are overwritten.  Each lane keeps its best and
+// second-best untaken key (order: larger key, then lower expert); a round takes the warp's best
+// with two redux reductions, and only a lane that wins a second time rescans its experts.
+__device__ __forceinline__ void topk_warp(uint32_t* s_key, int E, int K, int& my_i, float& my_w) {
+  const int lane = threadIdx.x & 31;
+  const int nj = (E + 31) >> 5;
+  uint32_t b1 = 0u, b2 = 0u;
+  int j1 = 0, j2 = 0;
+#pragma unroll 4
+  for (int j = 0; j < nj; ++j) {
+    const uint32_t key = s_key[j * 32 + lane];
+    if (key > b1) {
+      b2 = b1;
+      j2 = j1;
+      b1 = key;
+      j1 = j;
+    } else if (key > b2) {
+      b2 = key;
+      j2 = j;
+    }
+  }
+  const float m = topk_key_value(__reduce_max_sync(0xffffffffu, b1));
+  float z = 0.f;
+#pragma unroll 4
+  for (int j = 0; j < nj; ++j) {
+    const uint32_t key = s_key[j * 32 + lane];
+    if (key != 0u) z += expf(topk_key_value(key) - m);
+  }
+  z = warp_sum(z);
+  bool have2 = true;
+  uint32_t my_key = 0u;
+  my_i = 0;
+#pragma unroll 1
+  for (int k = 0; k < K; ++k) {
+    const uint32_t best = __reduce_max_sync(0xffffffffu, b1);
+    const uint32_t cand = (b1 == best && b1 != 0u) ? (uint32_t)(lane + 32 * j1) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == k) {
+      my_i = (int)win;
+      my_key = best;
+    }
+    if (lane == (int)(win & 31u)) {
+      s_key[j1 * 32 + lane] = 0u;  // taken
+      if (have2) {
+        b1 = b2;
+        j1 = j2;
+        have2 = false;
+      } else {
+        b1 = 0u;
+        j1 = 0;
+#pragma unroll 4
+        for (int j = 0; j < nj; ++j) {
+          const uint32_t key = s_key[j * 32 + lane];
+          if (key > b1) {
+            b1 = key;
+            j1 = j;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+  const float my_p = lane < K ? expf(topk_key_value(my_key) - m) / z : 0.f;
+  float psum = 0.f;
+#pragma unroll 1
+  for (int k = 0; k < K; ++k) psum += __shfl_sync(0xffffffffu, my_p, k);
+  my_w = lane < K ? my_p / psum : 0.f;
+}
+
 }  // namespace moe
 
 namespace moe {
