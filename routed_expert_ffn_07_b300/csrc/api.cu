@@ -25,9 +25,9 @@ cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long 
                                          cudaStream_t st);
 bool fused_shape_ok(int T, int d, int f, int E, int K);
 cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const FusedExtra& fx, cudaStream_t st);
-size_t fused_down_copy_bytes(int n_exp, int d, int f);
-cudaError_t repack_down_blocked(const void* dn_q, const void* dn_s, int n_exp, int d, int f, void* out_q, void* out_s,
-                                cudaStream_t st);
+size_t fused_layout_bytes(int n_exp, int d, int f);
+cudaError_t fused_repack(const void* gu_q, const void* gu_s, const void* dn_q, const void* dn_s, int n_exp, int d,
+                         int f, void* out, cudaStream_t st);
 size_t gemm_workspace_bytes(int max_tokens, int d, int f, int E, int K);
 bool gemm_shape_ok(int d, int f);
 void* gemm_maps_new();
@@ -51,7 +51,7 @@ struct LayerW {
   moe_layer_weights w;
   bool set = false;
   void* maps = nullptr;  // TMA descriptors of the layer's planes (tensor-core path only)
-  void* dnb = nullptr;   // K-blocked copy of the down planes (one-launch decode path only)
+  void* dnb = nullptr;   // decode-layout copy of the experts (one-launch decode path only)
 };
 
 struct moe_ctx {
@@ -287,10 +287,10 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
     }
   }
   if (h->fused_capable) {
-    // the one-launch decode layer reads the down planes K-blocked: copy them once, here
+    // the one-launch decode layer reads the experts in its own fragment order: copy them once, here
     const moe_config& c = h->cfg;
-    const size_t rb = fused_down_copy_bytes(c.n_experts, c.d, c.f);
-    const size_t sb = c.has_shared ? fused_down_copy_bytes(1, c.d, c.f) : 0;
+    const size_t rb = (fused_layout_bytes(c.n_experts, c.d, c.f) + 255) & ~size_t(255);
+    const size_t sb = c.has_shared ? fused_layout_bytes(1, c.d, c.f) : 0;
     if (!L.dnb && cudaMalloc(&L.dnb, rb + sb) != cudaSuccess) {
       cudaGetLastError();
       L.dnb = nullptr;
@@ -298,13 +298,11 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
       return MOE_ERR_OOM;
     }
     char* base = static_cast<char*>(L.dnb);
-    const size_t rq = ((size_t)c.n_experts * c.d * (c.f / 2) + 255) & ~size_t(255);
-    const size_t sq = ((size_t)c.d * (c.f / 2) + 255) & ~size_t(255);
     // the weights may have been written on any stream: wait for the device before reading them
     cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) e = repack_down_blocked(w->dn_q, w->dn_s, c.n_experts, c.d, c.f, base, base + rq, nullptr);
+    if (e == cudaSuccess) e = fused_repack(w->gu_q, w->gu_s, w->dn_q, w->dn_s, c.n_experts, c.d, c.f, base, nullptr);
     if (e == cudaSuccess && c.has_shared)
-      e = repack_down_blocked(w->sh_dn_q, w->sh_dn_s, 1, c.d, c.f, base + rb, base + rb + sq, nullptr);
+      e = fused_repack(w->sh_gu_q, w->sh_gu_s, w->sh_dn_q, w->sh_dn_s, 1, c.d, c.f, base + rb, nullptr);
     if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
     if (e != cudaSuccess) {
       g_last_cuda_error = (int)e;
@@ -402,14 +400,10 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
     ExpertArgs ea = make_expert_args(h, layer, x, T, y, resid);
     const moe_config& c = h->cfg;
     char* base = static_cast<char*>(h->layers[layer].dnb);
-    const size_t rb = fused_down_copy_bytes(c.n_experts, c.d, c.f);
-    const size_t rq = ((size_t)c.n_experts * c.d * (c.f / 2) + 255) & ~size_t(255);
-    const size_t sq = ((size_t)c.d * (c.f / 2) + 255) & ~size_t(255);
+    const size_t rb = (fused_layout_bytes(c.n_experts, c.d, c.f) + 255) & ~size_t(255);
     FusedExtra fx;
-    fx.dnb_q = base;
-    fx.dnb_s = base + rq;
-    fx.sh_dnb_q = c.has_shared ? base + rb : nullptr;
-    fx.sh_dnb_s = c.has_shared ? base + rb + sq : nullptr;
+    fx.dl = base;
+    fx.sh_dl = c.has_shared ? base + rb : nullptr;
     fx.part = h->part;
     fx.grid_bar = h->grid_bar;
     e = launch_decode_fused(ra, ea, fx, st);

@@ -177,10 +177,8 @@ struct ExpertArgs {
 
 // Extra arguments of the one-launch decode layer.
 struct FusedExtra {
-  const void* dnb_q;     // [E][f/8][d] uint32: K-blocked routed down codes (8 columns of one row per word)
-  const void* dnb_s;     // [E][f/32][d] fp16: their scales
-  const void* sh_dnb_q;  // the shared expert's, same layout (E = 1), or null
-  const void* sh_dnb_s;
+  const void* dl;        // the routed experts' decode-layout copy (unit blocks, then down scales)
+  const void* sh_dl;     // the shared expert's, or null
   float* part;           // [#SM][T][d] per-CTA partial outputs
   unsigned long long* grid_bar;
 };

@@ -1,5 +1,6 @@
 // Decode / verify layer in one launch (sm_103a): router logits, softmax + top-K, dispatch, the
-// gate/up and down GEMVs of the selected and shared experts, and the fixed-order combine.
+// gate/up and down projections of the selected and shared experts on tensor cores, and the
+// fixed-order combine.
 //
 // A decode step streams the bytes of the experts its few tokens chose and little else
 // ('Strata はなぜ少ない VRAM でも速いのか' (modeldock.net), section '1 トークン、三者の分担';
@@ -16,19 +17,20 @@
 //   phase 2  every CTA reads all logits and repeats the selection (one warp per token) and the
 //            dispatch in shared memory (identical, deterministic); CTA 0 publishes them;
 //   phase 3  the routed work, (slot, f-column) in units of 8 columns numbered slot-major, is cut
-//            into #CTA contiguous ranges.  A CTA streams, per window of at most 16 columns, the
-//            gate and up rows of those columns and the down weights of the same columns (a
-//            K-blocked copy of the down planes makes them one contiguous block) into a ring of
-//            shared-memory stages, computes h = silu(g) * u for them and at once their share of
-//            the down projection, w_k * W_down[:, cols] h[cols], for all d outputs.  No h leaves
-//            the CTA; each CTA ends with a partial output [T][d];                 [grid barrier]
+//            into #CTA contiguous ranges.  A CTA streams its units with one bulk copy per stage
+//            (plus the stage's down scales) from the layer's decode-layout copy into a ring of
+//            shared-memory stages and runs, per stage, gate/up as m16n8k16 tensor-core tiles
+//            (16 rows = 8 gate + 8 up rows of a unit, N = the slot's tokens), h = w silu(g) u in
+//            fp16, and the down share of those columns for all d outputs as m16n8k8 tiles into
+//            fp32 accumulators that stay in registers; each CTA ends with a partial [T][d]; [grid barrier]
 //   phase 4  each CTA sums the #CTA partials of its d / #CTA output rows in CTA order (a fixed
 //            order: the run is bit-reproducible), adds the optional residual and writes y.
 //
-// The arithmetic per product is that of the split-K GEMV path: int4 codes become fp32 0.5 + o/256
-// by one byte permute, x' = 256 x, sum q x = sum v x' - 136 sum x, one fp16 group scale per 32.
-// Every wait is bounded; on timeout the CTA records MOE status "timeout", stops issuing and
-// waits (bounded) for its copies in flight before exiting.
+// Tensor-core operands: int4 codes become fp16 q exactly (two bit operations and one f16x2
+// subtract per pair), x is fp16 (bf16 activations are exact in fp16 inside its range) and
+// w * h is rounded once to fp16; every group of 32 codes is summed in fp32 and scaled by its
+// fp16 group scale in fp32.  Every wait is bounded; on timeout the CTA records MOE status
+// "timeout", stops issuing and waits (bounded) for its copies in flight before exiting.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -39,15 +41,35 @@ namespace moe {
 
 constexpr int kFzWarps = 16;                     // consumer warps
 constexpr int kFzThreads = (kFzWarps + 1) * 32;  // + one producer warp
-constexpr int kFzMaxT = 8;
+constexpr int kFzMaxT = 8;                       // tokens: the N of the tensor-core tiles
 constexpr int kFzMaxStages = 8;
-constexpr int kFzUnit = 8;                       // columns per down block and per work unit
-constexpr int kFzWin = 16;                       // columns per stage window (one gate/up pair per warp)
+constexpr int kFzUnit = 8;                       // columns per work unit
+constexpr int kFzStageUnits = 2;                 // units per stage (inside one 32-column group)
 constexpr int kFzSmemMax = 227 * 1024;
 constexpr int kFzReduceLoads = 8;                // final sum: up to 32 * 8 CTAs
 constexpr unsigned kFzSpinLimit = 1u << 24;      // grid-barrier polls, at least 32 ns apart
 constexpr unsigned kFzProducerSleep = 200;        // ns between polls of the producer's waits
 constexpr unsigned kFzConsumerSleep = 64;         // ns between polls of a waiting consumer warp
+
+// ------------------------------------------------------------------ decode layout
+// The one-launch layer reads its own copy of each layer's experts, written by moe_set_layer in
+// the order of its tensor-core fragments (same bytes as the row-major planes; codes stored as
+// offset binary o = q + 8).  Per expert, f/8 unit blocks of dl_unit_bytes(d) each, unit u =
+// columns 8u .. 8u+7:
+//   gate/up part, per k-tile kt < d/128 (128 columns of K), 1152 bytes:
+//     codes [lane 32][half 2][j 4] u32: lane = 4g + t; half 0 = gate row 8u + g, half 1 = up row
+//       f + 8u + g; the word = the 8 codes of columns 32 (4 kt + j) + 8t .. + 7 of that row
+//       (code i in bits 4i .. 4i + 3);
+//     scales [g 8][half 2][j 4] fp16 at byte 1024: group 4 kt + j of those rows;
+//   down part, 4d bytes, [pair p < d/32][lane 32] u32: rows 32p .. 32p + 31 of the down matrix,
+//     columns 8u + 2t (bits 0-3, 4-7, 8-11, 12-15) and 8u + 2t + 1 (bits 16-19 .. 28-31) of rows
+//     32p + g, 32p + g + 8, 32p + 16 + g, 32p + 24 + g.
+// The down scales follow all unit blocks: per expert [group f/32][warp 16][g 8][tile i < d/256]
+// [r 2] fp16 = the scale of down row w d/16 + 16 i + g + 8 r.
+__host__ __device__ inline size_t dl_gu_bytes(int d) { return (size_t)(d / 128) * 1152; }
+__host__ __device__ inline size_t dl_unit_bytes(int d) { return dl_gu_bytes(d) + (size_t)d * 4; }
+__host__ __device__ inline size_t dl_expert_bytes(int d, int f) { return (size_t)(f / kFzUnit) * dl_unit_bytes(d); }
+__host__ __device__ inline size_t dl_scale_bytes(int d, int f) { return (size_t)(f / 32) * d * 2; }
 
 struct FusedArgs {
   const void* x;
@@ -66,14 +88,10 @@ struct FusedArgs {
   int32_t* n_active;
   int32_t* stat;
   int4* slots;
-  const uint8_t* gu_q;     // [E][2f][d/2] routed gate/up codes (rows 0..f-1 gate, f..2f-1 up)
-  const __half* gu_s;      // [E][2f][d/32]
-  const uint32_t* dnb_q;   // [E][f/8][d] routed down codes, K-blocked: word = 8 columns of one row
-  const __half* dnb_s;     // [E][f/32][d] their scales
-  const uint8_t* sh_gu_q;  // the shared expert, same layouts with E = 1
-  const __half* sh_gu_s;
-  const uint32_t* sh_dnb_q;
-  const __half* sh_dnb_s;
+  const uint8_t* dl;       // routed experts, decode layout: [E] expert blocks
+  const uint8_t* dls;      // their down scales: [E][dl_scale_bytes]
+  const uint8_t* sh_dl;    // the shared expert, same layouts
+  const uint8_t* sh_dls;
   float* part;             // [gridDim.x][T][d] per-CTA partial outputs
   void* y;
   const void* resid;
@@ -123,249 +141,208 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigne
   return true;
 }
 
-// ------------------------------------------------------------------ gate/up dot products
-// 2*NP int4 rows against TB tokens of x' (group-interleaved [t][8][G] float4), all in shared memory:
-// rows r < NP are gate rows p = r, rows r >= NP up rows p = r - NP, at gq/uq + min-clamped p*qrow
-// (rows p >= np repeat row 0), scales at gs/us + p*G.  Lane-partial sums acc[r][tt]; each x' load
-// is shared by all rows.  Lane = 32-column groups lane, lane+32, ...
-template <int NG, int TB, int NP>
-__device__ __forceinline__ void pairs_dot(const uint8_t* gq, const uint8_t* uq, const __half* gs, const __half* us,
-                                          size_t qrow, int np, int G, const float4* xq, const float* xs136,
-                                          const int (&tok)[TB], float (&acc)[2 * NP][TB], int lane) {
-  constexpr int ROWS = 2 * NP;
-#pragma unroll
-  for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-    for (int tt = 0; tt < TB; ++tt) acc[r][tt] = 0.f;
-#pragma unroll 1
-  for (int j = 0; j < NG; ++j) {
-    const int g = lane + 32 * j;
-    if (g >= G) continue;
-    uint4 wq[ROWS];
-#pragma unroll
-    for (int r = 0; r < ROWS; ++r) {
-      const int p = r < NP ? r : r - NP;
-      const int pp = p < np ? p : 0;
-      wq[r] = *reinterpret_cast<const uint4*>((r < NP ? gq : uq) + pp * qrow + g * 16);
-    }
-    float part[ROWS][TB];
-#pragma unroll
-    for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-      for (int tt = 0; tt < TB; ++tt) part[r][tt] = 0.f;
-#pragma unroll
-    for (int wd = 0; wd < 4; ++wd) {
-      float4 xa[TB], xb[TB];
-#pragma unroll
-      for (int tt = 0; tt < TB; ++tt) {
-        const float4* xp = xq + (size_t)tok[tt] * 8 * G + g;
-        xa[tt] = xp[(2 * wd) * G];
-        xb[tt] = xp[(2 * wd + 1) * G];
-      }
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r) {
-        const uint32_t w32 = wd == 0 ? wq[r].x : wd == 1 ? wq[r].y : wd == 2 ? wq[r].z : wq[r].w;
-        const uint32_t lo = (w32 & 0x0F0F0F0Fu) ^ 0x08080808u;
-        const uint32_t hi = ((w32 >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-        const float v0 = v_lo(lo, 0), v1 = v_lo(hi, 0), v2 = v_lo(lo, 1), v3 = v_lo(hi, 1);
-        const float v4 = v_lo(lo, 2), v5 = v_lo(hi, 2), v6 = v_lo(lo, 3), v7 = v_lo(hi, 3);
-#pragma unroll
-        for (int tt = 0; tt < TB; ++tt) {
-          float a2 = part[r][tt];
-          a2 = fmaf(v0, xa[tt].x, a2);
-          a2 = fmaf(v1, xa[tt].y, a2);
-          a2 = fmaf(v2, xa[tt].z, a2);
-          a2 = fmaf(v3, xa[tt].w, a2);
-          a2 = fmaf(v4, xb[tt].x, a2);
-          a2 = fmaf(v5, xb[tt].y, a2);
-          a2 = fmaf(v6, xb[tt].z, a2);
-          a2 = fmaf(v7, xb[tt].w, a2);
-          part[r][tt] = a2;
-        }
-      }
-    }
-#pragma unroll
-    for (int tt = 0; tt < TB; ++tt) {
-      const float x136 = xs136[tok[tt] * G + g];
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r) {
-        const int p = r < NP ? r : r - NP;
-        const int pp = p < np ? p : 0;
-        const float sc = __half2float((r < NP ? gs : us)[(size_t)pp * G + g]);
-        acc[r][tt] = fmaf(sc, part[r][tt] - x136, acc[r][tt]);
-      }
-    }
-  }
+// ------------------------------------------------------------------ tensor-core helpers
+// D += A B for one m16n8k16 (A 16x16 row-major fp16, B 16x8 fp16, fp32 accumulators) and one
+// m16n8k8 tile, in the register fragments of the PTX mma.sync description: lane = 4g + t holds
+// A rows g and g + 8, B column g, C rows g and g + 8 at columns 2t and 2t + 1.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(b0));
 }
 
-// ------------------------------------------------------------------ stages
-// A stage holds at most kFzWin columns [col, col + n) of one expert, n a multiple of kFzUnit, all
-// inside one kFzWin-aligned window (so inside one 32-column scale group of the down weights):
-// the n gate rows and n up rows (d/2 code bytes, d/32 fp16 scales each), the n/8 down blocks
-// ([d] words of 8 columns) and the [d] down scales of the group.  Byte offsets for d:
-struct StageLayout {
-  uint32_t uq, gs, us, dq, ds, bytes;
-};
-__host__ __device__ inline StageLayout stage_layout(int d) {
-  const uint32_t qrow = (uint32_t)d / 2, srow = (uint32_t)d / 16;
-  StageLayout L;
-  L.uq = kFzWin * qrow;
-  L.gs = 2u * kFzWin * qrow;
-  L.us = L.gs + kFzWin * srow;
-  L.dq = L.us + kFzWin * srow;
-  L.ds = L.dq + (kFzWin / kFzUnit) * 4u * (uint32_t)d;
-  L.bytes = L.ds + 2u * (uint32_t)d;
-  return L;
+// Two offset-binary int4 codes of a word as the fp16 pair (q, q'), q = o - 8, exact: q_lo takes
+// the codes in bits 0-3 and 16-19 (1024 + o through the exponent of 1024, minus 1032), q_hi those
+// in bits 4-7 and 20-23 (1024 + 16 o, times 1/16, minus 72).
+__device__ __forceinline__ uint32_t q_lo(uint32_t w) {
+  const uint32_t p = (w & 0x000F000Fu) | 0x64006400u;
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(0x64086408u));  // 1032
+  return r;
 }
-
-// The bulk copies of one stage: expert e of the given planes, columns [col, col + n).
-__device__ __forceinline__ void issue_stage(uint8_t* dst, const StageLayout& L, const uint8_t* gu_q,
-                                            const __half* gu_s, const uint32_t* dnb_q, const __half* dnb_s, int e,
-                                            int col, int n, int d, int f, uint64_t* bar) {
-  const size_t qrow = (size_t)d / 2, G = (size_t)d / 32;
-  const size_t rg = (size_t)e * 2 * f + col, ru = rg + f;
-  const uint32_t nq = (uint32_t)(n * qrow), nsc = (uint32_t)(n * G * 2);
-  const uint32_t nd = (uint32_t)(n / kFzUnit) * 4u * (uint32_t)d;
-  tc::mbar_arrive_expect_tx(bar, 2 * nq + 2 * nsc + nd + 2u * (uint32_t)d);
-  tc::bulk_g2s(dst, gu_q + rg * qrow, nq, bar);
-  tc::bulk_g2s(dst + L.uq, gu_q + ru * qrow, nq, bar);
-  tc::bulk_g2s(dst + L.gs, gu_s + rg * G, nsc, bar);
-  tc::bulk_g2s(dst + L.us, gu_s + ru * G, nsc, bar);
-  tc::bulk_g2s(dst + L.dq, dnb_q + ((size_t)e * (f / kFzUnit) + col / kFzUnit) * d, nd, bar);
-  tc::bulk_g2s(dst + L.ds, dnb_s + ((size_t)e * (f / 32) + col / 32) * d, 2u * (uint32_t)d, bar);
+__device__ __forceinline__ uint32_t q_hi(uint32_t w) {
+  const uint32_t p = (w & 0x00F000F0u) | 0x64006400u;
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(p), "r"(0x2C002C00u), "r"(0xD480D480u));  // 1/16, -72
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);  // lo in the low 16 bits
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float half_of(uint32_t v, int hi) {
+  return __half2float(__ushort_as_half((unsigned short)(hi ? (v >> 16) : (v & 0xFFFFu))));
 }
 
 // A CTA's routed work: units [pos, end) of kFzUnit columns, numbered slot-major (slot * f/8 + u).
-// Stages are cut at slot boundaries and at kFzWin-column windows.
+// Stages are cut at slot boundaries and at kFzStageUnits-unit windows (inside one 32-column
+// scale group of the down weights).
 struct UnitRange {
   int pos, end;
 };
-__device__ __forceinline__ bool next_stage(UnitRange& r, int fu, int& s, int& col, int& n) {
+__device__ __forceinline__ bool next_stage(UnitRange& r, int fu, int& s, int& u0, int& nu) {
   if (r.pos >= r.end) return false;
   s = r.pos / fu;
   const int u = r.pos - s * fu;
-  constexpr int wu = kFzWin / kFzUnit;
-  const int ue = min(min((u / wu + 1) * wu, fu), u + (r.end - r.pos));
-  col = u * kFzUnit;
-  n = (ue - u) * kFzUnit;
-  r.pos += ue - u;
+  const int ue = min(min((u / kFzStageUnits + 1) * kFzStageUnits, fu), u + (r.end - r.pos));
+  u0 = u;
+  nu = ue - u;
+  r.pos += nu;
   return true;
 }
 
-// h of one column for TB tokens of a slot: the tokens of assignments perm_s[pb + t0 ..] (or, for
-// the shared expert, pb < 0, tokens t0 ..); stores 256 * silu(g) * u at hcol[(t0 + tt) * kFzWin].
-template <int NG, int TB>
-__device__ __forceinline__ void col_h(const uint8_t* gq, const uint8_t* uq, const __half* gs, const __half* us,
-                                      size_t qrow, int G, int t0, int pb, int K, const int* perm_s, const float4* xq,
-                                      const float* xs136, float* hcol, int lane) {
-  int tok[TB];
-#pragma unroll
-  for (int tt = 0; tt < TB; ++tt) tok[tt] = pb >= 0 ? perm_s[pb + t0 + tt] / K : t0 + tt;
-  float acc[2][TB];
-  pairs_dot<NG, TB, 1>(gq, uq, gs, us, qrow, 1, G, xq, xs136, tok, acc, lane);
-  constexpr int NV = 2 * TB;             // gate values of the TB tokens, then up values
-  constexpr int SH = NV == 4 ? 3 : 4;    // value i's total sits in the lanes with lane >> SH == i
-  float vals[NV];
-#pragma unroll
-  for (int tt = 0; tt < TB; ++tt) {
-    vals[tt] = acc[0][tt];
-    vals[TB + tt] = acc[1][tt];
-  }
-  const float g = warp_sum_multi<NV>(vals);
-  const float u = __shfl_down_sync(0xffffffffu, g, 16);  // the up value of the same token
-  if (lane < 16 && (lane & ((1 << SH) - 1)) == 0) hcol[(t0 + (lane >> SH)) * kFzWin] = 256.f * (silu(g) * u);
+// The two bulk copies of a stage: units [u0, u0 + nu) of one expert (its unit blocks at dl, its
+// down scales at dls) into dst; the scales of the units' group go after kFzStageUnits blocks.
+__device__ __forceinline__ void issue_stage(uint8_t* dst, const uint8_t* dl, const uint8_t* dls, int u0, int nu,
+                                            int d, uint64_t* bar) {
+  const size_t ub = dl_unit_bytes(d);
+  const uint32_t nb = (uint32_t)(nu * ub), sb = (uint32_t)(2 * d);
+  tc::mbar_arrive_expect_tx(bar, nb + sb);
+  tc::bulk_g2s(dst, dl + (size_t)u0 * ub, nb, bar);
+  tc::bulk_g2s(dst + kFzStageUnits * ub, dls + (size_t)(u0 / 4) * 2 * d, sb, bar);
 }
 
-// sum over the 8 columns of one down word (8 int4 codes of one row) of v * h', v = 0.5 + o/256.
-__device__ __forceinline__ float dot8(uint32_t w, const float4& ha, const float4& hb, float acc) {
-  const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-  acc = fmaf(v_lo(lo, 0), ha.x, acc);
-  acc = fmaf(v_lo(hi, 0), ha.y, acc);
-  acc = fmaf(v_lo(lo, 1), ha.z, acc);
-  acc = fmaf(v_lo(hi, 1), ha.w, acc);
-  acc = fmaf(v_lo(lo, 2), hb.x, acc);
-  acc = fmaf(v_lo(hi, 2), hb.y, acc);
-  acc = fmaf(v_lo(lo, 3), hb.z, acc);
-  acc = fmaf(v_lo(hi, 3), hb.w, acc);
-  return acc;
-}
-
-// One stage: h of its n columns for the nt tokens of its slot (assignments perm_s[pb ..], weights
-// w_s; pb < 0: the shared expert, tokens 0 .. nt-1, weight 1), then the down share of those
-// columns, y_s[t][r] += w * sum_{c in stage} W_down[r][c] h[t][c], every thread for its row quads.
-// Uniform over the consumer threads (one consumers_sync inside).  hb: [kFzMaxT][kFzWin].
-template <int NG>
-__device__ __noinline__ void run_stage(const FusedArgs& a, const uint8_t* stg, const StageLayout& L, int n,
-                                          int pb, int nt, const int* perm_s, const float* w_s, const float4* xq,
-                                          const float* xs136, float* hb, float* y_s, int warp, int lane, int ctid) {
-  const int d = a.d, G = d / 32, K = a.K;
-  const size_t qrow = (size_t)d / 2;
-  if (warp < n) {
-    // gate/up: warp w computes column w, two tokens per pass where it can
-    const uint8_t* gq = stg + (size_t)warp * qrow;
-    const uint8_t* uq = stg + L.uq + (size_t)warp * qrow;
-    const __half* gs = reinterpret_cast<const __half*>(stg + L.gs) + (size_t)warp * G;
-    const __half* us = reinterpret_cast<const __half*>(stg + L.us) + (size_t)warp * G;
-    int t0 = 0;
-    for (; t0 + 2 <= nt; t0 += 2) col_h<NG, 2>(gq, uq, gs, us, qrow, G, t0, pb, K, perm_s, xq, xs136, hb + warp, lane);
-    if (t0 < nt) col_h<NG, 1>(gq, uq, gs, us, qrow, G, t0, pb, K, perm_s, xq, xs136, hb + warp, lane);
-  }
-  consumers_sync();
-  // down: 4 rows (one 16-byte group of words per block) per thread and pass
-  const uint4* dq0 = reinterpret_cast<const uint4*>(stg + L.dq);
-  const uint4* dq1 = reinterpret_cast<const uint4*>(stg + L.dq + 4u * (uint32_t)d);
-  const uint2* dsq = reinterpret_cast<const uint2*>(stg + L.ds);
-  const bool two = n > kFzUnit;
-  #pragma unroll 1
-  for (int qd = ctid; qd < d / 4; qd += kFzWarps * 32) {
-    const uint4 w0 = dq0[qd];
-    const uint4 w1 = two ? dq1[qd] : make_uint4(0u, 0u, 0u, 0u);
-    const uint2 sv = dsq[qd];
-    const float s0 = __half2float(__ushort_as_half((unsigned short)(sv.x & 0xFFFFu)));
-    const float s1 = __half2float(__ushort_as_half((unsigned short)(sv.x >> 16)));
-    const float s2 = __half2float(__ushort_as_half((unsigned short)(sv.y & 0xFFFFu)));
-    const float s3 = __half2float(__ushort_as_half((unsigned short)(sv.y >> 16)));
-    #pragma unroll 1
-    for (int j = 0; j < nt; ++j) {
-      const int as = pb >= 0 ? perm_s[pb + j] : 0;
-      const int t = pb >= 0 ? as / K : j;
-      const float wt = pb >= 0 ? w_s[as] : 1.f;
-      const float4* hp = reinterpret_cast<const float4*>(hb + j * kFzWin);
-      const float4 h0 = hp[0], h1 = hp[1];
-      float hs = (h0.x + h0.y) + (h0.z + h0.w) + ((h1.x + h1.y) + (h1.z + h1.w));
-      float a0 = dot8(w0.x, h0, h1, 0.f), a1 = dot8(w0.y, h0, h1, 0.f);
-      float a2 = dot8(w0.z, h0, h1, 0.f), a3 = dot8(w0.w, h0, h1, 0.f);
-      if (two) {
-        const float4 h2 = hp[2], h3 = hp[3];
-        hs += (h2.x + h2.y) + (h2.z + h2.w) + ((h3.x + h3.y) + (h3.z + h3.w));
-        a0 = dot8(w1.x, h2, h3, a0);
-        a1 = dot8(w1.y, h2, h3, a1);
-        a2 = dot8(w1.z, h2, h3, a2);
-        a3 = dot8(w1.w, h2, h3, a3);
-      }
-      // h' = 256 h and v = (q + 136) / 256: sum v h' - 136 sum h = sum q h
-      hs *= 136.0f / 256.0f;
-      const float ws = wt;
-      float4* yp = reinterpret_cast<float4*>(y_s + (size_t)t * d) + qd;
-      float4 yv = *yp;
-      yv.x = fmaf(ws * s0, a0 - hs, yv.x);
-      yv.y = fmaf(ws * s1, a1 - hs, yv.y);
-      yv.z = fmaf(ws * s2, a2 - hs, yv.z);
-      yv.w = fmaf(ws * s3, a3 - hs, yv.w);
-      *yp = yv;
+// Gate/up of a stage: warp w takes the items i = w + 16 m < nu * d/128 (unit i % nu, k-tile
+// i / nu) and leaves its fp32 partial tile in pgu[w][lane]: rows g (gate of column 8u + g) and
+// g + 8 (up), slot-local tokens 2t and 2t + 1.  xtok: the global token of slot-local token g
+// (lane >> 2), or -1 past the slot's tokens; xh: x as fp16 fragments [T][d/32][t 4][4 pairs].
+__device__ __forceinline__ void gu_stage(const uint8_t* stg, int nu, int d, int xtok, const uint4* xh, float4* pgu,
+                                         int warp, int lane) {
+  const int KT = d / 128, G = d / 32, t = lane & 3;
+  const size_t ub = dl_unit_bytes(d);
+  const int items = nu * KT;
+  if (warp >= items) return;
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  const int u = warp % nu;
+#pragma unroll 1
+  for (int i = warp; i < items; i += kFzWarps) {
+    const int kt = i / nu;
+    const uint8_t* blk = stg + u * ub + (size_t)kt * 1152;
+    const uint4 wg = *reinterpret_cast<const uint4*>(blk + lane * 32);
+    const uint4 wu = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
+    const uint4 sc = *reinterpret_cast<const uint4*>(blk + 1024 + (lane >> 2) * 16);
+    uint4 xb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      xb[j] = xtok >= 0 ? xh[((size_t)xtok * G + 4 * kt + j) * 4 + t] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w0 = j == 0 ? wg.x : j == 1 ? wg.y : j == 2 ? wg.z : wg.w;
+      const uint32_t w1 = j == 0 ? wu.x : j == 1 ? wu.y : j == 2 ? wu.z : wu.w;
+      float dg[4] = {0.f, 0.f, 0.f, 0.f};
+      // k-step 0: codes 0, 4 (K slots 2t, 2t+1) and 1, 5 (2t+8, 2t+9); k-step 1: codes 2, 6 and 3, 7
+      mma_16816(dg, q_lo(w0), q_lo(w1), q_hi(w0), q_hi(w1), xb[j].x, xb[j].y);
+      mma_16816(dg, q_lo(w0 >> 8), q_lo(w1 >> 8), q_hi(w0 >> 8), q_hi(w1 >> 8), xb[j].z, xb[j].w);
+      const uint32_t s01 = j < 2 ? sc.x : sc.y, s23 = j < 2 ? sc.z : sc.w;  // [half][j] fp16
+      const float sg = half_of(s01, j & 1), su = half_of(s23, j & 1);
+      c[0] = fmaf(sg, dg[0], c[0]);
+      c[1] = fmaf(sg, dg[1], c[1]);
+      c[2] = fmaf(su, dg[2], c[2]);
+      c[3] = fmaf(su, dg[3], c[3]);
     }
   }
+  pgu[warp * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
 }
 
-template <int NG>
+// h of a stage, once the gate/up partials are in: thread (u, n, col) of n_u * 64 writes
+// hb[u][n][col] = w silu(gate) up as fp16 for global token n and column 8u + col, where the
+// slot-local token j of token n holds the weight w (perm_s[pb + j], w_s); 0 for tokens outside
+// the slot.  pb < 0: the shared expert, slot-local token = global token < nt, weight 1.  The
+// partials of a unit are summed over its warps in warp order.
+__device__ __forceinline__ void h_stage(int nu, int d, int pb, int nt, int K, const int* perm_s, const float* w_s,
+                                        const float4* pgu, __half* hb, int ctid) {
+  if (ctid >= nu * 64) return;
+  const int u = ctid >> 6, n = (ctid >> 3) & 7, col = ctid & 7;
+  int j = -1;
+  float wt = 1.f;
+  if (pb < 0) {
+    if (n < nt) j = n;
+  } else {
+#pragma unroll 1
+    for (int q = 0; q < nt; ++q)
+      if (perm_s[pb + q] / K == n) {
+        j = q;
+        wt = w_s[perm_s[pb + q]];
+      }
+  }
+  float hv = 0.f;
+  if (j >= 0) {
+    const int items = nu * (d / 128);
+    const int ln = col * 4 + (j >> 1);
+    float g = 0.f, up = 0.f;
+#pragma unroll 1
+    for (int w = u; w < kFzWarps && w < items; w += nu) {
+      const float4 p = pgu[w * 32 + ln];
+      g += (j & 1) ? p.y : p.x;
+      up += (j & 1) ? p.w : p.z;
+    }
+    hv = wt * (silu(g) * up);
+  }
+  hb[(u * 8 + n) * 8 + col] = __float2half_rn(hv);
+}
+
+// Down share of a stage for the warp's TPW row tiles (rows w d/16 + 16 i + g, + 8): D over the
+// stage's units (one scale group), then C += s D in fp32.
+template <int TPW>
+__device__ __forceinline__ void dn_stage(const uint8_t* stg, int nu, int d, const __half* hb, float (&C)[TPW][4],
+                                         int warp, int lane) {
+  const size_t ub = dl_unit_bytes(d), gb = dl_gu_bytes(d);
+  const int g = lane >> 2, t = lane & 3;
+  float D[TPW][4];
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) D[i][0] = D[i][1] = D[i][2] = D[i][3] = 0.f;
+#pragma unroll 1
+  for (int u = 0; u < nu; ++u) {
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(hb + (u * 8 + g) * 8 + 2 * t);
+    const uint32_t* dw = reinterpret_cast<const uint32_t*>(stg + u * ub + gb) + (size_t)warp * (TPW / 2) * 32 + lane;
+#pragma unroll
+    for (int ip = 0; ip < TPW / 2; ++ip) {
+      const uint32_t w = dw[ip * 32];
+      mma_1688(D[2 * ip], q_lo(w), q_hi(w), b);
+      mma_1688(D[2 * ip + 1], q_lo(w >> 8), q_hi(w >> 8), b);
+    }
+  }
+  const uint32_t* sp = reinterpret_cast<const uint32_t*>(stg + kFzStageUnits * ub) + ((size_t)warp * 8 + g) * TPW;
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) {
+    const uint32_t s = sp[i];  // rows g, g + 8 of tile i
+    const float s0 = half_of(s, 0), s1 = half_of(s, 1);
+    C[i][0] = fmaf(s0, D[i][0], C[i][0]);
+    C[i][1] = fmaf(s0, D[i][1], C[i][1]);
+    C[i][2] = fmaf(s1, D[i][2], C[i][2]);
+    C[i][3] = fmaf(s1, D[i][3], C[i][3]);
+  }
+}
+
+// One stage: gate/up partials, h, down.  Uniform over the consumer threads (two consumers_sync).
+template <int TPW>
+__device__ __forceinline__ void run_stage(const uint8_t* stg, int nu, int d, int pb, int nt, int K, const int* perm_s,
+                                          const float* w_s, const uint4* xh, float4* pgu, __half* hb,
+                                          float (&C)[TPW][4], int warp, int lane, int ctid) {
+  const int gl = lane >> 2;
+  const int xtok = gl < nt ? (pb >= 0 ? perm_s[pb + gl] / K : gl) : -1;
+  gu_stage(stg, nu, d, xtok, xh, pgu, warp, lane);
+  consumers_sync();
+  h_stage(nu, d, pb, nt, K, perm_s, w_s, pgu, hb, ctid);
+  consumers_sync();
+  dn_stage<TPW>(stg, nu, d, hb, C, warp, lane);
+}
+
+template <int TPW>
 __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int T = a.T, d = a.d, E = a.E, K = a.K, f = a.f, G = d / 32;
   const int nc = gridDim.x, c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.ns, SB = a.stage_bytes;
-  const StageLayout L = stage_layout(d);
   const int fu = f / kFzUnit, QD = d / 4;
+  const size_t eb = dl_expert_bytes(d, f), sbytes = dl_scale_bytes(d, f);
 
   // this CTA's fixed shares
   const int e0 = (int)((long long)E * c / nc), ne = (int)((long long)E * (c + 1) / nc) - e0;  // router rows
@@ -373,13 +350,14 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   const int q0 = (int)((long long)QD * c / nc), q1 = (int)((long long)QD * (c + 1) / nc);    // output row quads
   const bool sh_on = a.has_shared && su1 > su0;
 
-  // shared memory carve (all offsets 16-byte multiples); the router rows use ring stage 1 and the
-  // shared-expert stage ring stage 0: both are done with before the routed stages are issued
+  // shared memory carve (all offsets 16-byte multiples); the router rows use ring stage 1, the
+  // shared-expert stage and the selection's keys ring stage 0: all are done with before the
+  // routed stages are issued
   uint8_t* ring = smem_raw;
-  float4* xq = reinterpret_cast<float4*>(ring + (size_t)NS * SB);  // x' = 256 x, [T][8][G] float4
-  float* xs136 = reinterpret_cast<float*>(xq + (size_t)T * 8 * G);  // [T][G]: 136 * (sum of x per group)
-  float* y_s = xs136 + (size_t)T * G;                               // [T][d] partial output
-  int4* slot_s = reinterpret_cast<int4*>(y_s + (size_t)T * d);      // [T*K]
+  float* x32 = reinterpret_cast<float*>(ring + (size_t)NS * SB);     // [T][d] x (optionally normalised)
+  uint4* xh = reinterpret_cast<uint4*>(x32 + (size_t)T * d);          // [T][G][4][4 fp16 pairs]
+  float4* pgu = reinterpret_cast<float4*>(xh + (size_t)T * G * 4);   // [16 warps][32 lanes]
+  int4* slot_s = reinterpret_cast<int4*>(pgu + kFzWarps * 32);       // [T*K]
   int* perm_s = reinterpret_cast<int*>(slot_s + T * K);
   int* idx_s = perm_s + T * K;
   float* w_s = reinterpret_cast<float*>(idx_s + T * K);
@@ -387,7 +365,7 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   uint8_t* sh_stg = ring;
 
   __shared__ __align__(8) uint64_t full[kFzMaxStages], empty[kFzMaxStages], wr_full, sh_full, route_ready;
-  __shared__ __align__(16) float hbuf[2][kFzMaxT * kFzWin];
+  __shared__ __align__(16) __half hb[kFzStageUnits * 8 * 8];
   __shared__ float lpart[kFzWarps * kFzMaxT];
   __shared__ int s_srt[kFzMaxT * kMaxK];
   __shared__ float inv_s[kFzMaxT];
@@ -399,7 +377,6 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   // shared memory and read-only weights; activations, workspace and the barrier counter come after.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
-    #pragma unroll 1
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], kFzWarps);
@@ -421,22 +398,21 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
         tc::mbar_arrive_expect_tx(&wr_full, (uint32_t)(ne * d * 4));
         tc::bulk_g2s(ring + SB, a.Wr + (size_t)e0 * d, (uint32_t)(ne * d * 4), &wr_full);
       }
-      if (sh_on)
-        issue_stage(sh_stg, L, a.sh_gu_q, a.sh_gu_s, a.sh_dnb_q, a.sh_dnb_s, 0, su0 * kFzUnit, kFzUnit, d, f, &sh_full);
+      if (sh_on) issue_stage(sh_stg, a.sh_dl, a.sh_dls, su0, 1, d, &sh_full);
       bool ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, kFzProducerSleep);
       int k = 0;
       if (ok) {
         const long long U = (long long)s_nact * fu;
         UnitRange ur{(int)(U * c / nc), (int)(U * (c + 1) / nc)};
-        int s, col, n;
-        while (next_stage(ur, fu, s, col, n)) {
+        int s, u0, nu;
+        while (next_stage(ur, fu, s, u0, nu)) {
           const int st = k % NS;
           if (!tc::mbar_wait_sleepy(&empty[st], ((k / NS) & 1) ^ 1u, &s_abort, kFzProducerSleep)) {
             ok = false;
             break;
           }
-          issue_stage(ring + (size_t)st * SB, L, a.gu_q, a.gu_s, a.dnb_q, a.dnb_s, slot_s[s].x, col, n, d, f,
-                      &full[st]);
+          const int e = slot_s[s].x;
+          issue_stage(ring + (size_t)st * SB, a.dl + (size_t)e * eb, a.dls + (size_t)e * sbytes, u0, nu, d, &full[st]);
           s_issued = ++k;
         }
       }
@@ -450,8 +426,9 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     // ================================================================ consumers
     const int ctid = threadIdx.x;
     bool ok = true;
-    #pragma unroll 1
-    for (int i = ctid; i < T * QD; i += kFzWarps * 32) reinterpret_cast<float4*>(y_s)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float C[TPW][4];  // this warp's down rows w d/16 + 16 i + g (+ 8), tokens 2t, 2t + 1
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) C[i][0] = C[i][1] = C[i][2] = C[i][3] = 0.f;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are visible
     // the barrier counter's base: the previous launch's barriers are complete and fewer than
@@ -459,7 +436,7 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     unsigned long long bar_base = 0;
     if (ctid == 0) bar_base = ld_acquire_gpu(a.grid_bar) / nc * nc;
 
-    // ---- phase 1: x (optionally RMS-normalised) as x' = 256 x, the router rows, the logits
+    // ---- phase 1: x (optionally RMS-normalised) in fp32 and as fp16 fragments, the logits
     if (a.prenorm) {
       #pragma unroll 1
       for (int t = warp; t < T; t += kFzWarps) {
@@ -477,6 +454,7 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       consumers_sync();
     }
     #pragma unroll 4
+#pragma unroll 4
     for (int cc = ctid; cc < T * d / 8; cc += kFzWarps * 32) {
       float v[8];
       load8_act(a.x, a.act, (size_t)cc * 8, v);
@@ -488,24 +466,21 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
           if (c == 0) store_act(a.xnorm, a.act, (size_t)cc * 8 + q, v[q]);
         }
       }
-      const int g = kk >> 5, m4 = (kk & 31) >> 2;
-      float4* dst = xq + ((size_t)ti * 8 + m4) * G + g;
-      dst[0] = make_float4(v[0] * 256.f, v[1] * 256.f, v[2] * 256.f, v[3] * 256.f);
-      dst[G] = make_float4(v[4] * 256.f, v[5] * 256.f, v[6] * 256.f, v[7] * 256.f);
+      float4* xf = reinterpret_cast<float4*>(x32 + (size_t)cc * 8);
+      xf[0] = make_float4(v[0], v[1], v[2], v[3]);
+      xf[1] = make_float4(v[4], v[5], v[6], v[7]);
+      // fragment order of columns 8w .. 8w+7 of group g: pairs (0,4), (1,5), (2,6), (3,7)
+      const int g = kk >> 5, w = (kk & 31) >> 3;
+      uint4 hv;
+      hv.x = pack_h2(v[0], v[4]);
+      hv.y = pack_h2(v[1], v[5]);
+      hv.z = pack_h2(v[2], v[6]);
+      hv.w = pack_h2(v[3], v[7]);
+      xh[((size_t)ti * G + g) * 4 + w] = hv;
     }
     consumers_sync();
-    #pragma unroll 1
-    for (int i = ctid; i < T * G; i += kFzWarps * 32) {
-      const int ti = i / G, g = i - ti * G;
-      const float* xb = reinterpret_cast<const float*>(xq) + (size_t)ti * 8 * G * 4;
-      float sx = 0.f;
-      #pragma unroll 1
-      for (int m = 0; m < 32; ++m) sx += xb[((m >> 2) * G + g) * 4 + (m & 3)];
-      xs136[i] = sx * (136.0f / 256.0f);
-    }
     {
-      // logits of the router rows [e0, e0 + ne): warp = (row, part of the columns); x' = 256 x,
-      // so the dot product is 256 times the wanted one, exactly
+      // logits of the router rows [e0, e0 + ne): warp = (row, part of the columns)
       const int ncol = d / 4;
       const int nparts = ne > 0 ? max(1, kFzWarps / ne) : 1;
       const int my_e = warp % max(ne, 1), my_p = warp / max(ne, 1);
@@ -517,14 +492,13 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
         float acc[kFzMaxT];
 #pragma unroll
         for (int t = 0; t < kFzMaxT; ++t) acc[t] = 0.f;
-        #pragma unroll 1
+#pragma unroll 2
         for (int cc = cb + lane; cc < ce; cc += 32) {
           const float4 wv = wr[cc];
-          const int g = cc >> 3, m4 = cc & 7;
 #pragma unroll
           for (int t = 0; t < kFzMaxT; ++t) {
             if (t < T) {
-              const float4 xv = xq[((size_t)t * 8 + m4) * G + g];
+              const float4 xv = reinterpret_cast<const float4*>(x32 + (size_t)t * d)[cc];
               acc[t] = fmaf(wv.x, xv.x, acc[t]);
               acc[t] = fmaf(wv.y, xv.y, acc[t]);
               acc[t] = fmaf(wv.z, xv.z, acc[t]);
@@ -543,23 +517,23 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       if (!ok && lane == 0) s_abort = 1;
       consumers_sync();
       if (ok)
-        #pragma unroll 1
+#pragma unroll 1
         for (int i = ctid; i < ne * T; i += kFzWarps * 32) {
           const int le = i / T, t = i - le * T;
           float v = 0.f;
-          #pragma unroll 1
+#pragma unroll 1
           for (int p = 0; p < nparts; ++p) v += lpart[(p * ne + le) * kFzMaxT + t];
-          a.logits[(size_t)t * E + e0 + le] = v * (1.0f / 256.0f) + (a.bias ? a.bias[e0 + le] : 0.f);
+          a.logits[(size_t)t * E + e0 + le] = v + (a.bias ? a.bias[e0 + le] : 0.f);
         }
       consumers_sync();
       if (ctid == 0) grid_arrive(a.grid_bar);  // always arrive: the other CTAs must not wait on this one
     }
 
-    // ---- the shared expert's columns of this CTA while the other CTAs finish their logits
+    // ---- the shared expert's unit of this CTA while the other CTAs finish their logits
     if (sh_on) {
       const bool okw = tc::mbar_wait_warp(&sh_full, 0, &s_abort, kFzConsumerSleep);
       ok = consumers_all(ok && okw && !s_abort);
-      if (ok) run_stage<NG>(a, sh_stg, L, kFzUnit, -1, T, perm_s, w_s, xq, xs136, hbuf[0], y_s, warp, lane, ctid);
+      if (ok) run_stage<TPW>(sh_stg, 1, d, -1, T, K, perm_s, w_s, xh, pgu, hb, C, warp, lane, ctid);
     }
     if (ctid == 0) s_ok = (!s_abort && grid_wait(a.grid_bar, bar_base + nc, &s_abort)) ? 1 : 0;
     consumers_sync();
@@ -663,15 +637,14 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     if (ok) {
       const long long U = (long long)s_nact * fu;
       UnitRange ur{(int)(U * c / nc), (int)(U * (c + 1) / nc)};
-      int s, col, n, k = 0;
-      while (next_stage(ur, fu, s, col, n)) {
+      int s, u0, nu, k = 0;
+      while (next_stage(ur, fu, s, u0, nu)) {
         const int st = k % NS;
         const bool okw = tc::mbar_wait_warp(&full[st], (k / NS) & 1, &s_abort, kFzConsumerSleep);
         ok = consumers_all(okw && !s_abort);
         if (!ok) break;
         const int4 sl = slot_s[s];
-        run_stage<NG>(a, ring + (size_t)st * SB, L, n, sl.y, sl.z, perm_s, w_s, xq, xs136, hbuf[k & 1], y_s, warp,
-                      lane, ctid);
+        run_stage<TPW>(ring + (size_t)st * SB, nu, d, sl.y, sl.z, K, perm_s, w_s, xh, pgu, hb, C, warp, lane, ctid);
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[st]);
         ++k;
@@ -680,12 +653,21 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     if (!ok && ctid == 0) s_abort = 1;
 
     // ---- the partial output of this CTA, then the second grid barrier
-    consumers_sync();
     if (ok) {
-      float4* pp = reinterpret_cast<float4*>(a.part + (size_t)c * T * d);
-      const float4* ys = reinterpret_cast<const float4*>(y_s);
-      #pragma unroll 1
-      for (int i = ctid; i < T * QD; i += kFzWarps * 32) pp[i] = ys[i];
+      const int g = lane >> 2, t = lane & 3;
+      float* pc = a.part + (size_t)c * T * d;
+#pragma unroll
+      for (int i = 0; i < TPW; ++i) {
+        const int r0 = warp * (d / 16) + 16 * i + g;
+        if (2 * t < T) {
+          pc[(size_t)(2 * t) * d + r0] = C[i][0];
+          pc[(size_t)(2 * t) * d + r0 + 8] = C[i][2];
+        }
+        if (2 * t + 1 < T) {
+          pc[(size_t)(2 * t + 1) * d + r0] = C[i][1];
+          pc[(size_t)(2 * t + 1) * d + r0 + 8] = C[i][3];
+        }
+      }
     }
     consumers_sync();
     if (ctid == 0) {
@@ -742,31 +724,6 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   }
 }
 
-// ------------------------------------------------------------------ K-blocked copy of the down planes
-// out_q[e][b][r] = the 4 code bytes of columns 8b .. 8b+7 of row r (row-major [E][d][f/2] input);
-// out_s[e][g][r] = the scale of group g of row r.  A word keeps the input's nibble order.
-__global__ void repack_down_kernel(const uint8_t* dn_q, const __half* dn_s, int n_exp, int d, int f, uint32_t* out_q,
-                                   __half* out_s) {
-  const size_t fu = (size_t)f / kFzUnit, fg = (size_t)f / 32;
-  const size_t nq = (size_t)n_exp * fu * d, nsc = (size_t)n_exp * fg * d;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nq; i += stride) {
-    const size_t r = i % d, eb = i / d, b = eb % fu, e = eb / fu;
-    out_q[i] = *reinterpret_cast<const uint32_t*>(dn_q + (e * d + r) * (f / 2) + 4 * b);
-  }
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nsc; i += stride) {
-    const size_t r = i % d, eg = i / d, g = eg % fg, e = eg / fg;
-    out_s[i] = dn_s[(e * d + r) * fg + g];
-  }
-}
-
-cudaError_t repack_down_blocked(const void* dn_q, const void* dn_s, int n_exp, int d, int f, void* out_q, void* out_s,
-                                cudaStream_t st) {
-  repack_down_kernel<<<1024, 256, 0, st>>>(static_cast<const uint8_t*>(dn_q), static_cast<const __half*>(dn_s), n_exp,
-                                           d, f, static_cast<uint32_t*>(out_q), static_cast<__half*>(out_s));
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ self-test of the bounded waits
 // One CTA: thread 0 waits on an mbarrier nobody arrives at and on a barrier counter nobody bumps,
 // each with a small budget, exactly as the layer kernels wait.  Bit 0 of *result: the mbarrier
@@ -802,6 +759,82 @@ cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ decode layout from the row-major planes
+// gu_q [n][2f][d/2], gu_s [n][2f][d/32], dn_q [n][d][f/2], dn_s [n][d][f/32] (n experts) -> out:
+// n expert blocks of dl_expert_bytes, then n down-scale blocks of dl_scale_bytes.
+__global__ void dl_repack_kernel(const uint8_t* gu_q, const __half* gu_s, const uint8_t* dn_q, const __half* dn_s,
+                                 int n_exp, int d, int f, uint8_t* out) {
+  const int KT = d / 128, G = d / 32, fu = f / kFzUnit, TPW = d / 256;
+  const size_t ub = dl_unit_bytes(d), eb = dl_expert_bytes(d, f), gb = dl_gu_bytes(d);
+  const size_t stride = (size_t)gridDim.x * blockDim.x, i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // gate/up codes: (e, u, kt, lane, half, j)
+  const size_t n_gu = (size_t)n_exp * fu * KT * 256;
+  for (size_t i = i0; i < n_gu; i += stride) {
+    const int j = (int)(i & 3), h = (int)((i >> 2) & 1), lane = (int)((i >> 3) & 31);
+    size_t r = i >> 8;
+    const int kt = (int)(r % KT);
+    r /= KT;
+    const int u = (int)(r % fu), e = (int)(r / fu);
+    const int g = lane >> 2, t = lane & 3;
+    const size_t row = (size_t)e * 2 * f + (h ? f : 0) + 8 * u + g;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(gu_q + row * (d / 2) + (4 * kt + j) * 16 + 4 * t);
+    *reinterpret_cast<uint32_t*>(out + e * eb + u * ub + (size_t)kt * 1152 + lane * 32 + h * 16 + j * 4) =
+        w ^ 0x88888888u;
+  }
+  // gate/up scales: (e, u, kt, g, half, j)
+  const size_t n_gs = (size_t)n_exp * fu * KT * 64;
+  for (size_t i = i0; i < n_gs; i += stride) {
+    const int j = (int)(i & 3), h = (int)((i >> 2) & 1), g = (int)((i >> 3) & 7);
+    size_t r = i >> 6;
+    const int kt = (int)(r % KT);
+    r /= KT;
+    const int u = (int)(r % fu), e = (int)(r / fu);
+    const size_t row = (size_t)e * 2 * f + (h ? f : 0) + 8 * u + g;
+    *reinterpret_cast<__half*>(out + e * eb + u * ub + (size_t)kt * 1152 + 1024 + (g * 8 + h * 4 + j) * 2) =
+        gu_s[row * G + 4 * kt + j];
+  }
+  // down codes: (e, u, pair, lane)
+  const size_t n_dn = (size_t)n_exp * fu * (d / 32) * 32;
+  for (size_t i = i0; i < n_dn; i += stride) {
+    const int lane = (int)(i & 31);
+    size_t r = i >> 5;
+    const int p = (int)(r % (d / 32));
+    r /= (d / 32);
+    const int u = (int)(r % fu), e = (int)(r / fu);
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t w = 0;
+#pragma unroll
+    for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const size_t row = (size_t)e * d + 32 * p + 16 * tile + g + 8 * hr;
+          const int col = 8 * u + 2 * t + cc;
+          const uint8_t byte = dn_q[row * (f / 2) + col / 2];
+          const uint32_t o = (uint32_t)(((col & 1) ? (byte >> 4) : (byte & 15)) ^ 8);
+          w |= o << (4 * hr + 8 * tile + 16 * cc);
+        }
+    *reinterpret_cast<uint32_t*>(out + e * eb + u * ub + gb + ((size_t)p * 32 + lane) * 4) = w;
+  }
+  // down scales: (e, group, warp, g, tile, r)
+  __half* os = reinterpret_cast<__half*>(out + (size_t)n_exp * eb);
+  const size_t n_ds = (size_t)n_exp * (f / 32) * d;
+  for (size_t i = i0; i < n_ds; i += stride) {
+    const int rr = (int)(i & 1);
+    size_t r = i >> 1;
+    const int ti = (int)(r % TPW);
+    r /= TPW;
+    const int g = (int)(r & 7);
+    r >>= 3;
+    const int w = (int)(r & 15);
+    r >>= 4;
+    const int grp = (int)(r % (f / 32)), e = (int)(r / (f / 32));
+    const size_t row = (size_t)w * (d / 16) + 16 * ti + g + 8 * rr;
+    os[i] = dn_s[((size_t)e * d + row) * (f / 32) + grp];
+  }
+}
+
 // ------------------------------------------------------------------ host side
 constexpr int kFzStaticSlack = 8192;  // static shared memory of the kernel and the driver's share
 
@@ -815,9 +848,8 @@ static FusedPlan fused_plan(int T, int d, int f, int E, int K) {
   (void)f;
   (void)E;
   FusedPlan p{};
-  p.stage_bytes = (int)((stage_layout(d).bytes + 127u) & ~127u);
-  const size_t G = (size_t)d / 32;
-  const size_t fixed = up16((size_t)T * d * 4) + up16((size_t)T * G * 4) + up16((size_t)T * d * 4) +
+  p.stage_bytes = (int)((kFzStageUnits * dl_unit_bytes(d) + 2 * (size_t)d + 127) & ~size_t(127));
+  const size_t fixed = up16((size_t)T * d * 4) + up16((size_t)T * d * 2) + (size_t)kFzWarps * 32 * 16 +
                        up16((size_t)T * K * 16) + 3 * up16((size_t)T * K * 4);
   const long long room = (long long)kFzSmemMax - kFzStaticSlack - (long long)fixed;
   p.ns = room > 0 ? (int)std::min<long long>(kFzMaxStages, room / p.stage_bytes) : 0;
@@ -827,14 +859,23 @@ static FusedPlan fused_plan(int T, int d, int f, int E, int K) {
 
 static int g_fz_sms = 0;
 
-template <int NG>
+template <int TPW>
 static const void* fused_fn() {
-  return (const void*)decode_layer_kernel<NG>;
+  return (const void*)decode_layer_kernel<TPW>;
+}
+
+static const void* fused_fn_for(int d) {
+  switch (d / 256) {
+    case 2: return fused_fn<2>();
+    case 4: return fused_fn<4>();
+    case 6: return fused_fn<6>();
+    default: return fused_fn<8>();
+  }
 }
 
 cudaError_t fused_kernels_init(int num_sms) {
   g_fz_sms = num_sms;
-  const void* fns[3] = {fused_fn<1>(), fused_fn<2>(), fused_fn<4>()};
+  const void* fns[4] = {fused_fn<2>(), fused_fn<4>(), fused_fn<6>(), fused_fn<8>()};
   for (const void* fn : fns) {
     cudaError_t e =
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFzSmemMax - kFzStaticSlack);
@@ -847,7 +888,7 @@ cudaError_t fused_kernels_init(int num_sms) {
 bool fused_shape_ok(int T, int d, int f, int E, int K) {
   const int nc = g_fz_sms;
   if (nc <= 0 || nc > 32 * kFzReduceLoads || T < 1 || T > kFzMaxT) return false;
-  if (d % 256 || d > 4096 || f % 32 || f > 1024 || E > kMaxE || K > kMaxK) return false;
+  if (d % 512 || d > 2048 || f % 32 || f > 1024 || E > kMaxE || K > kMaxK) return false;
   if (f / kFzUnit > nc) return false;         // at most one shared-expert unit per CTA
   if (T * K > kFzWarps * 32) return false;    // dispatch: one thread per assignment
   const FusedPlan p = fused_plan(T, d, f, E, K);
@@ -856,11 +897,17 @@ bool fused_shape_ok(int T, int d, int f, int E, int K) {
   return (size_t)((E + nc - 1) / nc) * d * 4 <= (size_t)p.stage_bytes;
 }
 
-// Bytes of the K-blocked down copy of n_exp experts: codes, then scales (256-byte aligned parts).
-size_t fused_down_copy_bytes(int n_exp, int d, int f) {
-  const size_t q = ((size_t)n_exp * d * (f / 2) + 255) & ~size_t(255);
-  const size_t s = ((size_t)n_exp * d * (f / 16) + 255) & ~size_t(255);
-  return q + s;
+// Bytes of the decode-layout copy of n_exp experts (unit blocks, then down scales).
+size_t fused_layout_bytes(int n_exp, int d, int f) {
+  return (size_t)n_exp * (dl_expert_bytes(d, f) + dl_scale_bytes(d, f));
+}
+
+cudaError_t fused_repack(const void* gu_q, const void* gu_s, const void* dn_q, const void* dn_s, int n_exp, int d,
+                         int f, void* out, cudaStream_t st) {
+  dl_repack_kernel<<<2048, 256, 0, st>>>(static_cast<const uint8_t*>(gu_q), static_cast<const __half*>(gu_s),
+                                         static_cast<const uint8_t*>(dn_q), static_cast<const __half*>(dn_s), n_exp, d,
+                                         f, static_cast<uint8_t*>(out));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const FusedExtra& fx, cudaStream_t st) {
@@ -888,14 +935,10 @@ cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const F
   a.n_active = r.n_active;
   a.stat = r.stat;
   a.slots = r.slots;
-  a.gu_q = static_cast<const uint8_t*>(x.gu_q);
-  a.gu_s = x.gu_s;
-  a.dnb_q = static_cast<const uint32_t*>(fx.dnb_q);
-  a.dnb_s = static_cast<const __half*>(fx.dnb_s);
-  a.sh_gu_q = static_cast<const uint8_t*>(x.sh_gu_q);
-  a.sh_gu_s = x.sh_gu_s;
-  a.sh_dnb_q = static_cast<const uint32_t*>(fx.sh_dnb_q);
-  a.sh_dnb_s = static_cast<const __half*>(fx.sh_dnb_s);
+  a.dl = static_cast<const uint8_t*>(fx.dl);
+  a.dls = static_cast<const uint8_t*>(fx.dl) + (size_t)r.E * dl_expert_bytes(r.d, x.f);
+  a.sh_dl = static_cast<const uint8_t*>(fx.sh_dl);
+  a.sh_dls = fx.sh_dl ? static_cast<const uint8_t*>(fx.sh_dl) + dl_expert_bytes(r.d, x.f) : nullptr;
   a.part = fx.part;
   a.y = x.y;
   a.resid = x.resid;
@@ -904,8 +947,6 @@ cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const F
   const FusedPlan p = fused_plan(r.T, r.d, x.f, r.E, r.K);
   a.ns = p.ns;
   a.stage_bytes = p.stage_bytes;
-  const int G = r.d / 32;
-  const void* fn = G <= 32 ? fused_fn<1>() : G <= 64 ? fused_fn<2>() : fused_fn<4>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g_fz_sms);
   cfg.blockDim = dim3(kFzThreads);
@@ -921,7 +962,7 @@ cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const F
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[1] = {&a};
-  return cudaLaunchKernelExC(&cfg, fn, args);
+  return cudaLaunchKernelExC(&cfg, fused_fn_for(r.d), args);
 }
 
 }  // namespace moe

@@ -323,11 +323,13 @@ def test_one_launch_layer_matches_gemv_path_closely(decode_layer):
         capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)
         capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 4)
     a, b = out["one_launch"], out["gemv"]
-    # Both sum the same fp32 products in different orders, then round once to bf16: they may differ
-    # by the bf16 rounding of each (2 ulps, 2^-7 relative) plus fp32 reassociation error, which
-    # scales with the size of the summed terms (the layer's output scale), not with a result that
-    # happens to cancel to near zero: 2^-16 of max|y| covers it with room to spare.
-    tol = 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 2.0 ** -16 * b.abs().max()
+    # The GEMV path multiplies in fp32; the one-launch layer feeds its tensor cores fp16 operands
+    # (exact int4 codes and bf16 activations, but w * h rounded to an 11-bit significand) and
+    # accumulates in fp32.  Both round once to bf16 (2 ulps, 2^-7 relative).  The fp16 rounding of
+    # h adds up to 2^-11 relative per term of the down sum, so the difference scales with the size
+    # of the summed terms (the layer's output scale), not with an output that cancels to near zero:
+    # 2^-9 of max|y| bounds it with room to spare.
+    tol = 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 2.0 ** -9 * b.abs().max()
     assert torch.all((a - b).abs() <= tol)
 
 
