@@ -129,7 +129,8 @@ __device__ __forceinline__ bool consumers_all(bool v) {
 // complete when the counter reaches base + (i + 1) * gridDim.x.  Arrival is a release reduction
 // (no reply awaited); the wait polls with acquire loads.
 __device__ __forceinline__ void grid_arrive(unsigned long long* bar) {
-  __threadfence();
+  // release at GPU scope; cumulative, so it also orders the writes of the CTA's other threads that
+  // precede it through the CTA barrier the caller passed
   asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
 }
 __device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigned long long target,
@@ -218,8 +219,8 @@ __device__ __forceinline__ void gu_stage(const uint8_t* stg, int nu, int d, int 
   const size_t ub = dl_unit_bytes(d);
   const int items = nu * KT;
   if (warp >= items) return;
-  float c[4] = {0.f, 0.f, 0.f, 0.f};
   const int u = warp % nu;
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
   for (int i = warp; i < items; i += kFzWarps) {
     const int kt = i / nu;
@@ -231,20 +232,28 @@ __device__ __forceinline__ void gu_stage(const uint8_t* stg, int nu, int d, int 
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       xb[j] = xtok >= 0 ? xh[((size_t)xtok * G + 4 * kt + j) * 4 + t] : make_uint4(0u, 0u, 0u, 0u);
+    // the four groups' tiles first (independent), their scales after
+    float dg[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t w0 = j == 0 ? wg.x : j == 1 ? wg.y : j == 2 ? wg.z : wg.w;
       const uint32_t w1 = j == 0 ? wu.x : j == 1 ? wu.y : j == 2 ? wu.z : wu.w;
-      float dg[4] = {0.f, 0.f, 0.f, 0.f};
+      dg[j][0] = dg[j][1] = dg[j][2] = dg[j][3] = 0.f;
       // k-step 0: codes 0, 4 (K slots 2t, 2t+1) and 1, 5 (2t+8, 2t+9); k-step 1: codes 2, 6 and 3, 7
-      mma_16816(dg, q_lo(w0), q_lo(w1), q_hi(w0), q_hi(w1), xb[j].x, xb[j].y);
-      mma_16816(dg, q_lo(w0 >> 8), q_lo(w1 >> 8), q_hi(w0 >> 8), q_hi(w1 >> 8), xb[j].z, xb[j].w);
-      const uint32_t s01 = j < 2 ? sc.x : sc.y, s23 = j < 2 ? sc.z : sc.w;  // [half][j] fp16
-      const float sg = half_of(s01, j & 1), su = half_of(s23, j & 1);
-      c[0] = fmaf(sg, dg[0], c[0]);
-      c[1] = fmaf(sg, dg[1], c[1]);
-      c[2] = fmaf(su, dg[2], c[2]);
-      c[3] = fmaf(su, dg[3], c[3]);
+      mma_16816(dg[j], q_lo(w0), q_lo(w1), q_hi(w0), q_hi(w1), xb[j].x, xb[j].y);
+      mma_16816(dg[j], q_lo(w0 >> 8), q_lo(w1 >> 8), q_hi(w0 >> 8), q_hi(w1 >> 8), xb[j].z, xb[j].w);
+    }
+    const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&sc.x));  // [half][j] fp16
+    const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&sc.y));
+    const float2 u01 = __half22float2(*reinterpret_cast<const __half2*>(&sc.z));
+    const float2 u23 = __half22float2(*reinterpret_cast<const __half2*>(&sc.w));
+    const float sg[4] = {g01.x, g01.y, g23.x, g23.y}, su[4] = {u01.x, u01.y, u23.x, u23.y};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c[0] = fmaf(sg[j], dg[j][0], c[0]);
+      c[1] = fmaf(sg[j], dg[j][1], c[1]);
+      c[2] = fmaf(su[j], dg[j][2], c[2]);
+      c[3] = fmaf(su[j], dg[j][3], c[3]);
     }
   }
   pgu[warp * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
@@ -288,38 +297,41 @@ __device__ __forceinline__ void h_stage(int nu, int d, int pb, int nt, int K, co
 }
 
 // Down share of a stage for the warp's TPW row tiles (rows w d/16 + 16 i + g, + 8): D over the
-// stage's units (one scale group), then C += s D in fp32.
+// stage's (at most two) units, all loads first, then C += s D in fp32.
 template <int TPW>
 __device__ __forceinline__ void dn_stage(const uint8_t* stg, int nu, int d, const __half* hb, float (&C)[TPW][4],
-                                         int warp, int lane) {
+                                          int warp, int lane) {
   const size_t ub = dl_unit_bytes(d), gb = dl_gu_bytes(d);
   const int g = lane >> 2, t = lane & 3;
   float D[TPW][4];
 #pragma unroll
   for (int i = 0; i < TPW; ++i) D[i][0] = D[i][1] = D[i][2] = D[i][3] = 0.f;
-#pragma unroll 1
-  for (int u = 0; u < nu; ++u) {
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(hb + (u * 8 + g) * 8 + 2 * t);
+  uint32_t w[2][TPW / 2], b[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    b[u] = u < nu ? *reinterpret_cast<const uint32_t*>(hb + (u * 8 + g) * 8 + 2 * t) : 0u;
     const uint32_t* dw = reinterpret_cast<const uint32_t*>(stg + u * ub + gb) + (size_t)warp * (TPW / 2) * 32 + lane;
 #pragma unroll
-    for (int ip = 0; ip < TPW / 2; ++ip) {
-      const uint32_t w = dw[ip * 32];
-      mma_1688(D[2 * ip], q_lo(w), q_hi(w), b);
-      mma_1688(D[2 * ip + 1], q_lo(w >> 8), q_hi(w >> 8), b);
-    }
+    for (int ip = 0; ip < TPW / 2; ++ip) w[u][ip] = u < nu ? dw[ip * 32] : 0x88888888u;
   }
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int ip = 0; ip < TPW / 2; ++ip) {
+      mma_1688(D[2 * ip], q_lo(w[u][ip]), q_hi(w[u][ip]), b[u]);
+      mma_1688(D[2 * ip + 1], q_lo(w[u][ip] >> 8), q_hi(w[u][ip] >> 8), b[u]);
+    }
   const uint32_t* sp = reinterpret_cast<const uint32_t*>(stg + kFzStageUnits * ub) + ((size_t)warp * 8 + g) * TPW;
 #pragma unroll
   for (int i = 0; i < TPW; ++i) {
-    const uint32_t s = sp[i];  // rows g, g + 8 of tile i
-    const float s0 = half_of(s, 0), s1 = half_of(s, 1);
-    C[i][0] = fmaf(s0, D[i][0], C[i][0]);
-    C[i][1] = fmaf(s0, D[i][1], C[i][1]);
-    C[i][2] = fmaf(s1, D[i][2], C[i][2]);
-    C[i][3] = fmaf(s1, D[i][3], C[i][3]);
+    const uint32_t s = sp[i];
+    const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&s));
+    C[i][0] = fmaf(sf.x, D[i][0], C[i][0]);
+    C[i][1] = fmaf(sf.x, D[i][1], C[i][1]);
+    C[i][2] = fmaf(sf.y, D[i][2], C[i][2]);
+    C[i][3] = fmaf(sf.y, D[i][3], C[i][3]);
   }
 }
-
 // One stage: gate/up partials, h, down.  Uniform over the consumer threads (two consumers_sync).
 template <int TPW>
 __device__ __forceinline__ void run_stage(const uint8_t* stg, int nu, int d, int pb, int nt, int K, const int* perm_s,
@@ -370,7 +382,10 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   __shared__ int s_srt[kFzMaxT * kMaxK];
   __shared__ float inv_s[kFzMaxT];
   __shared__ volatile int s_abort;
-  __shared__ int s_nact, s_issued, s_ok;
+  __shared__ int s_nact, s_issued, s_ok, s_ncand;
+  __shared__ uint32_t s_wmax[kFzWarps], s_tau;
+  __shared__ float s_zp[kFzWarps], s_m;
+  __shared__ uint2 s_sel[kMaxK];
 
   // This launch may start while the previous kernel in the stream is still finishing
   // (programmatic dependent launch): everything before griddepcontrol.wait touches only this CTA's
@@ -552,16 +567,100 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
         keys[i] = e < E ? topk_order_key(__ldcg(a.logits + (size_t)t * E + e)) : 0u;
       }
       consumers_sync();
-      if (warp < T) {
-        int my_i;
-        float my_w;
-        topk_warp(keys + (size_t)warp * EP, E, K, my_i, my_w);
-        if (lane < K) {
-          idx_s[warp * K + lane] = my_i;
-          w_s[warp * K + lane] = my_w;
+      // then, token by token, all consumer threads at once: the K-th largest of the 16 warp maxima
+      // is a lower bound of the K-th largest key (the K largest warp maxima are K distinct keys), so
+      // the keys at or above it hold the selection; each candidate is ranked against the others
+      // (larger key, then lower expert) and rank k < K is the k-th choice.  Weights: exp(l - max)
+      // over Z (all E, summed per warp and then over the warps in order), renormalised over the K
+      // kept in ascending k.  (K > 16: every expert is a candidate.)
+      uint2* cand = reinterpret_cast<uint2*>(keys + (size_t)T * EP);  // [E] (key, expert)
+      if (T > 2) {
+        // several tokens: one warp per token instead (the same choices)
+        if (warp < T) {
+          int my_i;
+          float my_w;
+          topk_warp_fast(keys + (size_t)warp * EP, E, K, cand + (size_t)warp * 64, my_i, my_w);
+          if (lane < K) {
+            idx_s[warp * K + lane] = my_i;
+            w_s[warp * K + lane] = my_w;
+          }
         }
+        consumers_sync();
       }
-      consumers_sync();
+#pragma unroll 1
+      for (int t = 0; t < (T > 2 ? 0 : T); ++t) {
+        const uint32_t* kt = keys + (size_t)t * EP;
+        const int ea = ctid, eb = ctid + kFzWarps * 32;
+        const uint32_t k0 = ea < E ? kt[ea] : 0u, k1 = eb < E ? kt[eb] : 0u;
+        const uint32_t wm = __reduce_max_sync(0xffffffffu, max(k0, k1));
+        if (lane == 0) s_wmax[warp] = wm;
+        if (ctid == 0) s_ncand = 0;
+        consumers_sync();
+        if (warp == 0) {
+          const uint32_t v = lane < kFzWarps ? s_wmax[lane] : 0u;
+          int rk = 0;
+#pragma unroll
+          for (int l = 0; l < kFzWarps; ++l) {
+            const uint32_t o = __shfl_sync(0xffffffffu, v, l);
+            rk += (o > v) || (o == v && l < lane);
+          }
+          const uint32_t tau = K <= kFzWarps ? __reduce_max_sync(0xffffffffu, (lane < kFzWarps && rk == K - 1) ? v : 0u) : 0u;
+          const uint32_t mx = __reduce_max_sync(0xffffffffu, v);
+          if (lane == 0) {
+            s_tau = tau;
+            s_m = topk_key_value(mx);
+          }
+        }
+        consumers_sync();
+        const uint32_t tau = s_tau;
+        const float mlog = s_m;
+        float zp = 0.f;
+        if (k0 != 0u) zp += expf(topk_key_value(k0) - mlog);
+        if (k1 != 0u) zp += expf(topk_key_value(k1) - mlog);
+        zp = warp_sum(zp);
+        if (lane == 0) s_zp[warp] = zp;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t kk = h ? k1 : k0;
+          const bool is_c = kk != 0u && kk >= tau;
+          const unsigned bal = __ballot_sync(0xffffffffu, is_c);
+          int basep = 0;
+          if (lane == 0 && bal) basep = atomicAdd(&s_ncand, __popc(bal));
+          basep = __shfl_sync(0xffffffffu, basep, 0);
+          if (is_c) cand[basep + __popc(bal & ((1u << lane) - 1u))] = make_uint2(kk, (uint32_t)(h ? eb : ea));
+        }
+        consumers_sync();
+        const int ncd = s_ncand;
+#pragma unroll 1
+        for (int ci = ctid; ci < ncd; ci += kFzWarps * 32) {
+          const uint2 me = cand[ci];
+          int rank = 0;
+#pragma unroll 4
+          for (int q = 0; q < ncd; ++q) {
+            const uint2 o = cand[q];
+            rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+          }
+          if (rank < K) {
+            s_sel[rank] = me;
+          }
+        }
+        consumers_sync();
+        if (warp == 0) {
+          float z = 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < kFzWarps; ++w2) z += s_zp[w2];
+          const uint2 sel = lane < K ? s_sel[lane] : make_uint2(0u, 0u);
+          const float p = lane < K ? expf(topk_key_value(sel.x) - mlog) / z : 0.f;
+          float psum = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < K; ++k) psum += __shfl_sync(0xffffffffu, p, k);
+          if (lane < K) {
+            idx_s[t * K + lane] = (int)sel.y;
+            w_s[t * K + lane] = p / psum;
+          }
+        }
+        consumers_sync();
+      }
       if (c == 0)
         #pragma unroll 1
         for (int i = ctid; i < T * K; i += kFzWarps * 32) {
@@ -893,7 +992,9 @@ bool fused_shape_ok(int T, int d, int f, int E, int K) {
   if (T * K > kFzWarps * 32) return false;    // dispatch: one thread per assignment
   const FusedPlan p = fused_plan(T, d, f, E, K);
   if (p.ns < 2) return false;                 // the router rows and the shared stage use stages 0 and 1
-  if ((size_t)T * ((E + 31) & ~31) * 4 > (size_t)p.stage_bytes) return false;  // the selection's scratch
+  if ((size_t)T * ((E + 31) & ~31) * 4 + (size_t)std::max(E, T * 64) * 8 > (size_t)p.stage_bytes)
+    return false;  // the selection's scratch
+  if (E > 2 * kFzWarps * 32) return false;    // selection: two keys per consumer thread
   return (size_t)((E + nc - 1) / nc) * d * 4 <= (size_t)p.stage_bytes;
 }
 

@@ -165,6 +165,76 @@ __device__ __forceinline__ void topk_warp(uint32_t* s_key, int E, int K, int& my
   my_w = lane < K ? my_p / psum : 0.f;
 }
 
+// The same selection and weights in fewer dependent steps.  The K-th largest of the 32 lane maxima
+// is a lower bound of the K-th largest key (the K largest lane maxima are K distinct keys), so the
+// keys at or above it hold the selection; when there are at most 32 of them each lane ranks one
+// candidate against the others (larger key, then lower expert) and rank k < K is the k-th choice.
+// Otherwise (many equal or clustered logits) it falls back to the rounds of topk_warp.
+// s_cand: 64 uint2 of shared-memory scratch for this warp.
+__device__ __forceinline__ void topk_warp_fast(uint32_t* s_key, int E, int K, uint2* s_cand, int& my_i, float& my_w) {
+  const int lane = threadIdx.x & 31;
+  const int nj = (E + 31) >> 5;
+  uint32_t lm = 0u;
+#pragma unroll 4
+  for (int j = 0; j < nj; ++j) lm = max(lm, s_key[j * 32 + lane]);
+  int rk = 0;  // rank of this lane's maximum among the lane maxima, ties to the lower lane
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const uint32_t o = __shfl_sync(0xffffffffu, lm, l);
+    rk += (o > lm) || (o == lm && l < lane);
+  }
+  const uint32_t tau = __reduce_max_sync(0xffffffffu, rk == K - 1 ? lm : 0u);
+  int cnt = 0;
+#pragma unroll 4
+  for (int j = 0; j < nj; ++j) {
+    const uint32_t key = s_key[j * 32 + lane];
+    cnt += key != 0u && key >= tau;
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total > 32) {
+    topk_warp(s_key, E, K, my_i, my_w);
+    return;
+  }
+  const float m = topk_key_value(__reduce_max_sync(0xffffffffu, lm));
+  float z = 0.f;
+  int pos = incl - cnt;
+#pragma unroll 4
+  for (int j = 0; j < nj; ++j) {
+    const uint32_t key = s_key[j * 32 + lane];
+    if (key != 0u) z += expf(topk_key_value(key) - m);
+    if (key != 0u && key >= tau) s_cand[pos++] = make_uint2(key, (uint32_t)(lane + 32 * j));
+  }
+  z = warp_sum(z);
+  __syncwarp();
+  const uint2 cd = lane < total ? s_cand[lane] : make_uint2(0u, 0xffffffffu);
+  int rank = 0;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const uint32_t ok = __shfl_sync(0xffffffffu, cd.x, l), oi = __shfl_sync(0xffffffffu, cd.y, l);
+    rank += l < total && (ok > cd.x || (ok == cd.x && oi < cd.y));
+  }
+  if (lane < total && rank < K) s_cand[32 + rank] = cd;
+  __syncwarp();
+  uint32_t my_key = 0u;
+  my_i = 0;
+  if (lane < K) {
+    const uint2 sel = s_cand[32 + lane];
+    my_i = (int)sel.y;
+    my_key = sel.x;
+  }
+  const float my_p = lane < K ? expf(topk_key_value(my_key) - m) / z : 0.f;
+  float psum = 0.f;
+#pragma unroll 1
+  for (int k = 0; k < K; ++k) psum += __shfl_sync(0xffffffffu, my_p, k);
+  my_w = lane < K ? my_p / psum : 0.f;
+}
+
 }  // namespace moe
 
 namespace moe {
