@@ -18,7 +18,9 @@
  *   w[t,k] = p[idx[t,k]] / sum_k' p[idx[t,k']]                                (renormalised)
  *   FFN_e(x) = W_down,e ( silu(W_gate,e x) * (W_up,e x) ),  silu(z) = z / (1 + exp(-z))
  *   y[t] = sum_{k=0..K-1} w[t,k] FFN_{idx[t,k]}(x[t])  (+ FFN_shared(x[t]) with weight 1),
- *   summed in fp32 in ascending k with the shared expert last, rounded once to the output type.
+ *   summed in fp32 in a fixed order and rounded once to the output type (the GEMV and prefill
+ *   paths: ascending k, the shared expert last; the one-launch decode layer: the routing weights
+ *   are folded into the down operand and the per-SM partial outputs are summed in SM order).
  *
  * Conventions (all entry points):
  *   - Pointers are DEVICE pointers owned by the caller unless a parameter says "host".
@@ -27,8 +29,11 @@
  *     moe_get_device_status and the *_host entry points.
  *   - Arguments are validated before anything is launched; on error nothing is launched and an
  *     error status is returned.  Status codes are returned, never printed.
- *   - The library allocates device memory only in moe_create (workspace sized for max_tokens) and
- *     frees it only in moe_destroy.  Weights are never copied: moe_set_layer stores pointers.
+ *   - The library allocates device memory in moe_create (workspace sized for max_tokens) and, when
+ *     the one-launch decode layer serves the config (INT4, d % 512 == 0, d <= 2048, f % 32 == 0,
+ *     f <= 1024), in moe_set_layer: a per-layer copy of that layer's expert weights in the
+ *     one-launch layer's own fragment order (the same number of bytes as the layer's gate/up and
+ *     down planes and scales).  Everything is freed in moe_destroy.
  *   - A handle is not thread-safe, and calls made with one handle on different streams that
  *     overlap in time race on its workspace.
  *
@@ -103,9 +108,13 @@ typedef struct {
  * workspace cannot be allocated.  *out is set only on success. */
 moe_status moe_create(const moe_config* cfg, moe_handle* out);
 
-/* Register the weights of layer `layer` (0 <= layer < n_layers).  Stores the pointers only;
- * the memory must stay valid while the handle uses it.  Pointers are checked for NULL (scales
- * only for INT4, shared planes only with has_shared) and 16-byte alignment. */
+/* Register the weights of layer `layer` (0 <= layer < n_layers).  Stores the pointers (the memory
+ * must stay valid while the handle uses it) and, when the one-launch decode layer serves the
+ * config, writes the layer's expert copy in that layer's fragment order: the weights must hold
+ * their final values when this is called (it synchronises the device before reading them and
+ * the default stream after writing), and a layer whose weights change must be registered again.
+ * Pointers are checked for NULL (scales only for INT4, shared planes only with has_shared) and
+ * 16-byte alignment; MOE_ERR_OOM if the copy cannot be allocated. */
 moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w);
 
 /* Router + top-K + dispatch of one layer for T tokens (1 <= T <= max_tokens):
@@ -159,9 +168,11 @@ moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream);
 /* Options (each returns the value in effect, or a negative moe_status on error; changing one
  * drops the handle's captured stack graphs).
  * MOE_OPT_FUSED_MAX_TOKENS: calls with T <= value run the whole layer (router, selection,
- *   dispatch, experts, combine) as one cooperative kernel with grid-wide barriers (value 0..8,
- *   0 = off; default 4; INT4 weights with d % 256 == 0, f % 256 == 0, f <= 1024, d <= 4096; the
- *   value in effect is clamped to what the shared-memory plan of the shape allows).
+ *   dispatch, experts on tensor cores, combine) as one kernel of one CTA per SM with grid-wide
+ *   barriers (value 0..8, 0 = off; default 4; INT4 weights with d % 512 == 0, d <= 2048,
+ *   f % 32 == 0, f <= 1024; the value in effect is clamped to what the shared-memory plan of the
+ *   shape allows).  Its operands are fp16 (exact int4 codes and bf16 activations, w * h rounded
+ *   once), accumulated in fp32.
  * MOE_OPT_GEMV_MAX_TOKENS: other calls with T <= value run the split-K GEMV experts, larger T the
  *   tensor-core grouped GEMM (value 0..16; default 4; the grouped GEMM needs INT4 weights with
  *   d % 256 == 0 and f % 256 == 0, otherwise the value is clamped to 16). */
