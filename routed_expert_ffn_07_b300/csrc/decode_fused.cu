@@ -297,7 +297,7 @@ __device__ __forceinline__ void h_stage(int nu, int d, int pb, int nt, int K, co
 }
 
 // Down share of a stage for the warp's TPW row tiles (rows w d/16 + 16 i + g, + 8): D over the
-// stage's (at most two) units, all loads first, then C += s D in fp32.
+// stage's (at most two) units as one K = 16 tile, all loads first, then C += s D in fp32.
 template <int TPW>
 __device__ __forceinline__ void dn_stage(const uint8_t* stg, int nu, int d, const __half* hb, float (&C)[TPW][4],
                                           int warp, int lane) {
@@ -314,13 +314,14 @@ __device__ __forceinline__ void dn_stage(const uint8_t* stg, int nu, int d, cons
 #pragma unroll
     for (int ip = 0; ip < TPW / 2; ++ip) w[u][ip] = u < nu ? dw[ip * 32] : 0x88888888u;
   }
+  // one m16n8k16 per tile: K slots 0-7 are unit 0's columns, 8-15 unit 1's (codes -8 and h 0 when
+  // the stage has one unit)
 #pragma unroll
-  for (int u = 0; u < 2; ++u)
-#pragma unroll
-    for (int ip = 0; ip < TPW / 2; ++ip) {
-      mma_1688(D[2 * ip], q_lo(w[u][ip]), q_hi(w[u][ip]), b[u]);
-      mma_1688(D[2 * ip + 1], q_lo(w[u][ip] >> 8), q_hi(w[u][ip] >> 8), b[u]);
-    }
+  for (int ip = 0; ip < TPW / 2; ++ip) {
+    mma_16816(D[2 * ip], q_lo(w[0][ip]), q_hi(w[0][ip]), q_lo(w[1][ip]), q_hi(w[1][ip]), b[0], b[1]);
+    mma_16816(D[2 * ip + 1], q_lo(w[0][ip] >> 8), q_hi(w[0][ip] >> 8), q_lo(w[1][ip] >> 8), q_hi(w[1][ip] >> 8), b[0],
+              b[1]);
+  }
   const uint32_t* sp = reinterpret_cast<const uint32_t*>(stg + kFzStageUnits * ub) + ((size_t)warp * 8 + g) * TPW;
 #pragma unroll
   for (int i = 0; i < TPW; ++i) {
@@ -377,6 +378,9 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
   uint8_t* sh_stg = ring;
 
   __shared__ __align__(8) uint64_t full[kFzMaxStages], empty[kFzMaxStages], wr_full, sh_full, route_ready;
+  __shared__ __align__(8) uint64_t logits_done, bar1_done;
+  __shared__ unsigned long long s_bar_base;
+  __shared__ volatile int s_ok1;
   __shared__ __align__(16) __half hb[kFzStageUnits * 8 * 8];
   __shared__ float lpart[kFzWarps * kFzMaxT];
   __shared__ int s_srt[kFzMaxT * kMaxK];
@@ -399,6 +403,9 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     tc::mbar_init(&wr_full, 1);
     tc::mbar_init(&sh_full, 1);
     tc::mbar_init(&route_ready, 1);
+    tc::mbar_init(&logits_done, 1);
+    tc::mbar_init(&bar1_done, 1);
+    s_ok1 = 0;
     s_abort = 0;
     s_issued = 0;
     s_ok = 1;
@@ -414,7 +421,13 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
         tc::bulk_g2s(ring + SB, a.Wr + (size_t)e0 * d, (uint32_t)(ne * d * 4), &wr_full);
       }
       if (sh_on) issue_stage(sh_stg, a.sh_dl, a.sh_dls, su0, 1, d, &sh_full);
-      bool ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, kFzProducerSleep);
+      // the first grid barrier on the consumers' behalf: they go on with the shared expert while the
+      // release of their logits and the polling run here
+      const bool got = tc::mbar_wait_sleepy(&logits_done, 0, &s_abort, 32);
+      grid_arrive(a.grid_bar);  // always arrive: the other CTAs must not wait on this one
+      s_ok1 = (got && !s_abort && grid_wait(a.grid_bar, s_bar_base + nc, &s_abort)) ? 1 : 0;
+      tc::mbar_arrive(&bar1_done);
+      bool ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, 32);
       int k = 0;
       if (ok) {
         const long long U = (long long)s_nact * fu;
@@ -449,7 +462,10 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
     // the barrier counter's base: the previous launch's barriers are complete and fewer than
     // gridDim.x arrivals of this launch's first barrier can precede this read
     unsigned long long bar_base = 0;
-    if (ctid == 0) bar_base = ld_acquire_gpu(a.grid_bar) / nc * nc;
+    if (ctid == 0) {
+      bar_base = ld_acquire_gpu(a.grid_bar) / nc * nc;
+      s_bar_base = bar_base;  // published to the producer with the logits_done arrival
+    }
 
     // ---- phase 1: x (optionally RMS-normalised) in fp32 and as fp16 fragments, the logits
     if (a.prenorm) {
@@ -541,7 +557,7 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
           a.logits[(size_t)t * E + e0 + le] = v + (a.bias ? a.bias[e0 + le] : 0.f);
         }
       consumers_sync();
-      if (ctid == 0) grid_arrive(a.grid_bar);  // always arrive: the other CTAs must not wait on this one
+      if (ctid == 0) tc::mbar_arrive(&logits_done);  // the producer arrives at the grid barrier
     }
 
     // ---- the shared expert's unit of this CTA while the other CTAs finish their logits
@@ -550,9 +566,9 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       ok = consumers_all(ok && okw && !s_abort);
       if (ok) run_stage<TPW>(sh_stg, 1, d, -1, T, K, perm_s, w_s, xh, pgu, hb, C, warp, lane, ctid);
     }
-    if (ctid == 0) s_ok = (!s_abort && grid_wait(a.grid_bar, bar_base + nc, &s_abort)) ? 1 : 0;
+    const bool okb = tc::mbar_wait_warp(&bar1_done, 0, &s_abort, kFzConsumerSleep);
     consumers_sync();
-    ok = consumers_all(ok && s_ok && !s_abort);
+    ok = consumers_all(ok && okb && s_ok1 && !s_abort);
     if (!ok && ctid == 0) s_abort = 1;  // the producer stops waiting for the routing
 
     // ---- phase 2: selection (one warp per token) and dispatch, repeated by every CTA
@@ -670,66 +686,79 @@ __global__ void __launch_bounds__(kFzThreads, 1) decode_layer_kernel(const Fused
       {
         // dispatch by counting, one thread per assignment i (n <= 256): its place in the stable
         // counting sort is the number of smaller (expert, i) keys; the distinct experts below its
-        // own give its slot
+        // own give its slot.  One token: its K experts are distinct, so place = slot.
         const int n = T * K;
-        int e_i = 0, start = 0, cnt_i = 0, first = 0;
-        if (ctid < n) {
-          e_i = idx_s[ctid];
-          int pos = 0, before = 0;
-          #pragma unroll 1
-          for (int j = 0; j < n; ++j) {
-            const int ej = idx_s[j];
-            start += ej < e_i;
-            cnt_i += ej == e_i;
-            pos += ej < e_i || (ej == e_i && j < ctid);
-            before += ej == e_i && j < ctid;
+        if (T == 1) {
+          if (ctid < n) {
+            const int e_i = idx_s[ctid];
+            int pos = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) pos += idx_s[j] < e_i;
+            perm_s[pos] = ctid;
+            slot_s[pos] = make_int4(e_i, pos, 1, 0);
           }
-          perm_s[pos] = ctid;
-          first = before == 0;
-          s_srt[ctid] = first;
-        }
-        consumers_sync();
-        if (ctid < n && first) {
-          int slot = 0;
-          #pragma unroll 1
-          for (int j = 0; j < n; ++j) slot += s_srt[j] && idx_s[j] < e_i;
-          slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
-        }
-        if (ctid == 0) {
-          int na = 0;
-          #pragma unroll 1
-          for (int j = 0; j < n; ++j) na += s_srt[j];
-          s_nact = na;
-        }
-        consumers_sync();
-        if (c == 0) {
-          // the full outputs: offs[e] = assignments with an expert below e
-          const int na = s_nact;
-          #pragma unroll 1
-          for (int e = ctid; e <= E; e += kFzWarps * 32) {
-            int o = 0, ce = 0;
-            #pragma unroll 1
-            for (int q = 0; q < n; ++q) {
-              o += idx_s[q] < e;
-              ce += idx_s[q] == e;
+          if (ctid == 0) s_nact = n;
+          consumers_sync();
+        } else {
+          int e_i = 0, start = 0, cnt_i = 0, first = 0;
+          if (ctid < n) {
+            e_i = idx_s[ctid];
+            int pos = 0, before = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+              const int ej = idx_s[j];
+              start += ej < e_i;
+              cnt_i += ej == e_i;
+              pos += ej < e_i || (ej == e_i && j < ctid);
+              before += ej == e_i && j < ctid;
             }
-            a.offs[e] = o;
-            if (e < E) a.counts[e] = ce;
+            perm_s[pos] = ctid;
+            first = before == 0;
+            s_srt[ctid] = first;
           }
-          #pragma unroll 1
-          for (int q = ctid; q < na; q += kFzWarps * 32) {
-            a.active[q] = slot_s[q].x;
-            a.slots[q] = slot_s[q];
+          consumers_sync();
+          if (ctid < n && first) {
+            int slot = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) slot += s_srt[j] && idx_s[j] < e_i;
+            slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
           }
-          #pragma unroll 1
-          for (int q = ctid; q < n; q += kFzWarps * 32) a.perm[q] = perm_s[q];
           if (ctid == 0) {
-            *a.n_active = na;
-            if (a.stat) *a.stat = na;
+            int na = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) na += s_srt[j];
+            s_nact = na;
           }
+          consumers_sync();
         }
       }
       if (ctid == 0) tc::mbar_arrive(&route_ready);  // the producer may now stream routed experts
+      if (c == 0) {
+        // the full outputs: offs[e] = assignments with an expert below e
+        const int n = T * K, na = s_nact;
+#pragma unroll 1
+        for (int e = ctid; e <= E; e += kFzWarps * 32) {
+          int o = 0, ce = 0;
+#pragma unroll 4
+          for (int q = 0; q < n; ++q) {
+            o += idx_s[q] < e;
+            ce += idx_s[q] == e;
+          }
+          a.offs[e] = o;
+          if (e < E) a.counts[e] = ce;
+        }
+#pragma unroll 1
+        for (int q = ctid; q < na; q += kFzWarps * 32) {
+          a.active[q] = slot_s[q].x;
+          a.slots[q] = slot_s[q];
+        }
+#pragma unroll 1
+        for (int q = ctid; q < n; q += kFzWarps * 32) a.perm[q] = perm_s[q];
+        if (ctid == 0) {
+          *a.n_active = na;
+          if (a.stat) *a.stat = na;
+        }
+      }
     }
 
     // ---- phase 3: this CTA's routed units through the ring
