@@ -57,9 +57,9 @@ constexpr unsigned kFzConsumerSleep = 64;         // ns between polls of a waiti
 // offset binary o = q + 8).  Per expert, f/8 unit blocks of dl_unit_bytes(d) each, unit u =
 // columns 8u .. 8u+7:
 //   gate/up part, per k-tile kt < d/128 (128 columns of K), 1152 bytes:
-//     codes [lane 32][half 2][j 4] u32: lane = 4g + t; half 0 = gate row 8u + g, half 1 = up row
-//       f + 8u + g; the word = the 8 codes of columns 32 (4 kt + j) + 8t .. + 7 of that row
-//       (code i in bits 4i .. 4i + 3);
+//     codes [half 2][lane 32][j 4] u32 (a warp's 16-byte loads of one half are contiguous): lane =
+//       4g + t; half 0 = gate row 8u + g, half 1 = up row f + 8u + g; the word = the 8 codes of
+//       columns 32 (4 kt + j) + 8t .. + 7 of that row (code i in bits 4i .. 4i + 3);
 //     scales [g 8][half 2][j 4] fp16 at byte 1024: group 4 kt + j of those rows;
 //   down part, 4d bytes, [pair p < d/32][lane 32] u32: rows 32p .. 32p + 31 of the down matrix,
 //     columns 8u + 2t (bits 0-3, 4-7, 8-11, 12-15) and 8u + 2t + 1 (bits 16-19 .. 28-31) of rows
@@ -225,8 +225,8 @@ __device__ __forceinline__ void gu_stage(const uint8_t* stg, int nu, int d, int 
   for (int i = warp; i < items; i += kFzWarps) {
     const int kt = i / nu;
     const uint8_t* blk = stg + u * ub + (size_t)kt * 1152;
-    const uint4 wg = *reinterpret_cast<const uint4*>(blk + lane * 32);
-    const uint4 wu = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
+    const uint4 wg = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    const uint4 wu = *reinterpret_cast<const uint4*>(blk + 512 + lane * 16);
     const uint4 sc = *reinterpret_cast<const uint4*>(blk + 1024 + (lane >> 2) * 16);
     uint4 xb[4];
 #pragma unroll
@@ -906,7 +906,7 @@ __global__ void dl_repack_kernel(const uint8_t* gu_q, const __half* gu_s, const 
     const int g = lane >> 2, t = lane & 3;
     const size_t row = (size_t)e * 2 * f + (h ? f : 0) + 8 * u + g;
     const uint32_t w = *reinterpret_cast<const uint32_t*>(gu_q + row * (d / 2) + (4 * kt + j) * 16 + 4 * t);
-    *reinterpret_cast<uint32_t*>(out + e * eb + u * ub + (size_t)kt * 1152 + lane * 32 + h * 16 + j * 4) =
+    *reinterpret_cast<uint32_t*>(out + e * eb + u * ub + (size_t)kt * 1152 + h * 512 + lane * 16 + j * 4) =
         w ^ 0x88888888u;
   }
   // gate/up scales: (e, u, kt, g, half, j)
