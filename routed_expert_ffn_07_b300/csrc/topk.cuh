@@ -236,104 +236,3 @@ __device__ __forceinline__ void topk_warp_fast(uint32_t* s_key, int E, int K, ui
 }
 
 }  // namespace moe
-
-namespace moe {
-
-// Softmax + top-K of T tokens by NW cooperating warps (warp index `warp` in [0, NW)).  Tokens are
-// taken NW at a time; within a batch of nt tokens each gets WPT = NW / nt warps, and warp p of a
-// token holds the experts [p*E/WPT, (p+1)*E/WPT).  Order: larger logit, then lower expert index.
-// Weights: exp(l - max)/Z renormalised over the kept K (summed in ascending k; Z summed over the
-// warps in ascending order).  Results: out_idx/out_w [T][K] (shared memory).  `sync()` must
-// synchronise the NW warps.  Scratch: s_f [2*NW] floats, s_c [2*NW] u64.
-constexpr int kTopkLanes = 4;  // logits per lane: E <= 128 * (NW / tokens per batch)
-
-__device__ __forceinline__ uint64_t topk_key(float v, int e) {
-  const uint32_t u = __float_as_uint(v);
-  const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving, never 0
-  return ((uint64_t)key << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
-}
-__device__ __forceinline__ float topk_value(uint64_t k) {
-  const uint32_t key = (uint32_t)(k >> 32);
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-// Warp-wide maximum of a 64-bit key (0 = none).
-__device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
-  const uint32_t hi = (uint32_t)(k >> 32);
-  const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
-  const uint32_t lo = hi == mhi ? (uint32_t)k : 0u;
-  const uint32_t mlo = __reduce_max_sync(0xffffffffu, lo);
-  return ((uint64_t)mhi << 32) | mlo;
-}
-
-// K rounds of a block-wide arg-max (compact code: it runs once per launch, where instruction fetch
-// dominates).  Token t of a batch gets WPT = NW / nt warps; each lane holds at most 4 of the
-// token's logits (E <= 128 * WPT).  Round k: every warp takes the best untaken key of its lanes,
-// the token's warps publish theirs (double-buffered, one barrier per round), and every warp of
-// the token reads the WPT keys and knows the winner; its owner marks it taken.
-template <class Sync>
-__device__ void topk_group(const float* logits, int T, int E, int K, int NW, int warp, float* s_f, uint64_t* s_c,
-                           int* out_idx, float* out_w, Sync sync) {
-  const int lane = threadIdx.x & 31;
-  for (int t0 = 0; t0 < T; t0 += NW) {
-    const int nt = min(NW, T - t0), WPT = NW / nt;
-    const int tl = warp / WPT, p = warp - tl * WPT, t = t0 + tl;
-    const bool on = tl < nt;
-    const int eb = on ? (int)((long long)E * p / WPT) : 0, ee = on ? (int)((long long)E * (p + 1) / WPT) : 0;
-    float v[4];
-    uint64_t key[4];
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = eb + lane + 32 * j;
-      v[j] = e < ee ? __ldcg(logits + (size_t)t * E + e) : -INFINITY;
-      key[j] = e < ee ? topk_key(v[j], e) : 0ull;
-      m = fmaxf(m, v[j]);
-    }
-    m = warp_max(m);
-    if (lane == 0) s_f[warp] = m;
-    sync();
-    float tm = -INFINITY;
-    for (int q = 0; q < WPT; ++q) tm = fmaxf(tm, s_f[tl * WPT + q]);
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (key[j] != 0ull) z += expf(v[j] - tm);
-    z = warp_sum(z);
-    if (lane == 0) s_f[NW + warp] = z;
-    float my_p = 0.f;
-    int my_i = 0;
-#pragma unroll 1
-    for (int k = 0; k < K; ++k) {
-      uint64_t best = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) best = key[j] > best ? key[j] : best;
-      const uint64_t wk = warp_max_key(best);
-      uint64_t* buf = s_c + (k & 1) * NW;
-      if (lane == 0) buf[warp] = wk;
-      sync();
-      const uint64_t cand = (on && lane < WPT) ? buf[tl * WPT + lane] : 0ull;
-      const uint64_t win = warp_max_key(cand);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (key[j] == win) key[j] = 0ull;  // the owner drops it
-      if (lane == k) {
-        my_i = (int)(0xFFFFFFFFu - (uint32_t)win);
-        my_p = topk_value(win);  // the logit for now
-      }
-    }
-    if (on && p == 0) {
-      float Z = 0.f;
-      for (int q = 0; q < WPT; ++q) Z += s_f[NW + tl * WPT + q];
-      my_p = lane < K ? expf(my_p - tm) / Z : 0.f;
-      float psum = 0.f;
-      for (int k = 0; k < K; ++k) psum += __shfl_sync(0xffffffffu, my_p, k);
-      if (lane < K) {
-        out_idx[t * K + lane] = my_i;
-        out_w[t * K + lane] = my_p / psum;
-      }
-    }
-    sync();
-  }
-}
-
-}  // namespace moe
