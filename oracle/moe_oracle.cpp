@@ -97,7 +97,10 @@ void weight_row(int wfmt, const void* q, const void* s, int r, int cols, double*
   }
   const uint8_t* row = static_cast<const uint8_t*>(q) + static_cast<size_t>(r) * (cols / 2);
   const uint16_t* sc = static_cast<const uint16_t*>(s) + static_cast<size_t>(r) * (cols / 32);
-  for (int k = 0; k < cols; ++k) out[k] = int4_at(row, k) * f16_to_double(sc[k / 32]);
+  for (int g = 0; g < cols / 32; ++g) {
+    const double scale = f16_to_double(sc[g]);  // one scale per run of 32 columns
+    for (int k = 32 * g; k < 32 * g + 32; ++k) out[k] = int4_at(row, k) * scale;
+  }
 }
 
 double silu(double z) { return z / (1.0 + std::exp(-z)); }

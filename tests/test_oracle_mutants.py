@@ -17,7 +17,7 @@ MUTANTS = {
     "silu_sign": ("z / (1.0 + std::exp(-z))", "z / (1.0 + std::exp(z))"),
     "nibble_order": ("(k & 1) ? (b >> 4) : (b & 0xF)", "(k & 1) ? (b & 0xF) : (b >> 4)"),
     "offset_binary": ("n >= 8 ? n - 16 : n", "n - 8"),
-    "one_scale_per_row": ("sc[k / 32]", "sc[0]"),
+    "one_scale_per_row": ("f16_to_double(sc[g])", "f16_to_double(sc[0])"),
     "ties_to_higher_index": ("for (int e = 0; e < E; ++e) order[e] = e;", "for (int e = 0; e < E; ++e) order[e] = E - 1 - e;"),
     "no_renormalisation": ("for (int k = 0; k < K; ++k) w[k] = p[idx[k]] / kept;", "for (int k = 0; k < K; ++k) w[k] = p[idx[k]];"),
     "shared_dropped": ("for (int j = 0; j < d; ++j) yt[j] += o[j];", "for (int j = 0; j < d; ++j) yt[j] += 0.0 * o[j];"),
