@@ -127,7 +127,8 @@ moe_status moe_route(moe_handle h, int layer, const void* x, int T, int32_t* top
                      int32_t* expert_offs, int32_t* perm, void* stream);
 
 /* y = MoE_layer(x) for T tokens.  x, y: [T][d] of the configured act type; y must not overlap x.
- * T <= 16 runs the split-K GEMV path; larger T runs the grouped tensor-core path. */
+ * Which kernels run depends on T (see MOE_OPT_FUSED_MAX_TOKENS and MOE_OPT_GEMV_MAX_TOKENS): small T
+ * runs the one-launch decode layer, larger T the grouped tensor-core GEMM. */
 moe_status moe_layer_forward(moe_handle h, int layer, const void* x, int T, void* y, void* stream);
 
 /* All n_layers layers in order, in place: x <- x + MoE_l(N(x)) with N = RMSNorm (no weight,
@@ -138,6 +139,32 @@ moe_status moe_layer_forward(moe_handle h, int layer, const void* x, int T, void
  * layer input x_l and the normalised input N(x_l) (both in the act type); with a trace the
  * layers are launched directly instead of through the graph. */
 moe_status moe_stack_forward(moe_handle h, void* x_inout, int T, void* trace, void* stream);
+
+/* moe_stack_forward with launches made one by one (no graph) and, per layer l, a device copy of the
+ * routing the layer used: route_idx [L][T*K] int32, route_w [L][T*K] fp32, route_offs [L][E+1] int32,
+ * route_perm [L][T*K] int32 (each may be NULL), with the meaning of moe_route's outputs.  trace as in
+ * moe_stack_forward (may be NULL).  For checking a stack against a reference layer by layer. */
+moe_status moe_stack_forward_traced(moe_handle h, void* x_inout, int T, void* trace, int32_t* route_idx,
+                                    float* route_w, int32_t* route_offs, int32_t* route_perm, void* stream);
+
+/* Device copy (asynchronous on `stream`) of the routing that the most recent layer enqueued on the
+ * handle used -- by moe_layer_forward, moe_layer_forward_host, moe_route, or the last layer of
+ * moe_stack_forward -- as computed by whichever kernels served it: topk_idx [T*K], topk_w [T*K],
+ * expert_offs [E+1], perm [T*K], meanings as in moe_route (each may be NULL).  T must be the T of that
+ * call (MOE_ERR_INVALID_ARG otherwise).  Must be enqueued before the next call that routes. */
+moe_status moe_get_last_routing(moe_handle h, int T, int32_t* topk_idx, float* topk_w, int32_t* expert_offs,
+                                int32_t* perm, void* stream);
+
+/* Per-expert usage histogram ('Strata はなぜ少ない VRAM でも速いのか', section '粗から細へ：モデルを分ける
+ * 四つの方法': the engine ranks experts by how often they are used).  With on = 1, every forward pass
+ * (moe_layer_forward, moe_layer_forward_host, moe_stack_forward) adds, per layer l and expert e, the
+ * number of (token, slot) assignments routed to e; moe_route does not count.  The counters are
+ * uint64 [n_layers][E] inside the handle's workspace (zero at moe_create), added in the dispatch step
+ * of every path, so they are exact.  Toggling drops the handle's captured stack graphs.
+ * moe_usage_read copies them to counts_host (n_layers*E values), optionally zeroes them, and
+ * synchronises `stream`. */
+moe_status moe_usage_enable(moe_handle h, int on);
+moe_status moe_usage_read(moe_handle h, unsigned long long* counts_host, int reset, void* stream);
 
 /* End-to-end form of moe_layer_forward for HOST buffers: copies x_host to the device, runs the
  * layer, copies the result to y_host and synchronises `stream`.  x_host / y_host should be
@@ -176,8 +203,19 @@ moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream);
  * MOE_OPT_GEMV_MAX_TOKENS: other calls with T <= value run the split-K GEMV experts, larger T the
  *   tensor-core grouped GEMM (value 0..16; default 4; the grouped GEMM needs INT4 weights with
  *   d % 256 == 0 and f % 256 == 0, otherwise the value is clamped to 16). */
-enum { MOE_OPT_GEMV_MAX_TOKENS = 1, MOE_OPT_FUSED_MAX_TOKENS = 2 };
+enum { MOE_OPT_GEMV_MAX_TOKENS = 1, MOE_OPT_FUSED_MAX_TOKENS = 2, MOE_OPT_KERNEL_TIMELINE = 3 };
 int moe_set_option(moe_handle h, int option, int value);
+
+/* In-kernel timeline of the one-launch decode layer (tracing).  With MOE_OPT_KERNEL_TIMELINE = 1 every
+ * launch of that layer writes, per CTA and event, the GPU global timer (ns) at its phase boundaries
+ * (kernel entry, dependency wait passed, logits stored, grid barrier passed, routing done, first
+ * gate/up unit landed, gate/up done, first down item landed, down done, y written, and the producer's
+ * last gate/up issue, first and last down issue); each launch overwrites the previous one's stamps.
+ * moe_timeline_read copies the most recent stamps ([n_ctas][n_events] uint64, at most `capacity`
+ * values) to the host and synchronises `stream`; MOE_ERR_UNSUPPORTED when the config has no one-launch
+ * layer. */
+moe_status moe_timeline_read(moe_handle h, unsigned long long* stamps_host, int capacity, int* n_ctas, int* n_events,
+                             void* stream);
 
 /* Stage timing (tracing).  moe_timing_enable(h, n) creates 5*n CUDA events; afterwards every
  * layer enqueued by moe_layer_forward / moe_stack_forward (also inside a graph captured after
@@ -206,8 +244,10 @@ moe_status moe_timing_read(moe_handle h, float* ms, int max_records, int* n_reco
  * the process exits.  All calls on a device share it, so calls that overlap on the GPU (different
  * streams, or threads without ordering) race and give wrong results; the array keeps the last
  * call's contents.  The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  No cudaMalloc, cudaFree or
- * allocating library call is made. */
+ * device current); make that first call before any stream capture, and do not reset the device
+ * (cudaDeviceReset) between calls: the address is kept for the life of the process.  No cudaMalloc,
+ * cudaFree or allocating library call is made.  Its kernels make no device-side checks and never
+ * wait, so there is no device status to read back; MOE_ERR_CUDA sets moe_last_cuda_error. */
 moe_status moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int act, int T, int d,
                              int E, int K, int32_t* topk_idx, float* topk_w, int32_t* expert_offs, int32_t* perm,
                              void* stream);

@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe_b300.so")
-SOURCES = ["api.cu", "router.cu", "experts_gemv.cu", "experts_gemm.cu", "decode_fused.cu", "gen.cu"]
+SOURCES = ["api.cu", "router.cu", "experts_gemv.cu", "experts_gemm.cu", "decode_layer.cu", "gen.cu"]
 HEADERS = ["common.cuh", "tc_ptx.cuh", "topk.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -42,7 +42,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     procs = []
     for src in SOURCES:
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = [_nvcc(), *ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-dc" if False else "-c",
+        cmd = [_nvcc(), *ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-c",
                os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")

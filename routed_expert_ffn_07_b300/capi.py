@@ -20,6 +20,11 @@ MOE_W_F32, MOE_W_INT4_G32 = 0, 1
 SMALL_T = 16  # T <= SMALL_T can run the split-K GEMV path
 MOE_OPT_GEMV_MAX_TOKENS = 1
 MOE_OPT_FUSED_MAX_TOKENS = 2
+MOE_OPT_KERNEL_TIMELINE = 3
+TIMELINE_EVENTS = ("start", "dep_wait", "logits", "barrier", "routed", "first_unit", "units_done", "first_down",
+                   "down_done", "end", "last_unit_issued", "first_down_issued", "last_down_issued",
+                   "first_unit_issued", "clk_start", "clk_end", "x_staged", "router_rows", "keys", "selected",
+                   "dispatched", "producer_routed", "last_down_weights", "first_h")
 
 
 class MoeError(RuntimeError):
@@ -56,6 +61,10 @@ def _load():
         "moe_route": ([vp, ci, vp, ci, i32p, vp, i32p, i32p, vp], ci),
         "moe_layer_forward": ([vp, ci, vp, ci, vp, vp], ci),
         "moe_stack_forward": ([vp, vp, ci, vp, vp], ci),
+        "moe_stack_forward_traced": ([vp, vp, ci, vp, i32p, vp, i32p, i32p, vp], ci),
+        "moe_get_last_routing": ([vp, ci, i32p, vp, i32p, i32p, vp], ci),
+        "moe_usage_enable": ([vp, ci], ci),
+        "moe_usage_read": ([vp, vp, ci, vp], ci),
         "moe_layer_forward_host": ([vp, ci, vp, ci, vp, vp], ci),
         "moe_get_active_counts": ([vp, i32p, vp], ci),
         "moe_get_device_status": ([vp, vp], ci),
@@ -66,6 +75,7 @@ def _load():
         "moe_timing_enable": ([vp, ci], ci),
         "moe_timing_rewind": ([vp], ci),
         "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
+        "moe_timeline_read": ([vp, vp, ci, ctypes.POINTER(ci), ctypes.POINTER(ci), vp], ci),
         "moe_status_str": ([ci], ctypes.c_char_p),
         "moe_version": ([], ci),
         "moe_last_cuda_error": ([], ci),
@@ -146,6 +156,30 @@ def moe_stack_forward(h, x_inout, T, trace=None, stream=None):
     _check("moe_stack_forward", lib.moe_stack_forward(h, _ptr(x_inout), T, _ptr(trace), _stream(stream)))
 
 
+def moe_stack_forward_traced(h, x_inout, T, trace=None, route_idx=None, route_w=None, route_offs=None,
+                             route_perm=None, stream=None):
+    _check("moe_stack_forward_traced",
+           lib.moe_stack_forward_traced(h, _ptr(x_inout), T, _ptr(trace), _ptr(route_idx), _ptr(route_w),
+                                        _ptr(route_offs), _ptr(route_perm), _stream(stream)))
+
+
+def moe_get_last_routing(h, T, topk_idx=None, topk_w=None, expert_offs=None, perm=None, stream=None):
+    _check("moe_get_last_routing", lib.moe_get_last_routing(h, T, _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offs),
+                                                            _ptr(perm), _stream(stream)))
+
+
+def moe_usage_enable(h, on=True):
+    _check("moe_usage_enable", lib.moe_usage_enable(h, int(bool(on))))
+
+
+def moe_usage_read(h, n_layers, n_experts, reset=False, stream=None):
+    """The per-layer expert usage histogram as a uint64 array [n_layers, n_experts]."""
+    import numpy as np
+    out = np.zeros((n_layers, n_experts), dtype=np.uint64)
+    _check("moe_usage_read", lib.moe_usage_read(h, out.ctypes.data, int(bool(reset)), _stream(stream)))
+    return out
+
+
 def moe_layer_forward_host(h, layer, x_host, T, y_host, stream=None):
     _check("moe_layer_forward_host",
            lib.moe_layer_forward_host(h, layer, _ptr(x_host), T, _ptr(y_host), _stream(stream)))
@@ -193,6 +227,17 @@ def moe_timing_read(h, max_records, stream=None):
     n = ctypes.c_int(0)
     _check("moe_timing_read", lib.moe_timing_read(h, ms.ctypes.data, max_records, ctypes.byref(n), _stream(stream)))
     return ms[: n.value].copy()
+
+
+def moe_timeline_read(h, stream=None):
+    """The one-launch decode layer's most recent in-kernel timeline: uint64 [n_ctas, n_events] (ns)."""
+    import numpy as np
+    cap = 4096 * 16
+    out = np.zeros(cap, dtype=np.uint64)
+    nc, ne = ctypes.c_int(0), ctypes.c_int(0)
+    _check("moe_timeline_read", lib.moe_timeline_read(h, out.ctypes.data, cap, ctypes.byref(nc), ctypes.byref(ne),
+                                                      _stream(stream)))
+    return out[: nc.value * ne.value].reshape(nc.value, ne.value).copy()
 
 
 def moe_status_str(s):

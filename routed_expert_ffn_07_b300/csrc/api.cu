@@ -5,7 +5,9 @@
 // sits between layers ('Strata はなぜ少ない VRAM でも速いのか' (modeldock.net), section
 // '1 トークン、三者の分担').
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <vector>
 
@@ -20,14 +22,18 @@ cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, 
 size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K);
 size_t gemv_smem_dn(int T, int K, int E);
 cudaError_t gemm_kernels_init(int num_sms);
-cudaError_t fused_kernels_init(int num_sms);
+cudaError_t decode_kernels_init();
 cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
                                          cudaStream_t st);
-bool fused_shape_ok(int T, int d, int f, int E, int K);
-cudaError_t launch_decode_fused(const RouteArgs& r, const ExpertArgs& x, const FusedExtra& fx, cudaStream_t st);
-size_t fused_layout_bytes(int n_exp, int d, int f);
-cudaError_t fused_repack(const void* gu_q, const void* gu_s, const void* dn_q, const void* dn_s, int n_exp, int d,
-                         int f, void* out, cudaStream_t st);
+bool decode_shape_ok(int T, int d, int f, int E, int K, int nsm);
+size_t decode_maps_bytes();
+cudaError_t decode_build_maps(void* maps, int E, int d, int f, int nsm, int has_shared, const void* gu_q,
+                              const void* gu_s, const void* dn_q, const void* dn_s, const void* sh_gu_q,
+                              const void* sh_gu_s, const void* sh_dn_q, const void* sh_dn_s);
+cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const void* maps, __half* hw,
+                                unsigned* ready, unsigned long long* lgt, unsigned long long* launches, int nsm,
+                                unsigned long long* timeline, cudaStream_t st);
+int decode_timeline_events();
 size_t gemm_workspace_bytes(int max_tokens, int d, int f, int E, int K);
 bool gemm_shape_ok(int d, int f);
 void* gemm_maps_new();
@@ -41,8 +47,9 @@ cudaError_t gemm_build_act_maps(void* ws, int T, int d, int f, int E, int K, voi
 size_t gemm_act_maps_bytes();
 constexpr int kDispatchBlockHost = 256;
 constexpr int kTimingEvents = 5;  // before route, after route, after stage A, after stage B, end
-constexpr int kFusedMaxTokensHost = 8;    // the one-launch decode layer's limit
-constexpr int kFusedDefaultTokens = 4;    // decode and 1 + 3 verify
+constexpr int kFusedMaxTokensHost = 16;   // the one-launch decode layer's limit
+constexpr int kFusedDefaultTokens = 16;   // decode, 1 + 3 verify and small concurrent batches
+constexpr int kReadyCounters = 2 * 1024;  // the one-launch layer's per-slot counters (two launch parities)
 }  // namespace moe
 
 using namespace moe;
@@ -50,8 +57,8 @@ using namespace moe;
 struct LayerW {
   moe_layer_weights w;
   bool set = false;
-  void* maps = nullptr;  // TMA descriptors of the layer's planes (tensor-core path only)
-  void* dnb = nullptr;   // decode-layout copy of the experts (one-launch decode path only)
+  void* maps = nullptr;   // TMA descriptors of the layer's planes (grouped tensor-core path)
+  void* dmaps = nullptr;  // TMA descriptors of the same planes for the one-launch decode layer
 };
 
 struct moe_ctx {
@@ -88,9 +95,16 @@ struct moe_ctx {
   void* act_maps = nullptr;      // TMA descriptors of the workspace activation buffers
   int gemv_max_tokens = 4;       // T <= this runs the GEMV experts (when the grouped GEMM is available)
   int fused_max_tokens = 0;      // T <= this runs the one-launch decode layer (0: off)
-  unsigned long long* grid_bar = nullptr;  // grid-barrier counter of the one-launch decode layer
+  unsigned long long* lgt = nullptr;  // the one-launch decode layer's published logits [16][E] (epoch-tagged)
+  unsigned long long* launches = nullptr;  // and its launch counter (one per CTA per launch)
   bool fused_capable = false;    // the one-launch decode layer serves this config (T = 1 at least)
-  float* part = nullptr;         // its per-CTA partial outputs [#SM][min(max_tokens, 8)][d]
+  __half* hw = nullptr;          // its gate/up results [T + T*K][f] fp16 (T <= 16)
+  unsigned* ready = nullptr;     // its per-slot ready counters
+  unsigned long long* timeline = nullptr;  // its in-kernel timeline [#SM][events] (ns)
+  bool timeline_on = false;
+  unsigned long long* usage = nullptr;  // per-layer expert usage histogram [n_layers][E]
+  bool usage_on = false;         // forward passes add their per-expert counts to `usage`
+  int last_T = 0;                // T of the most recent routing enqueued on the handle
   // stage timing
   std::vector<cudaEvent_t> tev;
   int t_next = 0;
@@ -100,11 +114,11 @@ struct moe_ctx {
 static size_t act_size(int act) { return act == MOE_ACT_BF16 ? 2 : 4; }
 
 // Largest T <= want (and <= max_tokens) that the one-launch decode layer serves for this config.
-static int fused_limit(const moe_config& c, int want) {
+static int fused_limit(const moe_config& c, int nsm, int want) {
   int best = 0;
-  if (c.wfmt == MOE_W_INT4_G32)
+  if (c.wfmt == MOE_W_INT4_G32 && c.act == MOE_ACT_BF16)
     for (int t = 1; t <= want && t <= c.max_tokens; ++t)
-      if (fused_shape_ok(t, c.d, c.f, c.n_experts, c.top_k)) best = t;
+      if (decode_shape_ok(t, c.d, c.f, c.n_experts, c.top_k, nsm)) best = t;
   return best;
 }
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -120,6 +134,11 @@ static thread_local int g_last_cuda_error = 0;
       return MOE_ERR_CUDA;                           \
     }                                                \
   } while (0)
+
+namespace moe {
+// Lets the entry points defined in other files report the CUDA error behind their MOE_ERR_CUDA.
+void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+}  // namespace moe
 
 extern "C" {
 
@@ -179,43 +198,46 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   if (!h->gemm_ok) h->gemv_max_tokens = kSmallT;
   if (route_kernels_init() != cudaSuccess || gemv_kernels_init(h->num_sms) != cudaSuccess ||
       (h->gemm_ok && gemm_kernels_init(h->num_sms) != cudaSuccess) ||
-      (c.wfmt == MOE_W_INT4_G32 && fused_kernels_init(h->num_sms) != cudaSuccess)) {
+      (c.wfmt == MOE_W_INT4_G32 && decode_kernels_init() != cudaSuccess)) {
     delete h;
     return MOE_ERR_CUDA;
   }
-  h->fused_max_tokens = fused_limit(c, kFusedDefaultTokens);
-  h->fused_capable = fused_limit(c, 1) == 1;
+  h->fused_max_tokens = fused_limit(c, h->num_sms, kFusedDefaultTokens);
+  h->fused_capable = fused_limit(c, h->num_sms, 1) == 1;
 
   const int T = c.max_tokens, E = c.n_experts, K = c.top_k, d = c.d, f = c.f;
   const size_t as = act_size(c.act);
   h->nblocks_max = (T * K + kDispatchBlockHost - 1) / kDispatchBlockHost;
-  size_t sz[24];
-  int n = 0;
-  sz[n++] = up256((size_t)T * E * 4);                 // logits
-  sz[n++] = up256((size_t)T * K * 4);                 // idx
-  sz[n++] = up256((size_t)T * K * 4);                 // w
-  sz[n++] = up256((size_t)E * 4);                     // counts
-  sz[n++] = up256((size_t)(E + 1) * 4);               // offs
-  sz[n++] = up256((size_t)T * K * 4);                 // perm
-  sz[n++] = up256((size_t)E * 4);                     // active
-  sz[n++] = up256(4);                                 // n_active
-  sz[n++] = up256((size_t)c.n_layers * 4);            // stats
-  sz[n++] = up256((size_t)E * 16);                    // slot table
-  sz[n++] = up256(4);                                 // ticket
-  sz[n++] = up256(4);                                 // status
-  sz[n++] = up256(8);                                 // grid barrier
-  sz[n++] = up256((size_t)h->nblocks_max * E * 4);    // blockhist
+  std::vector<size_t> sz;
+  sz.push_back(up256((size_t)T * E * 4));                 // logits
+  sz.push_back(up256((size_t)T * K * 4));                 // idx
+  sz.push_back(up256((size_t)T * K * 4));                 // w
+  sz.push_back(up256((size_t)E * 4));                     // counts
+  sz.push_back(up256((size_t)(E + 1) * 4));               // offs
+  sz.push_back(up256((size_t)T * K * 4));                 // perm
+  sz.push_back(up256((size_t)E * 4));                     // active
+  sz.push_back(up256(4));                                 // n_active
+  sz.push_back(up256((size_t)c.n_layers * 4));            // stats
+  sz.push_back(up256((size_t)E * 16));                    // slot table
+  sz.push_back(up256(4));                                 // ticket
+  sz.push_back(up256(4));                                 // status
+  sz.push_back(up256(8));                                 // one-launch layer: launch counter
+  sz.push_back(up256((size_t)h->nblocks_max * E * 4));    // blockhist
   const int TS = T < kSmallT ? T : kSmallT;
-  sz[n++] = up256((size_t)(TS * K + TS) * f * 4);     // h (GEMV path)
-  sz[n++] = h->gemm_ok ? up256(gemm_workspace_bytes(T, d, f, E, K)) : 0;
-  sz[n++] = up256((size_t)T * d * as);                // xnorm
-  sz[n++] = up256((size_t)T * d * as);                // stack x
-  sz[n++] = up256((size_t)T * d * as);                // host x
-  sz[n++] = up256((size_t)T * d * as);                // host y
+  sz.push_back(up256((size_t)(TS * K + TS) * f * 4));     // h (GEMV path)
+  sz.push_back(h->gemm_ok ? up256(gemm_workspace_bytes(T, d, f, E, K)) : 0);
+  sz.push_back(up256((size_t)T * d * as));                // xnorm
+  sz.push_back(up256((size_t)T * d * as));                // stack x
+  sz.push_back(up256((size_t)T * d * as));                // host x
+  sz.push_back(up256((size_t)T * d * as));                // host y
   const int TF = T < kFusedMaxTokensHost ? T : kFusedMaxTokensHost;
-  sz[n++] = h->fused_capable ? up256((size_t)h->num_sms * TF * d * 4) : 0;  // one-launch partials
+  sz.push_back(h->fused_capable ? up256((size_t)(TF + TF * K) * f * 2) : 0);   // one-launch gate/up results
+  sz.push_back(h->fused_capable ? up256((size_t)kReadyCounters * 4) : 0);     // its per-slot counters
+  sz.push_back(h->fused_capable ? up256((size_t)kFusedMaxTokensHost * E * 8) : 0);  // its published logits
+  sz.push_back(h->fused_capable ? up256((size_t)h->num_sms * decode_timeline_events() * 8) : 0);  // its timeline
+  sz.push_back(up256((size_t)c.n_layers * E * 8));        // usage histogram
   size_t total = 0;
-  for (int i = 0; i < n; ++i) total += sz[i];
+  for (size_t v : sz) total += v;
   if (cudaMalloc(&h->slab, total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -236,7 +258,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   h->slots = reinterpret_cast<int4*>(p); p += sz[i++];
   h->ticket = reinterpret_cast<unsigned*>(p); p += sz[i++];
   h->status = reinterpret_cast<unsigned*>(p); p += sz[i++];
-  h->grid_bar = reinterpret_cast<unsigned long long*>(p); p += sz[i++];
+  h->launches = reinterpret_cast<unsigned long long*>(p); p += sz[i++];
   h->blockhist = reinterpret_cast<int32_t*>(p); p += sz[i++];
   h->h = reinterpret_cast<float*>(p); p += sz[i++];
   h->gemm_ws = sz[i] ? p : nullptr; p += sz[i++];
@@ -244,7 +266,11 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   h->stack_x = p; p += sz[i++];
   h->host_x = p; p += sz[i++];
   h->host_y = p; p += sz[i++];
-  h->part = sz[i] ? reinterpret_cast<float*>(p) : nullptr; p += sz[i++];
+  h->hw = sz[i] ? reinterpret_cast<__half*>(p) : nullptr; p += sz[i++];
+  h->ready = sz[i] ? reinterpret_cast<unsigned*>(p) : nullptr; p += sz[i++];
+  h->lgt = sz[i] ? reinterpret_cast<unsigned long long*>(p) : nullptr; p += sz[i++];
+  h->timeline = sz[i] ? reinterpret_cast<unsigned long long*>(p) : nullptr; p += sz[i++];
+  h->usage = reinterpret_cast<unsigned long long*>(p); p += sz[i++];
   if (cudaMemset(h->slab, 0, total) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->slab);
     delete h;
@@ -287,27 +313,14 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
     }
   }
   if (h->fused_capable) {
-    // the one-launch decode layer reads the experts in its own fragment order: copy them once, here
+    // the one-launch decode layer reads the same planes through its own TMA descriptors (host memory)
+    if (!L.dmaps) L.dmaps = aligned_alloc(64, (decode_maps_bytes() + 63) & ~size_t(63));
+    if (!L.dmaps) return MOE_ERR_OOM;
     const moe_config& c = h->cfg;
-    const size_t rb = (fused_layout_bytes(c.n_experts, c.d, c.f) + 255) & ~size_t(255);
-    const size_t sb = c.has_shared ? fused_layout_bytes(1, c.d, c.f) : 0;
-    if (!L.dnb && cudaMalloc(&L.dnb, rb + sb) != cudaSuccess) {
-      cudaGetLastError();
-      L.dnb = nullptr;
+    if (decode_build_maps(L.dmaps, c.n_experts, c.d, c.f, h->num_sms, c.has_shared, w->gu_q, w->gu_s, w->dn_q, w->dn_s,
+                          w->sh_gu_q, w->sh_gu_s, w->sh_dn_q, w->sh_dn_s) != cudaSuccess) {
       L.set = false;
-      return MOE_ERR_OOM;
-    }
-    char* base = static_cast<char*>(L.dnb);
-    // the weights may have been written on any stream: wait for the device before reading them
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) e = fused_repack(w->gu_q, w->gu_s, w->dn_q, w->dn_s, c.n_experts, c.d, c.f, base, nullptr);
-    if (e == cudaSuccess && c.has_shared)
-      e = fused_repack(w->sh_gu_q, w->sh_gu_s, w->sh_dn_q, w->sh_dn_s, 1, c.d, c.f, base + rb, nullptr);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
-    if (e != cudaSuccess) {
-      g_last_cuda_error = (int)e;
-      L.set = false;
-      return MOE_ERR_CUDA;
+      return MOE_ERR_INVALID_ARG;
     }
   }
   L.w = *w;
@@ -318,7 +331,8 @@ moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w) {
 }  // extern "C"
 
 // ------------------------------------------------------------------ internal launch sequences
-static RouteArgs make_route_args(moe_ctx* h, int layer, const void* x, int T, bool prenorm, int32_t* stat) {
+static RouteArgs make_route_args(moe_ctx* h, int layer, const void* x, int T, bool prenorm, int32_t* stat,
+                                 bool count_usage) {
   const moe_config& c = h->cfg;
   const moe_layer_weights& w = h->layers[layer].w;
   RouteArgs a;
@@ -346,6 +360,8 @@ static RouteArgs make_route_args(moe_ctx* h, int layer, const void* x, int T, bo
   a.blockhist = h->blockhist;
   a.ticket = h->ticket;
   a.status = h->status;
+  a.usage = (count_usage && h->usage_on) ? h->usage + (size_t)layer * c.n_experts : nullptr;
+  h->last_T = T;
   return a;
 }
 
@@ -394,19 +410,12 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
   }
   cudaError_t e;
   if (ev && (e = record_timing_event(ev[0], st)) != cudaSuccess) return e;
-  RouteArgs ra = make_route_args(h, layer, x, T, prenorm, h->stats + layer);
-  if (T <= h->fused_max_tokens && h->layers[layer].dnb) {
+  RouteArgs ra = make_route_args(h, layer, x, T, prenorm, h->stats + layer, true);
+  if (T <= h->fused_max_tokens && h->layers[layer].dmaps) {
     // one launch for the whole layer; its stages are not separated (all of it counts as "route")
     ExpertArgs ea = make_expert_args(h, layer, x, T, y, resid);
-    const moe_config& c = h->cfg;
-    char* base = static_cast<char*>(h->layers[layer].dnb);
-    const size_t rb = (fused_layout_bytes(c.n_experts, c.d, c.f) + 255) & ~size_t(255);
-    FusedExtra fx;
-    fx.dl = base;
-    fx.sh_dl = c.has_shared ? base + rb : nullptr;
-    fx.part = h->part;
-    fx.grid_bar = h->grid_bar;
-    e = launch_decode_fused(ra, ea, fx, st);
+    e = launch_decode_layer(ra, ea, h->layers[layer].dmaps, h->hw, h->ready, h->lgt, h->launches, h->num_sms,
+                            h->timeline_on ? h->timeline : nullptr, st);
     if (e != cudaSuccess) return e;
     for (int k = 1; ev && k < kTimingEvents; ++k)
       if ((e = record_timing_event(ev[k], st)) != cudaSuccess) return e;
@@ -445,7 +454,7 @@ moe_status moe_route(moe_handle h, int layer, const void* x, int T, int32_t* top
   if (s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   CUDA_TRY(cudaGetLastError());
-  RouteArgs ra = make_route_args(h, layer, x, T, false, h->stats + layer);
+  RouteArgs ra = make_route_args(h, layer, x, T, false, h->stats + layer, false);
   const int K = h->cfg.top_k, E = h->cfg.n_experts;
   const int nb = (T * K + kDispatchBlockHost - 1) / kDispatchBlockHost;
   CUDA_TRY(launch_route(ra, nb, st));
@@ -485,7 +494,26 @@ moe_status moe_layer_forward_host(moe_handle h, int layer, const void* x_host, i
 
 }  // extern "C"
 
-static cudaError_t enqueue_stack(moe_ctx* h, int T, void* trace, cudaStream_t st) {
+// Per-layer copies of the routing a traced stack used (each pointer may be null).
+struct RouteRecord {
+  int32_t* idx;   // [L][T*K]
+  float* w;       // [L][T*K]
+  int32_t* offs;  // [L][E+1]
+  int32_t* perm;  // [L][T*K]
+};
+
+static cudaError_t copy_routing(moe_ctx* h, int T, int32_t* idx, float* w, int32_t* offs, int32_t* perm,
+                                cudaStream_t st) {
+  const size_t nk = (size_t)T * h->cfg.top_k * 4, ne = (size_t)(h->cfg.n_experts + 1) * 4;
+  cudaError_t e = cudaSuccess;
+  if (idx && e == cudaSuccess) e = cudaMemcpyAsync(idx, h->idx, nk, cudaMemcpyDeviceToDevice, st);
+  if (w && e == cudaSuccess) e = cudaMemcpyAsync(w, h->w, nk, cudaMemcpyDeviceToDevice, st);
+  if (offs && e == cudaSuccess) e = cudaMemcpyAsync(offs, h->offs, ne, cudaMemcpyDeviceToDevice, st);
+  if (perm && e == cudaSuccess) e = cudaMemcpyAsync(perm, h->perm, nk, cudaMemcpyDeviceToDevice, st);
+  return e;
+}
+
+static cudaError_t enqueue_stack(moe_ctx* h, int T, void* trace, const RouteRecord* rr, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const size_t bytes = (size_t)T * c.d * act_size(c.act);
   for (int l = 0; l < c.n_layers; ++l) {
@@ -496,7 +524,12 @@ static cudaError_t enqueue_stack(moe_ctx* h, int T, void* trace, cudaStream_t st
     }
     cudaError_t e = enqueue_layer(h, l, h->stack_x, T, h->stack_x, h->stack_x, c.prenorm != 0, st);
     if (e != cudaSuccess) return e;
-    (void)0;
+    if (rr) {
+      const size_t nk = (size_t)l * T * c.top_k, ne = (size_t)l * (c.n_experts + 1);
+      e = copy_routing(h, T, rr->idx ? rr->idx + nk : nullptr, rr->w ? rr->w + nk : nullptr,
+                       rr->offs ? rr->offs + ne : nullptr, rr->perm ? rr->perm + nk : nullptr, st);
+      if (e != cudaSuccess) return e;
+    }
     if (trace) {
       // the normalised input of layer l (its expert input) was produced by the route step
       char* tl = static_cast<char*>(trace) + (size_t)l * 2 * bytes + bytes;
@@ -512,9 +545,8 @@ static cudaError_t enqueue_stack(moe_ctx* h, int T, void* trace, cudaStream_t st
   return cudaSuccess;
 }
 
-extern "C" {
-
-moe_status moe_stack_forward(moe_handle h, void* x_inout, int T, void* trace, void* stream) {
+static moe_status stack_forward(moe_handle h, void* x_inout, int T, void* trace, const RouteRecord* rr,
+                                void* stream) {
   if (!h || !x_inout || !aligned16(x_inout)) return MOE_ERR_INVALID_ARG;
   if (T < 1 || T > h->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (trace && !aligned16(trace)) return MOE_ERR_INVALID_ARG;
@@ -524,15 +556,15 @@ moe_status moe_stack_forward(moe_handle h, void* x_inout, int T, void* trace, vo
   const size_t bytes = (size_t)T * h->cfg.d * act_size(h->cfg.act);
   CUDA_TRY(cudaGetLastError());
   CUDA_TRY(cudaMemcpyAsync(h->stack_x, x_inout, bytes, cudaMemcpyDeviceToDevice, st));
-  if (trace) {
-    CUDA_TRY(enqueue_stack(h, T, trace, st));
+  if (trace || rr) {
+    CUDA_TRY(enqueue_stack(h, T, trace, rr, st));
   } else {
     auto it = h->graphs.find(T);
     if (it == h->graphs.end()) {
       if (!h->cap_stream) CUDA_TRY(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
       cudaGraph_t g = nullptr;
       CUDA_TRY(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
-      cudaError_t e = enqueue_stack(h, T, nullptr, h->cap_stream);
+      cudaError_t e = enqueue_stack(h, T, nullptr, nullptr, h->cap_stream);
       cudaError_t e2 = cudaStreamEndCapture(h->cap_stream, &g);
       if (e != cudaSuccess || e2 != cudaSuccess) {
         if (g) cudaGraphDestroy(g);
@@ -547,6 +579,46 @@ moe_status moe_stack_forward(moe_handle h, void* x_inout, int T, void* trace, vo
     CUDA_TRY(cudaGraphLaunch(it->second, st));
   }
   CUDA_TRY(cudaMemcpyAsync(x_inout, h->stack_x, bytes, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+extern "C" {
+
+moe_status moe_stack_forward(moe_handle h, void* x_inout, int T, void* trace, void* stream) {
+  return stack_forward(h, x_inout, T, trace, nullptr, stream);
+}
+
+moe_status moe_stack_forward_traced(moe_handle h, void* x_inout, int T, void* trace, int32_t* route_idx,
+                                    float* route_w, int32_t* route_offs, int32_t* route_perm, void* stream) {
+  RouteRecord rr{route_idx, route_w, route_offs, route_perm};
+  const bool any = route_idx || route_w || route_offs || route_perm;
+  return stack_forward(h, x_inout, T, trace, any ? &rr : nullptr, stream);
+}
+
+moe_status moe_get_last_routing(moe_handle h, int T, int32_t* topk_idx, float* topk_w, int32_t* expert_offs,
+                                int32_t* perm, void* stream) {
+  if (!h || T < 1 || T != h->last_T) return MOE_ERR_INVALID_ARG;
+  CUDA_TRY(copy_routing(h, T, topk_idx, topk_w, expert_offs, perm, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_usage_enable(moe_handle h, int on) {
+  if (!h || (on != 0 && on != 1)) return MOE_ERR_INVALID_ARG;
+  if (h->usage_on != (on != 0)) {
+    h->usage_on = on != 0;
+    for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);  // the graphs hold the old kernel arguments
+    h->graphs.clear();
+  }
+  return MOE_OK;
+}
+
+moe_status moe_usage_read(moe_handle h, unsigned long long* counts_host, int reset, void* stream) {
+  if (!h || !counts_host || (reset != 0 && reset != 1)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)h->cfg.n_layers * h->cfg.n_experts * 8;
+  CUDA_TRY(cudaMemcpyAsync(counts_host, h->usage, bytes, cudaMemcpyDeviceToHost, st));
+  if (reset) CUDA_TRY(cudaMemsetAsync(h->usage, 0, bytes, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
   return MOE_OK;
 }
 
@@ -567,8 +639,11 @@ moe_status moe_get_device_status(moe_handle h, void* stream) {
   CUDA_TRY(cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
   if (v) CUDA_TRY(cudaMemset(h->status, 0, 4));
   if (v & kStatusTimeout) {
-    // a grid barrier that gave up may hold a partial count: start the next launch from zero
-    CUDA_TRY(cudaMemset(h->grid_bar, 0, 8));
+    // the one-launch layer's per-slot counters may hold partial sums and its published logits a
+    // stale epoch: start the next launch from zero
+    CUDA_TRY(cudaMemset(h->launches, 0, 8));
+    if (h->ready) CUDA_TRY(cudaMemset(h->ready, 0, (size_t)kReadyCounters * 4));
+    if (h->lgt) CUDA_TRY(cudaMemset(h->lgt, 0, (size_t)kFusedMaxTokensHost * h->cfg.n_experts * 8));
     return MOE_ERR_TIMEOUT;
   }
   if (v) return MOE_ERR_DEVICE;
@@ -613,9 +688,17 @@ int moe_set_option(moe_handle h, int option, int value) {
     h->graphs.clear();
     return h->gemv_max_tokens;
   }
+  if (option == MOE_OPT_KERNEL_TIMELINE) {
+    if (value != 0 && value != 1) return -(int)MOE_ERR_INVALID_ARG;
+    if (!h->timeline) return value ? -(int)MOE_ERR_UNSUPPORTED : 0;
+    h->timeline_on = value != 0;
+    for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+    h->graphs.clear();
+    return value;
+  }
   if (option == MOE_OPT_FUSED_MAX_TOKENS) {
     if (value < 0 || value > kFusedMaxTokensHost) return -(int)MOE_ERR_INVALID_ARG;
-    h->fused_max_tokens = fused_limit(h->cfg, value);
+    h->fused_max_tokens = fused_limit(h->cfg, h->num_sms, value);
     for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
     h->graphs.clear();
     return h->fused_max_tokens;
@@ -655,13 +738,27 @@ moe_status moe_timing_read(moe_handle h, float* ms, int max_records, int* n_reco
   return MOE_OK;
 }
 
+moe_status moe_timeline_read(moe_handle h, unsigned long long* stamps_host, int capacity, int* n_ctas, int* n_events,
+                             void* stream) {
+  if (!h || !n_ctas || !n_events || (capacity > 0 && !stamps_host)) return MOE_ERR_INVALID_ARG;
+  if (!h->timeline) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ev = decode_timeline_events();
+  const size_t n = std::min((size_t)capacity, (size_t)h->num_sms * ev);
+  if (n) CUDA_TRY(cudaMemcpyAsync(stamps_host, h->timeline, n * 8, cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  *n_ctas = h->num_sms;
+  *n_events = ev;
+  return MOE_OK;
+}
+
 moe_status moe_destroy(moe_handle h) {
   if (!h) return MOE_ERR_INVALID_ARG;
   cudaError_t e = cudaDeviceSynchronize();
   for (cudaEvent_t ev : h->tev) cudaEventDestroy(ev);
   for (LayerW& L : h->layers) {
     if (L.maps) gemm_maps_free(L.maps);
-    if (L.dnb) cudaFree(L.dnb);
+    if (L.dmaps) free(L.dmaps);
   }
   if (h->act_maps) gemm_maps_free(h->act_maps);
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);

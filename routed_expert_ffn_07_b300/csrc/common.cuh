@@ -149,6 +149,7 @@ struct RouteArgs {
   int32_t* blockhist;// [nblocks][E] (large-T dispatch)
   unsigned* ticket;  // last-block-done counter (zero between launches)
   unsigned* status;  // device status word
+  unsigned long long* usage;  // [E] or null: count[e] of this routing is added (usage histogram)
 };
 
 struct ExpertArgs {
@@ -173,14 +174,6 @@ struct ExpertArgs {
   void* y;                // [T][d]
   const void* resid;      // [T][d] or null: y = resid + moe
   unsigned* status;
-};
-
-// Extra arguments of the one-launch decode layer.
-struct FusedExtra {
-  const void* dl;        // the routed experts' decode-layout copy (unit blocks, then down scales)
-  const void* sh_dl;     // the shared expert's, or null
-  float* part;           // [#SM][T][d] per-CTA partial outputs
-  unsigned long long* grid_bar;
 };
 
 }  // namespace moe

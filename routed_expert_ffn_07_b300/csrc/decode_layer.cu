@@ -1,0 +1,1413 @@
+// Decode / verify layer in one launch (sm_103a): router logits, softmax + top-K, dispatch, the
+// gate/up and down projections of the selected and shared experts on tensor cores, and the
+// fixed-order combine, reading the experts' row-major int4 planes directly.
+//
+// A decode step streams the bytes of the experts its few tokens chose and little else
+// ('Strata はなぜ少ない VRAM でも速いのか' (modeldock.net), section '1 トークン、三者の分担';
+// verifying 1 + 3 drafted tokens adds only the experts the drafts pick, section
+// '予測してから検証する').  With every expert in HBM what remains besides those bytes is the chain
+// router -> selection -> experts -> combine, so it runs in one kernel of one CTA per SM:
+//
+//   prologue  (may overlap the previous kernel) the CTA's router rows and, when the CTA's first
+//             gate/up unit belongs to the shared expert, that unit start streaming in;
+//   phase 1   x (optionally RMS-normalised) becomes fp16 tensor-core fragments in shared memory;
+//             the CTA scores its E / #CTA experts for all T tokens and stores the logits;
+//             [grid barrier]
+//   phase 2   every CTA reads all logits and repeats the selection and the dispatch (identical,
+//             deterministic); CTA 0 publishes them;
+//   phase 3   gate/up.  The slots (the shared expert first, then the distinct routed experts in
+//             ascending order) are cut into units of 8 columns of f; unit g goes to CTA g mod
+//             #CTA.  A unit (8 gate + 8 up rows x d) arrives as one 128-byte-swizzled TMA box plus
+//             its scales; a team of 4 warps runs it as m16n8k16 tensor-core tiles (N = the slot's
+//             tokens), sums its 4 warps' partial tiles in a fixed order, and writes
+//             h = w silu(gate) up (fp16, routing weight folded in) for its 8 columns to global
+//             memory, then bumps the slot's ready counter (release);
+//   phase 4   down.  CTA c owns output rows [d c / #CTA, d (c + 1) / #CTA).  For every slot in
+//             order the producer waits until the slot's counter shows all its units done
+//             (acquire), then streams the slot's down rows of those outputs (TMA) and the slot's
+//             h rows (bulk copy); all 16 warps multiply them (N = all T tokens; a token that does
+//             not use the slot contributes zeros) into fp32 accumulators kept in registers across
+//             the slots.  The 16 warps' partial sums are added in warp order and the residual is
+//             added: y is written once, each element by one CTA.
+//
+// Tensor-core operands: int4 codes become fp16 q exactly, x is fp16 (bf16 activations are exact in
+// fp16 inside its range) and w * h is rounded once to fp16; every 32-code group is summed in fp32
+// and scaled by its fp16 group scale in fp32.  Every wait is bounded; on timeout the CTA records
+// MOE status "timeout", writes NaN to its rows of y, stops issuing, and waits (bounded) for its
+// copies in flight before exiting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "topk.cuh"
+
+namespace moe {
+
+constexpr int kDlWarps = 16;                     // consumer warps
+constexpr int kDlThreads = (kDlWarps + 2) * 32;  // + one producer warp + one flagger warp
+constexpr int kDlTeams = 4;                      // gate/up teams
+constexpr int kDlTeamWarps = kDlWarps / kDlTeams;
+constexpr int kDlMaxT = 16;                      // tokens: two n8 tiles
+constexpr int kDlMaxStages = 16;
+constexpr int kDlSmemMax = 227 * 1024;
+constexpr int kDlStaticSlack = 12 * 1024;        // static shared memory, alignment and reserve
+constexpr int kDlRowsMax = 16;                   // down rows per CTA: one m16 tile
+constexpr int kDlUnit = 8;                       // f columns per gate/up unit
+constexpr unsigned kDlSpinLimit = 1u << 24;      // grid-barrier / ready-counter polls, >= 32 ns apart
+constexpr unsigned kDlProducerSleep = 128;       // ns between polls of the producer's waits
+constexpr unsigned kDlConsumerSleep = 32;        // ns between polls of a waiting consumer warp
+constexpr int kDlReadyStride = 1024;             // per-slot ready counters per launch parity
+constexpr int kDlXPad = 4;                       // 16-byte blocks of padding per row of x fragments
+
+// TMA descriptors of one layer (routed planes, then the shared expert's).
+//   gu_q: 4-d view of the [rows][d/2] gate/up codes: (128 bytes, row, 128-byte chunk of the row,
+//         gate|up), box (128, 8, d/256, 2) = one unit (8 gate rows + the matching 8 up rows), laid
+//         out in shared memory as [gate|up][chunk][row][128 B] with the 128-byte swizzle;
+//   gu_s: (d/32 scales, row, gate|up), box (d/32, 8, 2), unswizzled [gate|up][row][d/32];
+//   dn_q: the down codes of `rows_box` consecutive rows: (128 bytes, row, chunk) box
+//         (128, rows_box, f/256) -> [chunk][row][128 B] when dn_swap, else (128 bytes, chunk, row)
+//         -> [row][chunk][128 B]; 128-byte swizzle either way;
+//   dn_s: (f/32 scales, row), box (f/32, rows_box).
+struct DlMaps {
+  CUtensorMap gu_q, gu_s, dn_q, dn_s;
+  CUtensorMap sh_gu_q, sh_gu_s, sh_dn_q, sh_dn_s;
+};
+
+struct DlArgs {
+  const void* x;
+  int act, T, d, E, K, f, has_shared, prenorm;
+  float eps;
+  void* xnorm;
+  const float* Wr;
+  const float* bias;
+  float* logits;
+  int32_t* idx;
+  float* w;
+  int32_t* counts;
+  int32_t* offs;
+  int32_t* perm;
+  int32_t* active;
+  int32_t* n_active;
+  int32_t* stat;
+  int4* slots;
+  unsigned long long* usage;
+  __half* hw;                    // [T (shared) + T*K][f]: w silu(g) u, fp16, 8-column blocks in fragment order
+  unsigned* ready;               // [2][kDlReadyStride] per-slot unit counters, one array per launch parity
+  void* y;
+  const void* resid;
+  unsigned long long* lgt;       // [T][E] published logits: (launch epoch << 32) | order-preserving key
+  unsigned long long* launches;  // every CTA of every launch adds 1 when it ends
+  unsigned* status;
+  int ns;                        // ring stages
+  int stage_bytes;
+  int rows_box;                  // down rows per TMA box (>= the rows of any CTA)
+  int dn_swap;                   // down box layout, see DlMaps
+  unsigned long long* timeline;  // [#CTA][kDlEvents] globaltimer stamps (ns), or null
+};
+
+// In-kernel timeline (tracing): one globaltimer stamp per CTA and event when enabled.
+enum DlEvent {
+  kEvStart = 0,        // kernel entered
+  kEvDepWait,          // griddepcontrol.wait passed
+  kEvLogits,           // logits stored
+  kEvBarrier,          // grid barrier passed (consumers learn it)
+  kEvRouted,           // selection and dispatch done
+  kEvFirstUnit,        // first gate/up unit's bytes landed (team 0)
+  kEvUnitsDone,        // all of the CTA's gate/up units done
+  kEvFirstDown,        // first down item's bytes landed
+  kEvDownDone,         // all down items done
+  kEvEnd,              // y written
+  kEvLastUnitIssued,   // producer: last gate/up unit issued
+  kEvFirstDownIssued,  // producer: first down item issued
+  kEvLastDownIssued,   // producer: last down item issued
+  kEvFirstUnitIssued,  // producer: first gate/up unit issued after the routing
+  kClkStart = 14,      // SM clock (clock64) at kernel entry
+  kClkEnd = 15,        // SM clock when y is written
+  kEvXStaged,          // x staged as fragments
+  kEvRouterRows,       // router rows landed
+  kEvKeys,             // selection keys loaded
+  kEvSelected,         // top-K chosen
+  kEvDispatched,       // dispatch done
+  kEvProducerRouted,   // producer learned the routing
+  kEvLastDownWeights,  // producer: last down weights issued
+  kEvFirstH,           // producer: first h rows issued
+  kDlEvents = 32
+};
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define DL_STAMP(ev) \
+  do { \
+    if (a.timeline) a.timeline[(size_t)blockIdx.x * kDlEvents + (ev)] = gtimer(); \
+  } while (0)
+#define DL_CLOCK(ev) \
+  do { \
+    if (a.timeline) a.timeline[(size_t)blockIdx.x * kDlEvents + (ev)] = (unsigned long long)clock64(); \
+  } while (0)
+
+// ------------------------------------------------------------------ grid barrier and counters
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_u32(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Grid barrier on a 64-bit arrival counter that only ever increases.  At the start (after
+// griddepcontrol.wait) one thread per CTA reads the counter and rounds it down to a multiple of
+// gridDim.x: the previous launch's barrier is complete and fewer than gridDim.x arrivals of this
+// launch can precede the read, so every CTA gets the same base; the barrier is complete when the
+// counter reaches base + gridDim.x.  Arrival is a release reduction, the wait polls with acquire
+// loads (cumulative: the writes the CTA's other threads made before the CTA barrier that precedes
+// the arrival are released too).
+__device__ __forceinline__ void red_relaxed_gpu_u32(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_release_cta(unsigned* p, unsigned v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(tc::smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(tc::smem_u32(p)) : "memory");
+  return v;
+}
+
+// Named barriers: 1 = the 512 consumer threads, 2 + team = the 128 threads of a gate/up team.
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDlWarps * 32) : "memory"); }
+__device__ __forceinline__ bool consumers_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kDlWarps * 32)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void team_sync(int team) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + team), "n"(kDlTeamWarps * 32) : "memory");
+}
+__device__ __forceinline__ bool team_all(int team, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(2 + team), "n"(kDlTeamWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------------ tensor-core helpers
+// D += A B for one m16n8k16 (A 16x16 row-major fp16, B 16x8 fp16, fp32 accumulators), in the
+// register fragments of the PTX mma.sync description: lane = 4g + t holds A rows g and g + 8 (K
+// slots 2t, 2t+1 in a0/a1, 2t+8, 2t+9 in a2/a3), B column g (K slots 2t, 2t+1 in b0, 2t+8, 2t+9
+// in b1), C rows g and g + 8 at columns 2t and 2t + 1.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Four 8x8 matrices of 16-bit elements from shared memory: lane 8m + r gives the address of row r
+// of matrix m; lane 4g + t receives, in register m, the two elements (bytes 4t .. 4t+3) of row g of
+// matrix m.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// The stored codes are two's complement nibbles n (q = n - 16 [n >= 8]); o = n ^ 8 = q + 8 is the
+// offset-binary code.  q_lo: the codes in bits 0-3 and 16-19 of w as the fp16 pair (q, q'): one
+// LOP3 builds 1024 + o under the exponent of 1024 -- mask ? (w ^ k) : k, truth table 0x6A, with
+// k = 0x64086408: inside the mask k's bit 3 flips the nibble, outside it k supplies the exponent
+// bits -- and one subtraction of 1032.
+// q_hi: the codes in bits 4-7 and 20-23: 1024 + 16 o, times 1/16, minus 72.  Both exact.
+__device__ __forceinline__ uint32_t q_lo(uint32_t w) {
+  uint32_t p, r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(p) : "r"(w), "r"(0x000F000Fu), "r"(0x64086408u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(0x64086408u));  // 1032
+  return r;
+}
+__device__ __forceinline__ uint32_t q_hi(uint32_t w) {
+  uint32_t p, r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(p) : "r"(w), "r"(0x00F000F0u), "r"(0x64806480u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(p), "r"(0x2C002C00u), "r"(0xD480D480u));  // 1/16, -72
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);  // lo in the low 16 bits
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Byte offset of 16-byte sub-block `sub` of 128-byte line `line` of a tile written by TMA with the
+// 128-byte swizzle (tile base 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t line, uint32_t sub) { return line * 128u + ((sub ^ (line & 7u)) << 4); }
+
+// One 32-code group of a tile: two k16 MMAs on the words wa (A rows g) and wb (rows g + 8) against
+// the x / h fragment pairs b (pairs of columns (0,4), (1,5), (2,6), (3,7) of the lane's 8 columns).
+__device__ __forceinline__ void mma_group(float (&dg)[4], uint32_t wa, uint32_t wb, const uint4& b) {
+  dg[0] = dg[1] = dg[2] = dg[3] = 0.f;
+  mma_16816(dg, q_lo(wa), q_lo(wb), q_hi(wa), q_hi(wb), b.x, b.y);
+  mma_16816(dg, q_lo(wa >> 8), q_lo(wb >> 8), q_hi(wa >> 8), q_hi(wb >> 8), b.z, b.w);
+}
+
+// Top-K of one token by one warp from its keys in shared memory (key[e] = order-preserving key of
+// logit e, never 0; 0 past E; E <= 512): lane l holds keys l + 32 j in registers.  The K-th
+// largest of the 32 lane maxima is a lower bound of the K-th largest key (the K largest lane maxima
+// are K keys), so the keys at or above it hold the selection; when there are at most 64 of them,
+// each is ranked against the others (larger key, then lower expert) and rank k < K is the k-th
+// choice; otherwise (many equal logits) the K rounds of topk_warp decide.  Weights: exp(l - l_max)
+// renormalised over the K kept (the full softmax's normaliser cancels).  scratch: 96 uint2 of this
+// warp.  Lane k < K returns the k-th expert and its weight.
+__device__ __forceinline__ void topk_select_warp(uint32_t* key, int E, int K, uint2* scratch, int& my_i, float& my_w) {
+  const int lane = threadIdx.x & 31;
+  const int nj = (E + 31) >> 5;
+  uint32_t k[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) k[j] = j < nj ? key[j * 32 + lane] : 0u;
+  uint32_t lm = 0u;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) lm = max(lm, k[j]);
+  int rk = 0;  // rank of this lane's maximum among the lane maxima, ties to the lower lane
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const uint32_t o = __shfl_sync(0xffffffffu, lm, l);
+    rk += (o > lm) || (o == lm && l < lane);
+  }
+  const uint32_t tau = __reduce_max_sync(0xffffffffu, rk == K - 1 ? lm : 0u);
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) cnt += (k[j] != 0u && k[j] >= tau);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  uint2* cand = scratch;        // [64]
+  uint2* sel = scratch + 64;    // [32]
+  if (total > 64) {
+    topk_warp(key, E, K, my_i, my_w);
+    return;
+  }
+  int pos = incl - cnt;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (k[j] != 0u && k[j] >= tau) cand[pos++] = make_uint2(k[j], (uint32_t)(j * 32 + lane));
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int ci = lane + 32 * h;
+    if (ci < total) {
+      const uint2 me = cand[ci];
+      int rank = 0;
+#pragma unroll 4
+      for (int q = 0; q < total; ++q) {
+        const uint2 o = cand[q];
+        rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+      }
+      if (rank < K) sel[rank] = me;
+    }
+  }
+  __syncwarp();
+  const uint2 mine = lane < K ? sel[lane] : make_uint2(0u, 0u);
+  const float top = topk_key_value(sel[0].x);
+  const float p = lane < K ? expf(topk_key_value(mine.x) - top) : 0.f;
+  const float psum = warp_sum(p);
+  my_i = (int)mine.y;
+  my_w = lane < K ? p / psum : 0.f;
+  __syncwarp();
+}
+
+// What a gate/up unit needs to know about the launch and the CTA (one copy in shared memory).
+struct UnitCtx {
+  uint8_t* ring;
+  const uint4* xh;        // [T][XS] x fragments
+  float4* pgu;            // [16 warps][NT][32] partial tiles
+  const int4* slot_s;     // routed slots {expert, start, count, 0}
+  const int* perm_s;
+  const float* w_s;
+  uint64_t* full;
+  uint64_t* empty;
+  unsigned* s_done;       // per team: units finished (release / acquire, read by the flagger)
+  volatile int* abort;
+  __half* hw;
+  unsigned long long* timeline;
+  int NS, SB, XS, CH, d, f, fu, T, K, HS, c, nc, gu_code_bytes;
+};
+
+// One gate/up unit (item i of this CTA) by the 4 warps of team `team`: wait for its bytes, run its
+// 16 rows x d as m16n8k16 tiles over this warp's quarter of d, free the stage, sum the team's 4
+// partial tiles in warp order, write h = w silu(gate) up (fp16) for its 8 columns and tokens, and
+// hand the unit to the flagger.  Returns false when a wait gave up (uniform over the team).
+template <int NT>
+__device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, int lane) {
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int st = i % u.NS;
+  const bool okw = tc::mbar_wait_warp(&u.full[st], (i / u.NS) & 1, u.abort, kDlConsumerSleep);
+  if (!team_all(team, okw && !*u.abort)) return false;
+  if (i == 0 && tw == 0 && lane == 0 && u.timeline) u.timeline[(size_t)u.c * kDlEvents + kEvFirstUnit] = gtimer();
+  const int g = u.c + i * u.nc, s = g / u.fu, un = g - s * u.fu;
+  int n_s, start = 0;
+  if (s < u.HS) {
+    n_s = u.T;
+  } else {
+    const int4 sl = u.slot_s[s - u.HS];
+    n_s = sl.z;
+    start = sl.y;
+  }
+  const uint8_t* stg = u.ring + (size_t)st * u.SB;
+  const uint32_t sbase = tc::smem_u32(stg);
+  const int CH = u.CH, d = u.d;
+  // B fragments: the lane's column g8 of n-tile j is slot-local token 8 j + g8
+  int xrow[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int n = 8 * j + g8;
+    xrow[j] = n < n_s ? (s < u.HS ? n : u.perm_s[start + n] / u.K) * u.XS : -1;
+  }
+  float C[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) C[j][0] = C[j][1] = C[j][2] = C[j][3] = 0.f;
+  const int cb = tw * CH / kDlTeamWarps, cend = (tw + 1) * CH / kDlTeamWarps;  // this warp's chunks of K
+  const __half* scl = reinterpret_cast<const __half*>(stg + u.gu_code_bytes);  // [gate|up][8][d/32]
+  const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll 1
+  for (int ch = cb; ch < cend; ++ch) {
+    const uint4 sgv = *reinterpret_cast<const uint4*>(scl + (size_t)g8 * (d / 32) + ch * 8);
+    const uint4 suv = *reinterpret_cast<const uint4*>(scl + (size_t)(8 + g8) * (d / 32) + ch * 8);
+    const uint32_t sgw[4] = {sgv.x, sgv.y, sgv.z, sgv.w}, suw[4] = {suv.x, suv.y, suv.z, suv.w};
+    const uint32_t line = (uint32_t)(((mi & 1) * CH + ch) * 8 + rr);
+#pragma unroll
+    for (int jj = 0; jj < 8; jj += 2) {
+      // matrices (gate, group jj), (up, jj), (gate, jj + 1), (up, jj + 1) of this chunk
+      uint32_t wg0, wu0, wg1, wu1;
+      ldsm_x4(sbase + swz(line, (uint32_t)(jj + (mi >> 1))), wg0, wu0, wg1, wu1);
+      const float2 sg = __half22float2(*reinterpret_cast<const __half2*>(&sgw[jj >> 1]));
+      const float2 su = __half22float2(*reinterpret_cast<const __half2*>(&suw[jj >> 1]));
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int J = ch * 8 + jj + h2;  // group of 32 columns of d
+        const float sgf = h2 ? sg.y : sg.x, suf = h2 ? su.y : su.x;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const uint4 xb = xrow[j] >= 0 ? u.xh[xrow[j] + 4 * J + t4] : make_uint4(0u, 0u, 0u, 0u);
+          float dg[4];
+          mma_group(dg, h2 ? wg1 : wg0, h2 ? wu1 : wu0, xb);
+          C[j][0] = fmaf(sgf, dg[0], C[j][0]);
+          C[j][1] = fmaf(sgf, dg[1], C[j][1]);
+          C[j][2] = fmaf(suf, dg[2], C[j][2]);
+          C[j][3] = fmaf(suf, dg[3], C[j][3]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive_cnt(&u.empty[st], kDlWarps / kDlTeamWarps);  // the stage is free
+  float4* my_p = u.pgu + (size_t)(team * kDlTeamWarps + tw) * NT * 32;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
+  team_sync(team);
+  // team thread (j, ln): column ln / 4 of the unit, slot-local tokens 8 j + 2 (ln % 4) (+ 1); the
+  // team's 4 partial tiles are summed in warp order
+  const int tt = tw * 32 + lane;
+  if (tt < NT * 32) {
+    const int j = tt >> 5, ln = tt & 31;
+    const int col = ln >> 2, n0 = 8 * j + 2 * (ln & 3);
+    float4 sum = u.pgu[((size_t)(team * kDlTeamWarps) * NT + j) * 32 + ln];
+#pragma unroll
+    for (int q = 1; q < kDlTeamWarps; ++q) {
+      const float4 pp = u.pgu[((size_t)(team * kDlTeamWarps + q) * NT + j) * 32 + ln];
+      sum.x += pp.x;
+      sum.y += pp.y;
+      sum.z += pp.z;
+      sum.w += pp.w;
+    }
+    const int pos = 2 * (col & 3) + (col >> 2);  // fragment order of the 8 columns
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      const int n = n0 + o;
+      if (n < n_s) {
+        const float gte = o ? sum.y : sum.x, upv = o ? sum.w : sum.z;
+        float wt = 1.f;
+        size_t row = (size_t)n;
+        if (s >= u.HS) {
+          wt = u.w_s[u.perm_s[start + n]];
+          row = (size_t)u.HS * u.T + start + n;
+        }
+        u.hw[row * u.f + 8 * un + pos] = __float2half_rn(wt * (silu(gte) * upv));
+      }
+    }
+  }
+  team_sync(team);
+  // hand the unit to the flagger (which publishes it GPU-wide); after the team's stores
+  if (tw == 0 && lane == 0) st_release_cta(&u.s_done[team], (unsigned)((i - team) / kDlTeams + 1));
+  return true;
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int NT>  // n8 token tiles: 1 (T <= 8) or 2 (T <= 16)
+__global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArgs a, const __grid_constant__ DlMaps m) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int T = a.T, d = a.d, E = a.E, K = a.K, f = a.f;
+  const int nc = gridDim.x, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = a.ns, SB = a.stage_bytes, RB = a.rows_box;
+  const int fu = f / kDlUnit;          // units per slot (unit g of the CTA plan: slot g / fu)
+  const int CH = d / 256;              // 128-byte chunks of a gate/up row
+  const int CHd = f / 256;             // 128-byte chunks of a down row
+  const int GF = f / 32;               // scale groups of a down row
+  const int NB = d / 8;                // 8-column blocks of x
+  const int XS = NB + kDlXPad;         // row stride of the x fragments (conflict-free B loads)
+  const int HS = a.has_shared ? 1 : 0;
+  const int gu_code_bytes = CH * 2048;                       // 2 halves x CH chunks x 8 rows x 128 B
+  const int dn_code_bytes = RB * CHd * 128;
+  const int dn_scale_off = (dn_code_bytes + 127) & ~127;
+  const int dn_h_off = (dn_scale_off + RB * GF * 2 + 127) & ~127;
+
+  // this CTA's fixed shares
+  const int e0 = (int)((long long)E * c / nc), ne = (int)((long long)E * (c + 1) / nc) - e0;  // router rows
+  const int r0 = (int)((long long)d * c / nc), nr = (int)((long long)d * (c + 1) / nc) - r0;  // down rows
+
+  // shared memory: ring | xh | pgu | slot tables
+  uint8_t* ring = smem;
+  uint4* xh = reinterpret_cast<uint4*>(ring + (size_t)NS * SB);           // [T][XS] fp16 fragment blocks
+  float4* pgu = reinterpret_cast<float4*>(xh + (size_t)T * XS);          // [16 warps][NT][32] partial tiles
+  int4* slot_s = reinterpret_cast<int4*>(pgu + kDlWarps * NT * 32);      // [T*K] {expert, start, count, 0}
+  signed char* tpos = reinterpret_cast<signed char*>(slot_s + T * K);    // [T*K + 1][kDlMaxT]: slot-local position
+  int* perm_s = reinterpret_cast<int*>(tpos + (size_t)(T * K + 1) * kDlMaxT);  // [T*K]
+  int* idx_s = perm_s + T * K;                                           // [T*K]
+  float* w_s = reinterpret_cast<float*>(idx_s + T * K);                  // [T*K]
+  // the router rows, then the selection's keys, use ring stages 1 and 2: both are done with before
+  // the routed units are issued
+  uint8_t* scratch = ring + SB;
+  const float* wr_s = reinterpret_cast<const float*>(scratch);
+
+  __shared__ __align__(8) uint64_t full[kDlMaxStages], empty[kDlMaxStages], wr_full, route_ready;
+  __shared__ UnitCtx uc_s;
+  __shared__ uint32_t s_bits[32], s_bpre[32];  // dispatch: bitmap of the selected experts, its prefix counts
+  __shared__ volatile int s_abort;
+  __shared__ unsigned s_ep;
+  __shared__ int s_nact, s_issued;
+  __shared__ unsigned s_par;
+  __shared__ unsigned s_done[kDlTeams];  // gate/up units finished per team (release / acquire)
+  __shared__ float lpart[kDlWarps * kDlMaxT];
+  __shared__ float inv_s[kDlMaxT];
+
+  // This launch may start while the previous kernel in the stream is still finishing
+  // (programmatic dependent launch): before griddepcontrol.wait only this CTA's shared memory and
+  // read-only weights are touched.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    DL_STAMP(kEvStart);
+    DL_CLOCK(kClkStart);
+    for (int q = 0; q < kDlTeams; ++q) s_done[q] = 0u;
+    for (int s = 0; s < NS; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], kDlWarps);
+    }
+    tc::mbar_init(&wr_full, 1);
+    tc::mbar_init(&route_ready, 1);
+    s_abort = 0;
+    s_issued = 0;
+    UnitCtx& u = uc_s;
+    u.ring = ring;
+    u.xh = xh;
+    u.pgu = pgu;
+    u.slot_s = slot_s;
+    u.perm_s = perm_s;
+    u.w_s = w_s;
+    u.full = full;
+    u.empty = empty;
+    u.s_done = s_done;
+    u.abort = &s_abort;
+    u.hw = a.hw;
+    u.timeline = a.timeline;
+    u.NS = NS;
+    u.SB = SB;
+    u.XS = XS;
+    u.CH = CH;
+    u.d = d;
+    u.f = f;
+    u.fu = fu;
+    u.T = T;
+    u.K = K;
+    u.HS = HS;
+    u.c = c;
+    u.nc = nc;
+    u.gu_code_bytes = gu_code_bytes;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- the unit plan (identical in the producer and the consumers): unit g = c + i * nc
+  const bool first_is_shared = HS && c < fu;
+  UnitCtx* uc = &uc_s;
+
+  if (warp == kDlWarps) {
+    // ================================================================ producer
+    int k = 0;            // items issued
+    bool ok = true;
+    unsigned par = 0;
+    int nact = 0;
+    if (lane == 0) {
+      tc::prefetch_tmap(&m.gu_q);
+      tc::prefetch_tmap(&m.gu_s);
+      tc::prefetch_tmap(&m.dn_q);
+      tc::prefetch_tmap(&m.dn_s);
+      if (ne > 0) {
+        tc::mbar_arrive_expect_tx(&wr_full, (uint32_t)(ne * d * 4));
+        tc::bulk_g2s(scratch, a.Wr + (size_t)e0 * d, (uint32_t)(ne * d * 4), &wr_full);
+      }
+      if (first_is_shared) {
+        tc::mbar_arrive_expect_tx(&full[0], (uint32_t)(gu_code_bytes + 2 * 8 * (d / 32) * 2));
+        tc::tma_load_4d(ring, &m.sh_gu_q, 0, 8 * c, 0, 0, &full[0]);
+        tc::tma_load_3d(ring + gu_code_bytes, &m.sh_gu_s, 0, 8 * c, 0, &full[0]);
+        k = 1;
+        s_issued = 1;
+      }
+      ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, 32);
+      par = s_par;
+      nact = ok ? s_nact : 0;
+      DL_STAMP(kEvProducerRouted);
+    }
+    k = __shfl_sync(0xffffffffu, k, 0);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    par = __shfl_sync(0xffffffffu, par, 0);
+    nact = __shfl_sync(0xffffffffu, nact, 0);
+    const int nslots = HS + nact;
+    const int total_units = nslots * fu;
+    const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
+    unsigned* ready = a.ready + (size_t)par * kDlReadyStride;
+    // gate/up units
+    for (int i = k; ok && i < nG; ++i) {
+      const int st = i % NS;
+      if (lane == 0) {
+        ok = tc::mbar_wait_sleepy(&empty[st], ((i / NS) & 1) ^ 1u, &s_abort, kDlProducerSleep);
+        if (ok) {
+          const int g = c + i * nc, s = g / fu, u = g - s * fu;
+          uint8_t* dst = ring + (size_t)st * SB;
+          tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(gu_code_bytes + 2 * 8 * (d / 32) * 2));
+          if (s < HS) {
+            tc::tma_load_4d(dst, &m.sh_gu_q, 0, 8 * u, 0, 0, &full[st]);
+            tc::tma_load_3d(dst + gu_code_bytes, &m.sh_gu_s, 0, 8 * u, 0, &full[st]);
+          } else {
+            const int row = slot_s[s - HS].x * 2 * f + 8 * u;
+            tc::tma_load_4d(dst, &m.gu_q, 0, row, 0, 0, &full[st]);
+            tc::tma_load_3d(dst + gu_code_bytes, &m.gu_s, 0, row, 0, &full[st]);
+          }
+          s_issued = i + 1;
+          if (i == nG - 1) DL_STAMP(kEvLastUnitIssued);
+          if (i == k) DL_STAMP(kEvFirstUnitIssued);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    // down items: the weights of slot s's down rows as soon as a ring stage is free (they depend
+    // only on the routing); the slot's h rows once its ready counter shows all its units done
+    // everywhere (one proxy fence per batch of newly ready slots: the h rows were written with
+    // ordinary stores and are read by the bulk copies)
+    {
+      int nw = 0, nh = 0, known = 0;
+      unsigned polls = 0;
+      while (ok && nh < nslots) {
+        bool progress = false;
+        // as many down weights as there are free stages, back to back
+        while (nw < nslots) {
+          const int item = nG + nw, st = item % NS;
+          bool freed = false;
+          if (lane == 0) freed = tc::mbar_try_wait(&empty[st], ((item / NS) & 1) ^ 1u);
+          freed = __shfl_sync(0xffffffffu, freed ? 1 : 0, 0) != 0;
+          if (!freed) break;
+          {
+            if (lane == 0) {
+              int n_s, drow;
+              const CUtensorMap *mq, *ms;
+              if (nw < HS) {
+                n_s = T;
+                mq = &m.sh_dn_q;
+                ms = &m.sh_dn_s;
+                drow = r0;
+              } else {
+                const int4 sl = slot_s[nw - HS];
+                n_s = sl.z;
+                mq = &m.dn_q;
+                ms = &m.dn_s;
+                drow = sl.x * d + r0;
+              }
+              uint8_t* dst = ring + (size_t)st * SB;
+              // the phase completes once the weights and, later, the h rows have landed
+              tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(dn_code_bytes + RB * GF * 2) + (uint32_t)n_s * f * 2);
+              if (a.dn_swap)
+                tc::tma_load_3d(dst, mq, 0, drow, 0, &full[st]);
+              else
+                tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
+              tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
+              if (nw == nslots - 1) DL_STAMP(kEvLastDownWeights);
+            }
+            ++nw;
+            progress = true;
+          }
+        }
+        if (nh < nw) {
+          if (nh >= known) {
+            const int j = known + lane;
+            const bool r = j >= nslots || ld_acquire_gpu_u32(ready + j) >= (unsigned)fu;
+            const unsigned bal = __ballot_sync(0xffffffffu, r);
+            known += bal == 0xffffffffu ? 32 : __ffs(~bal) - 1;
+          }
+          __syncwarp();  // the acquires (by any lane) are ordered before lane 0's copies below
+          if (nh < known) {
+            const int hi = min(known, nw);
+            if (lane == 0) {
+              tc::fence_proxy_async_global();
+              if (nh == 0) DL_STAMP(kEvFirstH);
+              for (int q = nh; q < hi; ++q) {
+                const int item = nG + q, st = item % NS;
+                int n_s, hrow;
+                if (q < HS) {
+                  n_s = T;
+                  hrow = 0;
+                } else {
+                  const int4 sl = slot_s[q - HS];
+                  n_s = sl.z;
+                  hrow = HS * T + sl.y;
+                }
+                tc::bulk_g2s(ring + (size_t)st * SB + dn_h_off, a.hw + (size_t)hrow * f, (uint32_t)n_s * f * 2,
+                             &full[st]);
+                s_issued = item + 1;
+              }
+              if (hi == nslots) DL_STAMP(kEvLastDownIssued);
+              if (nh == 0) DL_STAMP(kEvFirstDownIssued);
+            }
+            nh = hi;
+            progress = true;
+          }
+        }
+        if (!progress) {
+          if (__any_sync(0xffffffffu, ++polls > kDlSpinLimit || s_abort)) ok = false;
+          __nanosleep(64);
+        } else {
+          polls = 0;
+        }
+      }
+      if (nh < nw && lane == 0) {
+        // giving up: complete the stages whose weights are in flight (their h rows are read as they
+        // are, in bounds) so that the exit can wait for every copy to land
+        for (int q = nh; q < nw; ++q) {
+          const int item = nG + q, st = item % NS;
+          const int n_s = q < HS ? T : slot_s[q - HS].z;
+          const int hrow = q < HS ? 0 : HS * T + slot_s[q - HS].y;
+          tc::bulk_g2s(ring + (size_t)st * SB + dn_h_off, a.hw + (size_t)hrow * f, (uint32_t)n_s * f * 2, &full[st]);
+        }
+        s_issued = nG + nw;
+      }
+    }
+    if (!ok && lane == 0) {
+      atomicOr(a.status, kStatusTimeout);
+      s_abort = 1;
+    }
+    __syncwarp();
+  } else if (warp == kDlWarps + 1) {
+    // ================================================================ flagger
+    // Publishes this CTA's finished gate/up units to the whole GPU: per batch of units the teams
+    // have finished (acquired from s_done), one GPU-scope fence and a relaxed add per unit to its
+    // slot's ready counter (the release pattern), off the teams' critical path.  Team q finishes
+    // its units in the order q, q + 4, q + 8, ... of this CTA's unit list.
+    if (lane == 0) {
+      bool okf = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, 64);
+      const int nslots = HS + (okf ? s_nact : 0);
+      const int total_units = nslots * fu;
+      const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
+      unsigned* ready = a.ready + (size_t)s_par * kDlReadyStride;
+      unsigned rel[kDlTeams] = {0u, 0u, 0u, 0u};
+      int total = 0;
+      unsigned spins = 0;
+      while (okf && total < nG) {
+        unsigned got[kDlTeams];
+        int nnew = 0;
+#pragma unroll
+        for (int q = 0; q < kDlTeams; ++q) {
+          got[q] = ld_acquire_cta(&s_done[q]);
+          nnew += (int)(got[q] - rel[q]);
+        }
+        if (nnew == 0) {
+          if (++spins > kDlSpinLimit || s_abort) okf = false;
+          __nanosleep(32);
+          continue;
+        }
+        spins = 0;
+        fence_acq_rel_gpu();
+#pragma unroll
+        for (int q = 0; q < kDlTeams; ++q)
+          for (unsigned mm = rel[q]; mm < got[q]; ++mm) {
+            const int g = c + (q + kDlTeams * (int)mm) * nc;
+            red_relaxed_gpu_u32(ready + g / fu, 1u);
+          }
+#pragma unroll
+        for (int q = 0; q < kDlTeams; ++q) rel[q] = got[q];
+        total += nnew;
+      }
+      if (!okf && !s_abort) {
+        atomicOr(a.status, kStatusTimeout);
+        s_abort = 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ consumers
+    const int ctid = threadIdx.x;
+    const int team = warp / kDlTeamWarps, tw = warp % kDlTeamWarps;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    bool ok = true;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are visible
+    if (ctid == 0) {
+      DL_STAMP(kEvDepWait);
+      // this launch's epoch: 1 + the number of complete launches.  Every CTA adds 1 to the counter
+      // when it ends; the previous launch is complete and fewer than gridDim.x additions of this
+      // launch can precede this read (this CTA's own is not among them), so the quotient is exact.
+      // A launch that gave up leaves the status word's timeout bit set: then this one gives up too
+      // (its y is NaN) until moe_get_device_status has reported it and reset the state.
+      const unsigned ep = (unsigned)(__ldcg(a.launches) / (unsigned long long)nc) + 1u, stw = __ldcg(a.status);
+      if (stw & kStatusTimeout) s_abort = 1;
+      s_ep = ep;
+      s_par = ep & 1u;
+    }
+    consumers_sync();
+    const unsigned lpar = s_par;  // this launch's ready counters: parity lpar
+    const unsigned long long ep_tag = (unsigned long long)s_ep << 32;
+    ok = !s_abort;
+    if (c == 0)
+      // zero the other parity's counters for the next launch (the previous launch, which used them,
+      // is complete: griddepcontrol.wait)
+      for (int i = ctid; i < kDlReadyStride; i += kDlWarps * 32) a.ready[(size_t)(lpar ^ 1u) * kDlReadyStride + i] = 0u;
+
+    // ---- phase 1: x (optionally RMS-normalised) as fp16 fragments, then the logits
+    if (a.prenorm) {
+#pragma unroll 1
+      for (int t = warp; t < T; t += kDlWarps) {
+        float ss = 0.f;
+#pragma unroll 4
+        for (int cc = lane; cc < NB; cc += 32) {
+          float v[8];
+          load8_act(a.x, a.act, (size_t)t * d + cc * 8, v);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) inv_s[t] = 1.0f / sqrtf(ss / (float)d + a.eps);
+      }
+      consumers_sync();
+    }
+    {
+      // all of a thread's x loads in flight at once (at most 8 per thread: T * d / 8 <= 4096)
+      uint4 xraw[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int cc = ctid + q * kDlWarps * 32;
+        if (cc < T * NB) xraw[q] = __ldg(reinterpret_cast<const uint4*>(a.x) + cc);
+      }
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        const int cc = ctid + q * kDlWarps * 32;
+        if (cc >= T * NB) break;
+        const uint4 xr = q == 0 ? xraw[0] : q == 1 ? xraw[1] : q == 2 ? xraw[2] : q == 3 ? xraw[3]
+                       : q == 4 ? xraw[4] : q == 5 ? xraw[5] : q == 6 ? xraw[6] : xraw[7];
+        const uint32_t wv[4] = {xr.x, xr.y, xr.z, xr.w};
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // bf16 pairs
+          v[2 * j] = __uint_as_float(wv[j] << 16);
+          v[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
+        }
+        const int ti = cc / NB, b = cc - ti * NB;
+        if (a.prenorm) {
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq) {
+            v[qq] = round_act(a.act, v[qq] * inv_s[ti]);
+            if (c == 0) store_act(a.xnorm, a.act, (size_t)cc * 8 + qq, v[qq]);
+          }
+        }
+        // fragment order of the 8 columns: pairs (0,4), (1,5), (2,6), (3,7)
+        xh[(size_t)ti * XS + b] =
+            make_uint4(pack_h2(v[0], v[4]), pack_h2(v[1], v[5]), pack_h2(v[2], v[6]), pack_h2(v[3], v[7]));
+      }
+    }
+    consumers_sync();
+    if (ctid == 0) DL_STAMP(kEvXStaged);
+    {
+      // logits of the router rows [e0, e0 + ne): warp = (row, part of the columns), tokens 4 at a time
+      const int nparts = ne > 0 ? max(1, kDlWarps / ne) : 1;
+      const int my_e = warp % max(ne, 1), my_pt = warp / max(ne, 1);
+      const bool r_on = ne > 0 && my_pt < nparts;
+      if (ne > 0) ok = tc::mbar_wait_warp(&wr_full, 0, &s_abort, kDlConsumerSleep);
+      if (ctid == 0) DL_STAMP(kEvRouterRows);
+      if (ok && r_on) {
+        const int bb = (int)((long long)NB * my_pt / nparts), be = (int)((long long)NB * (my_pt + 1) / nparts);
+        const float4* wr = reinterpret_cast<const float4*>(wr_s + (size_t)my_e * d);
+#pragma unroll 1
+        for (int t0 = 0; t0 < T; t0 += 4) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int b = bb + lane; b < be; b += 32) {
+            const float4 wa = wr[2 * b], wb = wr[2 * b + 1];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int t = min(t0 + q, T - 1);  // past T: a repeated token, not stored
+              const uint4 xv = xh[(size_t)t * XS + b];
+              const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));  // x0, x4
+              const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));  // x1, x5
+              const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&xv.z));  // x2, x6
+              const float2 p3 = __half22float2(*reinterpret_cast<const __half2*>(&xv.w));  // x3, x7
+              float sacc = acc[q];
+              sacc = fmaf(wa.x, p0.x, sacc);
+              sacc = fmaf(wa.y, p1.x, sacc);
+              sacc = fmaf(wa.z, p2.x, sacc);
+              sacc = fmaf(wa.w, p3.x, sacc);
+              sacc = fmaf(wb.x, p0.y, sacc);
+              sacc = fmaf(wb.y, p1.y, sacc);
+              sacc = fmaf(wb.z, p2.y, sacc);
+              sacc = fmaf(wb.w, p3.y, sacc);
+              acc[q] = sacc;
+            }
+          }
+          const float v = warp_sum_multi<4>(acc);  // token t0 + q in the lanes with (lane >> 3) == q
+          if ((lane & 7) == 0 && t0 + (lane >> 3) < T) lpart[warp * kDlMaxT + t0 + (lane >> 3)] = v;
+        }
+      }
+      ok = consumers_all(ok && !s_abort);
+      if (ok)
+#pragma unroll 1
+        for (int i = ctid; i < ne * T; i += kDlWarps * 32) {
+          const int le = i / T, t = i - le * T;
+          float v = 0.f;
+#pragma unroll 1
+          for (int p = 0; p < nparts; ++p) v += lpart[(p * ne + le) * kDlMaxT + t];
+          // published as one 64-bit word (epoch, key): a reader sees both or neither
+          __stcg(a.lgt + (size_t)t * E + e0 + le, ep_tag | topk_order_key(v + (a.bias ? a.bias[e0 + le] : 0.f)));
+        }
+      consumers_sync();
+      if (ctid == 0) DL_STAMP(kEvLogits);
+    }
+
+    // ---- team 0 runs the shared expert's unit of this CTA (routing-independent) while the other
+    // CTAs publish their logits
+    if (first_is_shared && team == 0 && ok) ok = gu_unit<NT>(*uc, 0, 0, tw, lane);
+
+    // ---- phase 2: every CTA gathers all logits of this launch (polling their epoch tags), then
+    // repeats the selection and the dispatch
+    ok = consumers_all(ok && !s_abort);
+    if (ok) {
+      const int EP = (E + 31) & ~31;
+      uint32_t* keys = reinterpret_cast<uint32_t*>(scratch);  // [T][EP] order-preserving keys, 0 = none
+      {
+        // at most 16 words per thread (T * EP <= 8192), all loads in flight, then re-poll the stale
+        unsigned long long wv[16];
+        const unsigned ept = (unsigned)(ep_tag >> 32);
+        int pending = 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int i = ctid + q * kDlWarps * 32;
+          const int t = i / EP, e = i - t * EP;
+          wv[q] = (i < T * EP && e < E) ? __ldcg(a.lgt + (size_t)t * E + e) : ep_tag;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pending += (unsigned)(wv[q] >> 32) != ept;
+        unsigned polls = 0;
+        while (pending) {
+          if (++polls > kDlSpinLimit || s_abort) break;
+          __nanosleep(64);
+          pending = 0;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            if ((unsigned)(wv[q] >> 32) != ept) {
+              const int i = ctid + q * kDlWarps * 32;
+              const int t = i / EP, e = i - t * EP;
+              wv[q] = __ldcg(a.lgt + (size_t)t * E + e);
+              pending += (unsigned)(wv[q] >> 32) != ept;
+            }
+          }
+        }
+        ok = pending == 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int i = ctid + q * kDlWarps * 32;
+          if (i < T * EP) keys[i] = (i - (i / EP) * EP) < E ? (uint32_t)wv[q] : 0u;
+        }
+      }
+      // the dispatch's expert bitmap and the slot-local position table start cleared
+      if (ctid < 32) s_bits[ctid] = 0u;
+      for (int i = ctid; i < HS + T * K; i += kDlWarps * 32)
+        reinterpret_cast<uint4*>(tpos)[i] = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+      ok = consumers_all(ok && !s_abort);
+      if (!ok && ctid == 0) {
+        atomicOr(a.status, kStatusTimeout);
+        s_abort = 1;
+      }
+      if (ctid == 0) DL_STAMP(kEvKeys);
+    }
+    if (ok) {
+      const int EP = (E + 31) & ~31;
+      uint32_t* keys = reinterpret_cast<uint32_t*>(scratch);
+      // one warp per token
+      if (warp < T) {
+        int my_i;
+        float my_w;
+        uint2* tk_scratch = reinterpret_cast<uint2*>(keys + (size_t)T * EP) + (size_t)warp * 96;
+        if (E <= 512)
+          topk_select_warp(keys + (size_t)warp * EP, E, K, tk_scratch, my_i, my_w);
+        else
+          topk_warp(keys + (size_t)warp * EP, E, K, my_i, my_w);
+        if (lane < K) {
+          idx_s[warp * K + lane] = my_i;
+          w_s[warp * K + lane] = my_w;
+          atomicOr(&s_bits[my_i >> 5], 1u << (my_i & 31));
+        }
+      }
+      consumers_sync();
+      if (ctid == 0) DL_STAMP(kEvSelected);
+      if (warp == 0) {
+        // slot of expert e = number of selected experts below e: per-word prefix of the bitmap
+        const uint32_t bw = s_bits[lane];
+        const int pc = __popc(bw);
+        int incl = pc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        s_bpre[lane] = incl - pc;
+        if (lane == 31) s_nact = incl;
+      }
+      consumers_sync();
+      const int n = T * K;
+      if (ctid < n) {
+        // assignment ctid: its place in the stable counting sort by expert, its slot, its position
+        // among the slot's tokens (tokens ascend with the assignment number)
+        const int e_i = idx_s[ctid];
+        int start = 0, cnt_i = 0, before = 0;
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+          const int ej = idx_s[j];
+          start += ej < e_i;
+          cnt_i += ej == e_i;
+          before += ej == e_i && j < ctid;
+        }
+        perm_s[start + before] = ctid;
+        const int slot = s_bpre[e_i >> 5] + __popc(s_bits[e_i >> 5] & ((1u << (e_i & 31)) - 1u));
+        if (before == 0) slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
+        tpos[(HS + slot) * kDlMaxT + ctid / K] = (signed char)before;
+      }
+      if (HS && ctid < T) tpos[ctid] = (signed char)ctid;
+      if (c == 0)
+#pragma unroll 1
+        for (int i = ctid; i < n; i += kDlWarps * 32) {
+          a.idx[i] = idx_s[i];
+          a.w[i] = w_s[i];
+        }
+      // the keys are done with: the producer's bulk copies may overwrite them
+      tc::fence_proxy_async_smem();
+      consumers_sync();
+      if (ctid == 0) {
+        DL_STAMP(kEvDispatched);
+        DL_STAMP(kEvRouted);
+        tc::mbar_arrive(&route_ready);
+      }
+      if (c == 0) {
+        // the full outputs: offs[e] = assignments with an expert below e
+        const int na = s_nact;
+#pragma unroll 1
+        for (int e = ctid; e <= E; e += kDlWarps * 32) {
+          int o = 0, ce = 0;
+#pragma unroll 4
+          for (int q = 0; q < n; ++q) {
+            o += idx_s[q] < e;
+            ce += idx_s[q] == e;
+          }
+          a.offs[e] = o;
+          if (e < E) a.counts[e] = ce;
+          if (e < E && ce && a.usage) a.usage[e] += (unsigned long long)ce;
+        }
+#pragma unroll 1
+        for (int q = ctid; q < na; q += kDlWarps * 32) {
+          a.active[q] = slot_s[q].x;
+          a.slots[q] = slot_s[q];
+        }
+#pragma unroll 1
+        for (int q = ctid; q < n; q += kDlWarps * 32) a.perm[q] = perm_s[q];
+        if (ctid == 0) {
+          *a.n_active = na;
+          if (a.stat) *a.stat = na;
+        }
+      }
+    }
+
+    const int nslots = HS + (ok ? s_nact : 0);
+    const int total_units = nslots * fu;
+    const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
+
+    // ---- phase 3: gate/up units; team (i % 4) takes unit i of this CTA
+#pragma unroll 1
+    for (int i = team + (first_is_shared && team == 0 ? kDlTeams : 0); ok && i < nG; i += kDlTeams)
+      ok = gu_unit<NT>(*uc, i, team, tw, lane);
+    ok = consumers_all(ok && !s_abort);
+    if (!ok && ctid == 0) s_abort = 1;  // the producer stops issuing
+    if (ctid == 0) DL_STAMP(kEvUnitsDone);
+
+    // ---- phase 4: down rows [r0, r0 + nr) of every slot, all warps
+    float D[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
+    {
+      const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
+      const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
+#pragma unroll 1
+      for (int s = 0; ok && s < nslots; ++s) {
+        const int item = nG + s, st = item % NS;
+        const bool okw = tc::mbar_wait_warp(&full[st], (item / NS) & 1, &s_abort, kDlConsumerSleep);
+        if (!consumers_all(okw && !s_abort)) {
+          ok = false;
+          break;
+        }
+        if (s == 0 && ctid == 0) DL_STAMP(kEvFirstDown);
+        const uint8_t* stg = ring + (size_t)st * SB;
+        const uint32_t sbase = tc::smem_u32(stg);
+        const __half* dsc = reinterpret_cast<const __half*>(stg + dn_scale_off);  // [RB][GF]
+        const uint4* hrows = reinterpret_cast<const uint4*>(stg + dn_h_off);     // [n_s][f/8]
+        const signed char* tp = tpos + s * kDlMaxT;
+        int hpos[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int n = 8 * j + g8;
+          hpos[j] = n < T ? (int)tp[n] * (f / 8) : -1;
+        }
+#pragma unroll 1
+        for (int jg = warp; jg < GF; jg += kDlWarps) {
+          const int chd = jg >> 3, sub = jg & 7;
+          const uint32_t line = a.dn_swap ? (uint32_t)(chd * RB + rrow) : (uint32_t)(rrow * CHd + chd);
+          uint32_t wa, wb;
+          ldsm_x2(sbase + swz(line, (uint32_t)sub), wa, wb);
+          const float sa = __half2float(dsc[rga * GF + jg]), sb = __half2float(dsc[rgb * GF + jg]);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const uint4 hb = hpos[j] >= 0 ? hrows[hpos[j] + 4 * jg + t4] : make_uint4(0u, 0u, 0u, 0u);
+            float dd[4];
+            mma_group(dd, wa, wb, hb);
+            D[j][0] = fmaf(sa, dd[0], D[j][0]);
+            D[j][1] = fmaf(sa, dd[1], D[j][1]);
+            D[j][2] = fmaf(sb, dd[2], D[j][2]);
+            D[j][3] = fmaf(sb, dd[3], D[j][3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[st]);
+      }
+    }
+    ok = consumers_all(ok && !s_abort);
+    if (!ok && ctid == 0) s_abort = 1;
+    if (ctid == 0) DL_STAMP(kEvDownDone);
+
+    // ---- y rows [r0, r0 + nr): the 16 warps' partial sums in warp order (+ residual)
+    float4* my_p = pgu + (size_t)warp * NT * 32;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(D[j][0], D[j][1], D[j][2], D[j][3]);
+    consumers_sync();
+    for (int i = ctid; i < nr * T; i += kDlWarps * 32) {
+      const int n = i / nr, r = i - n * nr;
+      const int j = n >> 3, nn = n & 7;
+      const int ln = (r & 7) * 4 + (nn >> 1), comp = (r >> 3) * 2 + (nn & 1);
+      float v = 0.f;
+#pragma unroll 4
+      for (int q = 0; q < kDlWarps; ++q) {
+        const float4 pp = pgu[((size_t)q * NT + j) * 32 + ln];
+        v += comp == 0 ? pp.x : comp == 1 ? pp.y : comp == 2 ? pp.z : pp.w;
+      }
+      const size_t o = (size_t)n * d + r0 + r;
+      if (ok) {
+        if (a.resid) v = load_act(a.resid, a.act, o) + v;
+      } else {
+        v = __int_as_float(0x7fc00000);  // NaN: this CTA gave up, its rows are not a result
+      }
+      store_act(a.y, a.act, o, v);
+    }
+    if (!ok && ctid == 0) {
+      atomicOr(a.status, kStatusTimeout);
+      s_abort = 1;
+    }
+    consumers_sync();
+    if (ctid == 0) {
+      DL_STAMP(kEvEnd);
+      DL_CLOCK(kClkEnd);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(a.launches, 1ull);  // this CTA is done with the launch's epoch
+  if (threadIdx.x == 0 && s_abort) {
+    // copies still in flight must land before the CTA's shared memory goes away
+    volatile int never = 0;
+    const int issued = s_issued;
+    for (int kk = issued - 1; kk >= 0 && kk >= issued - NS; --kk)  // the last copy of every stage
+      tc::mbar_wait(&full[kk % NS], (kk / NS) & 1, &never, 2000000000ll);
+    if (ne > 0) tc::mbar_wait(&wr_full, 0, &never, 2000000000ll);
+  }
+}
+
+// ------------------------------------------------------------------ self-test of the bounded waits
+// One CTA: thread 0 waits on an mbarrier nobody arrives at and on a barrier counter nobody bumps,
+// each with a small budget, exactly as the layer kernels wait.  Bit 0 of *result: the mbarrier
+// wait gave up; bit 1: the counter wait gave up; bit 2: a wait returned success (a bug).
+__global__ void bounded_wait_selftest_kernel(unsigned long long* counter, long long budget, unsigned* result) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int never;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    never = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned r = 0;
+    if (!tc::mbar_wait(&bar, 0, &never, budget)) r |= 1u; else r |= 4u;
+    // the counter never reaches this target; the poll limit bounds the wait
+    const unsigned long long target = ld_acquire_gpu(counter) + (1ull << 40);
+    bool ok = true;
+    for (unsigned n = 0; ok && ld_acquire_gpu(counter) < target; ++n) {
+      if (n > (unsigned)(budget >> 6)) ok = false;
+      __nanosleep(32);
+    }
+    r |= ok ? 4u : 2u;
+    *result = r;
+    if (r & 3u) atomicOr(result + 1, kStatusTimeout);
+  }
+}
+
+cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
+                                         cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(counter, budget, result);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ host side
+struct DlPlan {
+  int ns, stage_bytes, smem, rows_box;
+};
+
+static size_t up16(size_t n) { return (n + 15) & ~size_t(15); }
+
+static int rows_box_for(int d, int nsm) { return (d + nsm - 1) / nsm; }
+
+static DlPlan dl_plan(int T, int d, int f, int E, int K, int nsm) {
+  DlPlan p{};
+  p.rows_box = rows_box_for(d, nsm);
+  const int RB = p.rows_box;
+  const size_t gu = (size_t)(d / 256) * 2048 + 2 * 8 * (d / 32) * 2;
+  const size_t dn_codes = (size_t)RB * (f / 2);
+  const size_t dn = ((((dn_codes + 127) & ~size_t(127)) + (size_t)RB * (f / 32) * 2 + 127) & ~size_t(127)) +
+                    (size_t)T * f * 2;
+  p.stage_bytes = (int)((std::max(gu, dn) + 1023) & ~size_t(1023));
+  const int NT = T > 8 ? 2 : 1;
+  const size_t fixed = 1024 /* alignment */ + (size_t)T * (d / 8 + kDlXPad) * 16 + (size_t)kDlWarps * NT * 32 * 16 +
+                       up16((size_t)T * K * 16) + 3 * up16((size_t)T * K * 4) + up16((size_t)(T * K + 1) * kDlMaxT);
+  const long long room = (long long)kDlSmemMax - kDlStaticSlack - (long long)fixed;
+  p.ns = room > 0 ? (int)std::min<long long>(kDlMaxStages, room / p.stage_bytes) : 0;
+  p.smem = (int)((size_t)p.ns * p.stage_bytes + fixed);
+  return p;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_dl_encode = nullptr;
+
+template <int NT>
+static const void* dl_fn() {
+  return (const void*)decode_layer_kernel<NT>;
+}
+
+cudaError_t decode_kernels_init() {
+  if (!g_dl_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_dl_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const void* fns[2] = {dl_fn<1>(), dl_fn<2>()};
+  for (const void* fn : fns) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDlSmemMax - kDlStaticSlack);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Whether the one-launch layer serves this shape (INT4 weights, bf16 activations) with T tokens on
+// nsm SMs, all resident at once.
+bool decode_shape_ok(int T, int d, int f, int E, int K, int nsm) {
+  if (nsm <= 0 || T < 1 || T > kDlMaxT) return false;
+  if ((d != 1024 && d != 2048) || f % 256 || f > 2048 || E > kMaxE || K > kMaxK) return false;
+  if (T * K > kDlWarps * 32 || E > 2 * kDlWarps * 32) return false;  // dispatch / selection thread maps
+  if (T * K + 1 > 1024) return false;                                 // ready counters
+  if (rows_box_for(d, nsm) > kDlRowsMax) return false;
+  const DlPlan p = dl_plan(T, d, f, E, K, nsm);
+  if (p.ns < 3) return false;  // stage 0 (first unit) + stages 1-2 (router rows, then the selection's keys)
+  if ((size_t)((E + nsm - 1) / nsm) * d * 4 > 2 * (size_t)p.stage_bytes) return false;
+  if ((size_t)T * ((E + 31) & ~31) * 4 + (size_t)kDlWarps * 96 * 8 > 2 * (size_t)p.stage_bytes) return false;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, T > 8 ? dl_fn<2>() : dl_fn<1>(), kDlThreads, p.smem) !=
+          cudaSuccess ||
+      occ < 1) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+size_t decode_maps_bytes() { return sizeof(DlMaps); }
+
+static cudaError_t encode(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank, const cuuint64_t* dims,
+                          const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_dl_encode(m, dt, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static cudaError_t expert_maps(CUtensorMap* gq, CUtensorMap* gs, CUtensorMap* dq, CUtensorMap* ds, int n_exp, int d,
+                               int f, int RB, int dn_swap, const void* gu_q, const void* gu_s, const void* dn_q,
+                               const void* dn_s) {
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cudaError_t e;
+  {
+    const cuuint64_t dims[4] = {128, (cuuint64_t)n_exp * 2 * f, (cuuint64_t)d / 256, 2};
+    const cuuint64_t str[3] = {(cuuint64_t)d / 2, 128, (cuuint64_t)f * d / 2};
+    const cuuint32_t box[4] = {128, 8, (cuuint32_t)d / 256, 2};
+    if ((e = encode(gq, gu_q, U8, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)d / 32, (cuuint64_t)n_exp * 2 * f, 2};
+    const cuuint64_t str[2] = {(cuuint64_t)d / 32 * 2, (cuuint64_t)f * (d / 32) * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)d / 32, 8, 2};
+    if ((e = encode(gs, gu_s, F16, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+  }
+  if (dn_swap) {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)n_exp * d, (cuuint64_t)f / 256};
+    const cuuint64_t str[2] = {(cuuint64_t)f / 2, 128};
+    const cuuint32_t box[3] = {128, (cuuint32_t)RB, (cuuint32_t)f / 256};
+    if ((e = encode(dq, dn_q, U8, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+  } else {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)f / 256, (cuuint64_t)n_exp * d};
+    const cuuint64_t str[2] = {128, (cuuint64_t)f / 2};
+    const cuuint32_t box[3] = {128, (cuuint32_t)f / 256, (cuuint32_t)RB};
+    if ((e = encode(dq, dn_q, U8, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)f / 32, (cuuint64_t)n_exp * d};
+    const cuuint64_t str[1] = {(cuuint64_t)f / 32 * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)f / 32, (cuuint32_t)RB};
+    if ((e = encode(ds, dn_s, F16, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// The down box is [chunk][row] when the row's chunk count is even (rows then differ in the
+// swizzle's line bits), [row][chunk] when it is odd.
+static int dn_swap_for(int f) { return ((f / 256) & 1) ? 0 : 1; }
+
+cudaError_t decode_build_maps(void* maps, int E, int d, int f, int nsm, int has_shared, const void* gu_q,
+                              const void* gu_s, const void* dn_q, const void* dn_s, const void* sh_gu_q,
+                              const void* sh_gu_s, const void* sh_dn_q, const void* sh_dn_s) {
+  if (!g_dl_encode) return cudaErrorNotSupported;
+  DlMaps* mp = static_cast<DlMaps*>(maps);
+  const int RB = rows_box_for(d, nsm), sw = dn_swap_for(f);
+  cudaError_t e = expert_maps(&mp->gu_q, &mp->gu_s, &mp->dn_q, &mp->dn_s, E, d, f, RB, sw, gu_q, gu_s, dn_q, dn_s);
+  if (e != cudaSuccess) return e;
+  if (!has_shared) {  // the maps must be valid even when unused
+    sh_gu_q = gu_q;
+    sh_gu_s = gu_s;
+    sh_dn_q = dn_q;
+    sh_dn_s = dn_s;
+  }
+  return expert_maps(&mp->sh_gu_q, &mp->sh_gu_s, &mp->sh_dn_q, &mp->sh_dn_s, 1, d, f, RB, sw, sh_gu_q, sh_gu_s,
+                     sh_dn_q, sh_dn_s);
+}
+
+int decode_timeline_events() { return kDlEvents; }
+
+cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const void* maps, __half* hw,
+                                unsigned* ready, unsigned long long* lgt, unsigned long long* launches, int nsm,
+                                unsigned long long* timeline, cudaStream_t st) {
+  DlArgs a;
+  a.x = r.x;
+  a.act = r.act;
+  a.T = r.T;
+  a.d = r.d;
+  a.E = r.E;
+  a.K = r.K;
+  a.f = x.f;
+  a.has_shared = x.has_shared;
+  a.prenorm = r.prenorm;
+  a.eps = r.eps;
+  a.xnorm = r.xnorm;
+  a.Wr = r.Wr;
+  a.bias = r.bias;
+  a.idx = r.idx;
+  a.w = r.w;
+  a.counts = r.counts;
+  a.offs = r.offs;
+  a.perm = r.perm;
+  a.active = r.active;
+  a.n_active = r.n_active;
+  a.stat = r.stat;
+  a.slots = r.slots;
+  a.usage = r.usage;
+  a.hw = hw;
+  a.ready = ready;
+  a.y = x.y;
+  a.resid = x.resid;
+  a.lgt = lgt;
+  a.launches = launches;
+  a.status = r.status;
+  const DlPlan p = dl_plan(r.T, r.d, x.f, r.E, r.K, nsm);
+  a.ns = p.ns;
+  a.stage_bytes = p.stage_bytes;
+  a.rows_box = p.rows_box;
+  a.dn_swap = dn_swap_for(x.f);
+  a.timeline = timeline;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nsm);
+  cfg.blockDim = dim3(kDlThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  // One CTA per SM (the shared-memory plan allows no second), grid = #SMs (checked resident with
+  // the occupancy query when the handle is created); every wait is bounded anyway.  The launch may
+  // overlap the tail of the previous kernel in the stream (its prologue only reads weights);
+  // griddepcontrol.wait orders everything else.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const DlMaps& mp = *static_cast<const DlMaps*>(maps);
+  void* args[2] = {&a, const_cast<DlMaps*>(&mp)};
+  return cudaLaunchKernelExC(&cfg, r.T > 8 ? dl_fn<2>() : dl_fn<1>(), args);
+}
+
+}  // namespace moe

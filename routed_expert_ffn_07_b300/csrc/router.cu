@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteArgs a) {
     a.counts[i] = c;
     offv[i] = c;
     flag[i] = c > 0 ? 1 : 0;
+    if (a.usage && c) a.usage[i] += (unsigned long long)c;
   }
   __syncthreads();
   const int total = block_exclusive_scan(offv, E, scratch);
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(RouteArgs a, int nb
     for (int b = 0; b < nblocks; ++b) s += a.blockhist[(size_t)b * E + e];
     a.counts[e] = s;
     vals[e] = s;
+    if (a.usage && s) a.usage[e] += (unsigned long long)s;
   }
   __syncthreads();
   const int total = block_exclusive_scan(vals, E, scratch);
@@ -543,6 +545,8 @@ constexpr size_t kNaBytes = kNaStatus + 256;  // 121,600 bytes
 
 static __device__ __align__(256) unsigned char g_route_scratch[kNaBytes];
 
+void set_last_cuda_error(cudaError_t e);
+
 }  // namespace moe
 
 extern "C" moe_status moe_route_noalloc(const float* router_w, const float* router_b, const void* x, int act, int T,
@@ -560,14 +564,23 @@ extern "C" moe_status moe_route_noalloc(const float* router_w, const float* rout
   static std::mutex mu;
   static void* base[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) {
+    set_last_cuda_error(ce);
+    return MOE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
   unsigned char* sc;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!base[dev]) {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-      if (route_kernels_init() != cudaSuccess) return MOE_ERR_CUDA;
+      ce = cudaGetSymbolAddress(&p, g_route_scratch);
+      if (ce == cudaSuccess) ce = route_kernels_init();
+      if (ce != cudaSuccess || !p) {
+        set_last_cuda_error(ce);
+        return MOE_ERR_CUDA;
+      }
       base[dev] = p;
     }
     sc = static_cast<unsigned char*>(base[dev]);
@@ -598,8 +611,13 @@ extern "C" moe_status moe_route_noalloc(const float* router_w, const float* rout
   a.blockhist = nullptr;
   a.ticket = reinterpret_cast<unsigned*>(sc + kNaTicket);
   a.status = reinterpret_cast<unsigned*>(sc + kNaStatus);
+  a.usage = nullptr;
   // the last-block ticket must start at zero
-  if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_route(a, 1, st) != cudaSuccess) return MOE_ERR_CUDA;
+  ce = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st);
+  if (ce == cudaSuccess) ce = launch_route(a, 1, st);
+  if (ce != cudaSuccess) {
+    set_last_cuda_error(ce);
+    return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }

@@ -5,9 +5,16 @@ import pytest
 import oracle
 from routed_expert_ffn_07_b300 import inputs
 from routed_expert_ffn_07_b300.workloads import WORKLOADS, Workload, alloc_and_fill, create_handle, host_experts
-from tests.parity import (Y_TOL, W_ATOL, check_dispatch, check_routing, from_torch_act, to_torch_act, y_error)
+from tests.parity import (TIE_EPS, Y_TOL, W_ATOL, check_dispatch, check_routing, from_torch_act, to_torch_act,
+                          y_error)
 
 pytestmark = pytest.mark.gpu
+
+PATHS = {  # decode path -> (MOE_OPT_FUSED_MAX_TOKENS, MOE_OPT_GEMV_MAX_TOKENS)
+    "one_launch": (16, 16),
+    "gemv": (0, 16),
+    "tensor_core": (0, 0),
+}
 
 
 def _torch():
@@ -16,34 +23,50 @@ def _torch():
 
 
 def run_layer(h, wl, weights, x_np, T, layer=0, gen_layer=0):
-    """Route + forward one layer on the GPU and check everything against the oracle."""
+    """Forward one layer on the GPU and check the routing that forward pass used (read back with
+    moe_get_last_routing), its dispatch and its output against the oracle; then check that the
+    stand-alone routing call agrees with the forward's routing."""
     torch = _torch()
     from routed_expert_ffn_07_b300 import capi
     K, E = wl.K, wl.E
     n_layers = weights["router"].shape[0]
     x = to_torch_act(x_np)
-    idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
-    w = torch.empty(T * K, dtype=torch.float32, device="cuda")
-    offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-    perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
+
+    def outs():
+        return (torch.full((T * K,), -1, dtype=torch.int32, device="cuda"),
+                torch.full((T * K,), -1.0, dtype=torch.float32, device="cuda"),
+                torch.full((E + 1,), -1, dtype=torch.int32, device="cuda"),
+                torch.full((T * K,), -1, dtype=torch.int32, device="cuda"))
+
+    idx, w, offs, perm = outs()
     y = torch.empty_like(x)
     capi.moe_layer_forward(h, layer, x, T, y)
+    capi.moe_get_last_routing(h, T, idx, w, offs, perm)
     torch.cuda.synchronize()
     assert capi.moe_get_device_status(h) == 0
-    n_active_fwd = int(capi.moe_get_active_counts(h, n_layers)[layer])  # from the forward's own routing
-    capi.moe_route(h, layer, x, T, idx, w, offs, perm)
-    torch.cuda.synchronize()
+    n_active_fwd = int(capi.moe_get_active_counts(h, n_layers)[layer])
     Wr = weights["router"][layer].cpu().numpy()
     bias = None if weights["bias"] is None else weights["bias"][layer].cpu().numpy()
     logits, idx_ref, w_ref, gap = oracle.route(x_np, Wr, bias, K)
     idx_g = idx.cpu().numpy().reshape(T, K)
     flagged = check_routing(logits, idx_ref, gap, idx_g)
-    check_dispatch(idx_g, E, offs.cpu().numpy(), perm.cpu().numpy())
+    active = check_dispatch(idx_g, E, offs.cpu().numpy(), perm.cpu().numpy())
+    assert n_active_fwd == len(active)
     w_exp = oracle.weights_for(logits, idx_g)
     np.testing.assert_allclose(w.cpu().numpy().reshape(T, K), w_exp, rtol=0, atol=W_ATOL)
+    # the stand-alone routing call picks the same experts in the same slots (its logits are summed
+    # in another order, so a near-tie token may legitimately go either way there)
+    r_idx, r_w, r_offs, r_perm = outs()
+    capi.moe_route(h, layer, x, T, r_idx, r_w, r_offs, r_perm)
+    torch.cuda.synchronize()
+    r_idx_g = r_idx.cpu().numpy().reshape(T, K)
+    check_routing(logits, idx_ref, gap, r_idx_g)
+    clear = gap >= TIE_EPS
+    np.testing.assert_array_equal(r_idx_g[clear], idx_g[clear])
+    if clear.all():
+        assert torch.equal(r_offs, offs) and torch.equal(r_perm, perm)
+        np.testing.assert_allclose(r_w.cpu().numpy(), w.cpu().numpy(), rtol=0, atol=W_ATOL)
     used = sorted(set(idx_g.ravel().tolist()))
-    if not flagged:
-        assert n_active_fwd == len(used), "the forward pass routed differently"
     ex = host_experts(wl, gen_layer, used + ([E] if wl.shared else []))
     sh = ex.pop(E) if wl.shared else None
     y_ref, _, _ = oracle.layer(x_np, Wr, bias, ex, E, K, shared=sh, idx=idx_g)
@@ -116,19 +139,54 @@ def test_small_int4_shapes(case):
         capi.moe_destroy(h)
 
 
-def test_exact_ties_lower_index_on_gpu():
-    """Duplicated router rows give bit-identical logits on both sides: the lower index must win."""
-    torch = _torch()
+@pytest.mark.parametrize("path", ["one_launch", "gemv", "tensor_core"])
+def test_exact_ties_lower_index_on_gpu(path):
+    """Duplicated router rows give bit-identical logits on both sides: the lower index must win, on
+    every decode path and at T = 1, 2 (the one-launch layer's block-wide selection) and 4, 16."""
     from routed_expert_ffn_07_b300 import capi
-    wl = Workload(250, "ties", 4, 1024, 32, 4, 128, True, "int4", "bf16", 1, False)
+    wl = Workload(250, "ties", 16, 1024, 32, 4, 128, True, "int4", "bf16", 1, False)
     wts = alloc_and_fill(wl)
     r = wts["router"][0]
-    for a, b in ((3, 17), (5, 6), (9, 30), (12, 2)):
+    for a, b in ((3, 17), (5, 6), (9, 30), (12, 2), (20, 21), (0, 31)):
         r[b] = r[a]
     h = create_handle(wl, wts)
+    fz, gv = PATHS[path]
+    capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, fz)
+    capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gv)
     try:
-        x = inputs.gen_activations(wl.seed, 4, wl.d, "bf16")
-        run_layer(h, wl, wts, x, 4)
+        x = inputs.gen_activations(wl.seed, 16, wl.d, "bf16")
+        for T in (1, 2, 4, 16):
+            run_layer(h, wl, wts, x[:T], T)
+    finally:
+        capi.moe_destroy(h)
+
+
+@pytest.mark.parametrize("path", ["one_launch", "gemv", "tensor_core"])
+def test_all_logits_equal_picks_the_first_k_experts(path):
+    """A zero router makes every logit of every token exactly 0: all E experts tie, so each token
+    must get experts 0 .. K-1 in that order with weights 1/K (ties go to the lower index)."""
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl = WORKLOADS[2]
+    wts = alloc_and_fill(wl, n_layers=1)
+    wts["router"].zero_()
+    h = create_handle(wl, wts, max_tokens=16, n_layers=1)
+    fz, gv = PATHS[path]
+    capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, fz)
+    capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gv)
+    try:
+        x_all = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=4)
+        for T in (1, 2, 4, 16):
+            y, err, flagged = run_layer(h, wl, wts, x_all[:T], T)
+            assert flagged == T
+            idx = torch.empty(T * wl.K, dtype=torch.int32, device="cuda")
+            w = torch.empty(T * wl.K, dtype=torch.float32, device="cuda")
+            capi.moe_layer_forward(h, 0, to_torch_act(x_all[:T]), T, y)
+            capi.moe_get_last_routing(h, T, idx, w)
+            torch.cuda.synchronize()
+            expect = np.tile(np.arange(wl.K, dtype=np.int32), T)
+            np.testing.assert_array_equal(idx.cpu().numpy(), expect)
+            np.testing.assert_allclose(w.cpu().numpy(), 1.0 / wl.K, rtol=0, atol=W_ATOL)
     finally:
         capi.moe_destroy(h)
 
@@ -169,6 +227,9 @@ def test_decode_layer_batch_sizes(decode_layer):
 
 
 def _stack_parity(wl, sample_layers, gemv_max=None, fused_max=None):
+    """The stack, checked teacher-forced per layer: each sampled layer's input, normalised input and
+    the routing that layer used come from a traced run; the oracle recomputes that layer from the
+    traced input."""
     torch = _torch()
     from routed_expert_ffn_07_b300 import capi
     wts = alloc_and_fill(wl)
@@ -182,7 +243,11 @@ def _stack_parity(wl, sample_layers, gemv_max=None, fused_max=None):
         x0 = inputs.gen_activations(wl.seed, T, d, "bf16")
         xa = to_torch_act(x0)
         trace = torch.empty((L, 2, T, d), dtype=torch.bfloat16, device="cuda")
-        capi.moe_stack_forward(h, xa, T, trace)
+        r_idx = torch.full((L, T * K), -1, dtype=torch.int32, device="cuda")
+        r_w = torch.full((L, T * K), -1.0, dtype=torch.float32, device="cuda")
+        r_offs = torch.full((L, E + 1), -1, dtype=torch.int32, device="cuda")
+        r_perm = torch.full((L, T * K), -1, dtype=torch.int32, device="cuda")
+        capi.moe_stack_forward_traced(h, xa, T, trace, r_idx, r_w, r_offs, r_perm)
         xg = to_torch_act(x0)
         capi.moe_stack_forward(h, xg, T)   # graph replay
         capi.moe_stack_forward(h, xg2 := to_torch_act(x0), T)
@@ -193,6 +258,7 @@ def _stack_parity(wl, sample_layers, gemv_max=None, fused_max=None):
         tr = trace.view(torch.int16).cpu().numpy().view(np.uint16)
         final = from_torch_act(xa)
         counts = capi.moe_get_active_counts(h, L)
+        ri, rw, ro, rp = (t.cpu().numpy() for t in (r_idx, r_w, r_offs, r_perm))
         flagged_total = 0
         worst = 0.0
         for l in sample_layers:
@@ -202,18 +268,14 @@ def _stack_parity(wl, sample_layers, gemv_max=None, fused_max=None):
             ref_n = oracle.rmsnorm(x_l, 1e-6)
             got_n = oracle.widen(xn_l)
             assert np.all(np.abs(got_n - ref_n) <= 2.0 ** -8 * np.abs(ref_n) + 1e-30)
-            # routing of the layer on its (GPU) normalised input, re-run through the public route call
-            idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
-            offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-            perm = torch.empty(T * K, dtype=torch.int32, device="cuda")
-            capi.moe_route(h, l, to_torch_act(xn_l), T, idx, None, offs, perm)
-            torch.cuda.synchronize()
+            # the routing this layer of the stack used, against the oracle on the traced input
             Wr = wts["router"][l].cpu().numpy()
             bias = None if wts["bias"] is None else wts["bias"][l].cpu().numpy()
             logits, idx_ref, _, gap = oracle.route(xn_l, Wr, bias, K)
-            idx_g = idx.cpu().numpy().reshape(T, K)
+            idx_g = ri[l].reshape(T, K)
             flagged_total += check_routing(logits, idx_ref, gap, idx_g)
-            active = check_dispatch(idx_g, E, offs.cpu().numpy(), perm.cpu().numpy())
+            active = check_dispatch(idx_g, E, ro[l], rp[l])
+            np.testing.assert_allclose(rw[l].reshape(T, K), oracle.weights_for(logits, idx_g), rtol=0, atol=W_ATOL)
             assert counts[l] == len(active)
             ex = host_experts(wl, l, sorted(set(idx_g.ravel().tolist())) + [E])
             sh = ex.pop(E)
@@ -277,11 +339,6 @@ def test_invalid_arguments_rejected():
         capi.moe_destroy(h)
 
 
-PATHS = {  # decode path -> (MOE_OPT_FUSED_MAX_TOKENS, MOE_OPT_GEMV_MAX_TOKENS)
-    "one_launch": (8, 16),
-    "gemv": (0, 16),
-    "tensor_core": (0, 0),
-}
 
 
 @pytest.mark.parametrize("path", list(PATHS))
@@ -298,7 +355,7 @@ def test_decode_sizes_on_every_expert_path(decode_layer, path):
         for T in (1, 2, 3, 4, 5, 8, 16):
             run_layer(h, wl, wts, x[:T], T, layer=2, gen_layer=2)
     finally:
-        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)
+        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 16)
         capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 4)
 
 
@@ -320,7 +377,7 @@ def test_one_launch_layer_matches_gemv_path_closely(decode_layer):
             assert capi.moe_get_device_status(h) == 0
             out[path] = y.float()
     finally:
-        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)
+        capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 16)
         capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, 4)
     a, b = out["one_launch"], out["gemv"]
     # The GEMV path multiplies in fp32; the one-launch layer feeds its tensor cores fp16 operands
@@ -357,3 +414,32 @@ def test_bounded_waits_give_up_and_the_context_survives(decode_layer):
     wl, wts, h = decode_layer
     x = inputs.gen_activations(wl.seed, 1, wl.d, "bf16", layer=3)
     run_layer(h, wl, wts, x, 1, layer=0, gen_layer=0)
+
+
+def test_usage_histogram_counts_every_forward_exactly(decode_layer):
+    """The per-expert usage counters equal the sum of the oracle's dispatch counts of the routings
+    the forward passes used, over several calls, layers and token counts; moe_route adds nothing."""
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl, wts, h = decode_layer
+    L, E, K = wts["router"].shape[0], wl.E, wl.K
+    capi.moe_usage_read(h, L, E, reset=True)
+    capi.moe_usage_enable(h, True)
+    expect = np.zeros((L, E), dtype=np.uint64)
+    try:
+        x_all = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=13)
+        for i, (layer, T) in enumerate([(0, 1), (1, 4), (2, 16), (0, 2), (0, 1), (1, 16)]):
+            x = to_torch_act(x_all[:T])
+            y = torch.empty_like(x)
+            idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
+            capi.moe_layer_forward(h, layer, x, T, y)
+            capi.moe_get_last_routing(h, T, idx)
+            capi.moe_route(h, layer, x, T)          # not counted
+            torch.cuda.synchronize()
+            counts, _, _, _ = oracle.dispatch(idx.cpu().numpy().reshape(T, K), E)
+            expect[layer] += counts.astype(np.uint64)
+        got = capi.moe_usage_read(h, L, E, reset=True)
+        np.testing.assert_array_equal(got, expect)
+        assert not capi.moe_usage_read(h, L, E).any()
+    finally:
+        capi.moe_usage_enable(h, False)

@@ -61,3 +61,48 @@ def test_noalloc_route_rejects_sizes_beyond_its_scratch():
     with pytest.raises(capi.MoeError) as ei:
         capi.moe_route_noalloc(w, None, x, capi.MOE_ACT_BF16, 4, 256, 8, 9)    # K > E
     assert ei.value.status == 1
+
+
+def test_noalloc_route_inside_stream_capture_and_with_null_outputs():
+    """After one warm-up call (which looks up the scratch address), the call can be recorded into a
+    CUDA graph by the caller and replayed; outputs left NULL go to the library's scratch."""
+    import torch
+    from routed_expert_ffn_07_b300 import capi
+    wl = Workload(501, "noalloc_capture", 4, 1024, 64, 4, 128, True, "int4", "bf16", 1, False)
+    wts = alloc_and_fill(wl, n_layers=1)
+    h = create_handle(wl, wts, max_tokens=4, n_layers=1)
+    try:
+        T, E, K = 4, wl.E, wl.K
+        x = to_torch_act(inputs.gen_activations(wl.seed, T, wl.d, "bf16", layer=1))
+        ref = [torch.empty(T * K, dtype=torch.int32, device="cuda"),
+               torch.empty(T * K, dtype=torch.float32, device="cuda"),
+               torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+               torch.empty(T * K, dtype=torch.int32, device="cuda")]
+        capi.moe_route(h, 0, x, T, *ref)
+        # only the permutation requested
+        perm = torch.full_like(ref[3], -7)
+        capi.moe_route_noalloc(wts["router"][0], None, x, capi.MOE_ACT_BF16, T, wl.d, E, K, None, None, None, perm)
+        torch.cuda.synchronize()
+        assert torch.equal(perm, ref[3])
+        # recorded into a graph on a side stream, replayed twice
+        out = [torch.full_like(r, -7) for r in ref]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            capi.moe_route_noalloc(wts["router"][0], None, x, capi.MOE_ACT_BF16, T, wl.d, E, K, *out,
+                                   stream=s.cuda_stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            capi.moe_route_noalloc(wts["router"][0], None, x, capi.MOE_ACT_BF16, T, wl.d, E, K, *out,
+                                   stream=torch.cuda.current_stream().cuda_stream)
+        for _ in range(2):
+            for o in out:
+                o.fill_(-7)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out[0], ref[0]) and torch.equal(out[2], ref[2]) and torch.equal(out[3], ref[3])
+            np.testing.assert_allclose(out[1].cpu().numpy(), ref[1].cpu().numpy(), rtol=0, atol=W_ATOL)
+        del g
+    finally:
+        capi.moe_destroy(h)
