@@ -156,6 +156,16 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+// Strong (relaxed, GPU scope) load: a poll of a word that another SM writes must be a strong
+// operation to be sure to see the new value.
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -352,6 +362,9 @@ struct UnitCtx {
   __half* hw;
   unsigned long long* timeline;
   int NS, SB, XS, CH, d, f, fu, T, K, HS, c, nc, gu_code_bytes;
+  // down items
+  const signed char* tpos;  // [slot][kDlMaxT] slot-local position of every token (-1: not in the slot)
+  int RB, CHd, GF, dn_swap, dn_scale_off, dn_h_off;
 };
 
 // One gate/up unit (item i of this CTA) by the 4 warps of team `team`: wait for its bytes, run its
@@ -463,6 +476,55 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   return true;
 }
 
+// One down item (slot s, item k of this CTA) by the 4 warps of team `team`: wait for the slot's down
+// rows of this CTA's outputs and its h rows, and add this warp's quarter of the slot's 32-column
+// groups into the warp's accumulators D (rows g / g + 8 of the CTA's output tile, all T tokens as N;
+// a token not in the slot contributes zeros); free the stage.  Returns false when the wait gave up.
+template <int NT>
+__device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int team, int tw, int lane,
+                                          float (&D)[NT][4]) {
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int st = k % u.NS;
+  const bool okw = tc::mbar_wait_warp(&u.full[st], (k / u.NS) & 1, u.abort, kDlConsumerSleep);
+  if (!team_all(team, okw && !*u.abort)) return false;
+  const uint8_t* stg = u.ring + (size_t)st * u.SB;
+  const uint32_t sbase = tc::smem_u32(stg);
+  const __half* dsc = reinterpret_cast<const __half*>(stg + u.dn_scale_off);  // [RB][GF]
+  const uint4* hrows = reinterpret_cast<const uint4*>(stg + u.dn_h_off);     // [n_s][f/8]
+  const signed char* tp = u.tpos + s * kDlMaxT;
+  const int RB = u.RB, GF = u.GF;
+  int hpos[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int n = 8 * j + g8;
+    hpos[j] = n < u.T ? (int)tp[n] * (u.f / 8) : -1;
+  }
+  const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
+  const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
+  const int jb = tw * GF / kDlTeamWarps, je = (tw + 1) * GF / kDlTeamWarps;
+#pragma unroll 2
+  for (int jg = jb; jg < je; ++jg) {
+    const int chd = jg >> 3, sub = jg & 7;
+    const uint32_t line = u.dn_swap ? (uint32_t)(chd * RB + rrow) : (uint32_t)(rrow * u.CHd + chd);
+    uint32_t wa, wb;
+    ldsm_x2(sbase + swz(line, (uint32_t)sub), wa, wb);
+    const float sa = __half2float(dsc[rga * GF + jg]), sb = __half2float(dsc[rgb * GF + jg]);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const uint4 hb = hpos[j] >= 0 ? hrows[hpos[j] + 4 * jg + t4] : make_uint4(0u, 0u, 0u, 0u);
+      float dd[4];
+      mma_group(dd, wa, wb, hb);
+      D[j][0] = fmaf(sa, dd[0], D[j][0]);
+      D[j][1] = fmaf(sa, dd[1], D[j][1]);
+      D[j][2] = fmaf(sb, dd[2], D[j][2]);
+      D[j][3] = fmaf(sb, dd[3], D[j][3]);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive_cnt(&u.empty[st], kDlWarps / kDlTeamWarps);  // the stage is free
+  return true;
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int NT>  // n8 token tiles: 1 (T <= 8) or 2 (T <= 16)
 __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArgs a, const __grid_constant__ DlMaps m) {
@@ -555,6 +617,13 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     u.c = c;
     u.nc = nc;
     u.gu_code_bytes = gu_code_bytes;
+    u.tpos = tpos;
+    u.RB = RB;
+    u.CHd = CHd;
+    u.GF = GF;
+    u.dn_swap = a.dn_swap;
+    u.dn_scale_off = dn_scale_off;
+    u.dn_h_off = dn_h_off;
     tc::fence_mbar_init();
   }
   __syncthreads();
@@ -570,10 +639,15 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     unsigned par = 0;
     int nact = 0;
     if (lane == 0) {
-      tc::prefetch_tmap(&m.gu_q);
-      tc::prefetch_tmap(&m.gu_s);
-      tc::prefetch_tmap(&m.dn_q);
-      tc::prefetch_tmap(&m.dn_s);
+      // warm the routed experts' descriptors in the TMA unit: a small L2 prefetch through each (the
+      // rows of expert 0 that this CTA would read; harmless if unused)
+      tc::tma_prefetch_l2_4d(&m.gu_q, 0, 0, 0, 0);
+      tc::tma_prefetch_l2_3d(&m.gu_s, 0, 0, 0);
+      if (a.dn_swap)
+        tc::tma_prefetch_l2_3d(&m.dn_q, 0, r0, 0);
+      else
+        tc::tma_prefetch_l2_3d(&m.dn_q, 0, 0, r0);
+      tc::tma_prefetch_l2_2d(&m.dn_s, 0, r0);
       if (ne > 0) {
         tc::mbar_arrive_expect_tx(&wr_full, (uint32_t)(ne * d * 4));
         tc::bulk_g2s(scratch, a.Wr + (size_t)e0 * d, (uint32_t)(ne * d * 4), &wr_full);
@@ -598,30 +672,45 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     const int total_units = nslots * fu;
     const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
     unsigned* ready = a.ready + (size_t)par * kDlReadyStride;
-    // gate/up units
-    for (int i = k; ok && i < nG; ++i) {
-      const int st = i % NS;
-      if (lane == 0) {
-        ok = tc::mbar_wait_sleepy(&empty[st], ((i / NS) & 1) ^ 1u, &s_abort, kDlProducerSleep);
-        if (ok) {
-          const int g = c + i * nc, s = g / fu, u = g - s * fu;
-          uint8_t* dst = ring + (size_t)st * SB;
-          tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(gu_code_bytes + 2 * 8 * (d / 32) * 2));
-          if (s < HS) {
-            tc::tma_load_4d(dst, &m.sh_gu_q, 0, 8 * u, 0, 0, &full[st]);
-            tc::tma_load_3d(dst + gu_code_bytes, &m.sh_gu_s, 0, 8 * u, 0, &full[st]);
-          } else {
-            const int row = slot_s[s - HS].x * 2 * f + 8 * u;
-            tc::tma_load_4d(dst, &m.gu_q, 0, row, 0, 0, &full[st]);
-            tc::tma_load_3d(dst + gu_code_bytes, &m.gu_s, 0, row, 0, &full[st]);
-          }
-          s_issued = i + 1;
-          if (i == nG - 1) DL_STAMP(kEvLastUnitIssued);
-          if (i == k) DL_STAMP(kEvFirstUnitIssued);
+    // gate/up units: lane 0 alone, a tight loop (this warp shares its scheduler with busy consumer
+    // warps, so every instruction here is slow); a stage is waited for only once the ring wraps
+    if (lane == 0) {
+      const uint32_t gu_bytes = (uint32_t)(gu_code_bytes + 2 * 8 * (d / 32) * 2);
+      int st = k % NS, ph = (k / NS) & 1;
+      int g = c + k * nc, s = g / fu, u = g - s * fu;
+      const int step_s = nc / fu, step_u = nc - step_s * fu;  // g += nc in (slot, unit) coordinates
+      int i = k;
+      for (; i < nG; ++i) {
+        if (i >= NS && !tc::mbar_wait_sleepy(&empty[st], ph ^ 1u, &s_abort, kDlProducerSleep)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = ring + (size_t)st * SB;
+        tc::mbar_arrive_expect_tx(&full[st], gu_bytes);
+        if (s < HS) {
+          tc::tma_load_4d(dst, &m.sh_gu_q, 0, 8 * u, 0, 0, &full[st]);
+          tc::tma_load_3d(dst + gu_code_bytes, &m.sh_gu_s, 0, 8 * u, 0, &full[st]);
+        } else {
+          const int row = slot_s[s - HS].x * 2 * f + 8 * u;
+          tc::tma_load_4d(dst, &m.gu_q, 0, row, 0, 0, &full[st]);
+          tc::tma_load_3d(dst + gu_code_bytes, &m.gu_s, 0, row, 0, &full[st]);
+        }
+        if (i == k) DL_STAMP(kEvFirstUnitIssued);
+        if (++st == NS) {
+          st = 0;
+          ph ^= 1;
+        }
+        s += step_s;
+        u += step_u;
+        if (u >= fu) {
+          u -= fu;
+          ++s;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      s_issued = i;
+      DL_STAMP(kEvLastUnitIssued);
     }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     // down items: the weights of slot s's down rows as soon as a ring stage is free (they depend
     // only on the routing); the slot's h rows once its ready counter shows all its units done
     // everywhere (one proxy fence per batch of newly ready slots: the h rows were written with
@@ -630,44 +719,41 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
       int nw = 0, nh = 0, known = 0;
       unsigned polls = 0;
       while (ok && nh < nslots) {
-        bool progress = false;
-        // as many down weights as there are free stages, back to back
-        while (nw < nslots) {
-          const int item = nG + nw, st = item % NS;
-          bool freed = false;
-          if (lane == 0) freed = tc::mbar_try_wait(&empty[st], ((item / NS) & 1) ^ 1u);
-          freed = __shfl_sync(0xffffffffu, freed ? 1 : 0, 0) != 0;
-          if (!freed) break;
-          {
-            if (lane == 0) {
-              int n_s, drow;
-              const CUtensorMap *mq, *ms;
-              if (nw < HS) {
-                n_s = T;
-                mq = &m.sh_dn_q;
-                ms = &m.sh_dn_s;
-                drow = r0;
-              } else {
-                const int4 sl = slot_s[nw - HS];
-                n_s = sl.z;
-                mq = &m.dn_q;
-                ms = &m.dn_s;
-                drow = sl.x * d + r0;
-              }
-              uint8_t* dst = ring + (size_t)st * SB;
-              // the phase completes once the weights and, later, the h rows have landed
-              tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(dn_code_bytes + RB * GF * 2) + (uint32_t)n_s * f * 2);
-              if (a.dn_swap)
-                tc::tma_load_3d(dst, mq, 0, drow, 0, &full[st]);
-              else
-                tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
-              tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
-              if (nw == nslots - 1) DL_STAMP(kEvLastDownWeights);
+        // as many down weights as there are free stages, back to back (lane 0 alone)
+        int nw_new = nw;
+        if (lane == 0) {
+          while (nw_new < nslots) {
+            const int item = nG + nw_new, st = item % NS;
+            if (!tc::mbar_try_wait(&empty[st], ((item / NS) & 1) ^ 1u)) break;
+            int n_s, drow;
+            const CUtensorMap *mq, *ms;
+            if (nw_new < HS) {
+              n_s = T;
+              mq = &m.sh_dn_q;
+              ms = &m.sh_dn_s;
+              drow = r0;
+            } else {
+              const int4 sl = slot_s[nw_new - HS];
+              n_s = sl.z;
+              mq = &m.dn_q;
+              ms = &m.dn_s;
+              drow = sl.x * d + r0;
             }
-            ++nw;
-            progress = true;
+            uint8_t* dst = ring + (size_t)st * SB;
+            // the phase completes once the weights and, later, the h rows have landed
+            tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(dn_code_bytes + RB * GF * 2) + (uint32_t)n_s * f * 2);
+            if (a.dn_swap)
+              tc::tma_load_3d(dst, mq, 0, drow, 0, &full[st]);
+            else
+              tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
+            tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
+            ++nw_new;
           }
+          if (nw_new == nslots && nw < nslots) DL_STAMP(kEvLastDownWeights);
         }
+        nw_new = __shfl_sync(0xffffffffu, nw_new, 0);
+        bool progress = nw_new > nw;
+        nw = nw_new;
         if (nh < nw) {
           if (nh >= known) {
             const int j = known + lane;
@@ -777,7 +863,6 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     // ================================================================ consumers
     const int ctid = threadIdx.x;
     const int team = warp / kDlTeamWarps, tw = warp % kDlTeamWarps;
-    const int g8 = lane >> 2, t4 = lane & 3;
     bool ok = true;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are visible
@@ -904,7 +989,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 #pragma unroll 1
           for (int p = 0; p < nparts; ++p) v += lpart[(p * ne + le) * kDlMaxT + t];
           // published as one 64-bit word (epoch, key): a reader sees both or neither
-          __stcg(a.lgt + (size_t)t * E + e0 + le, ep_tag | topk_order_key(v + (a.bias ? a.bias[e0 + le] : 0.f)));
+          st_relaxed_gpu(a.lgt + (size_t)t * E + e0 + le, ep_tag | topk_order_key(v + (a.bias ? a.bias[e0 + le] : 0.f)));
         }
       consumers_sync();
       if (ctid == 0) DL_STAMP(kEvLogits);
@@ -929,7 +1014,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         for (int q = 0; q < 16; ++q) {
           const int i = ctid + q * kDlWarps * 32;
           const int t = i / EP, e = i - t * EP;
-          wv[q] = (i < T * EP && e < E) ? __ldcg(a.lgt + (size_t)t * E + e) : ep_tag;
+          wv[q] = (i < T * EP && e < E) ? ld_relaxed_gpu(a.lgt + (size_t)t * E + e) : ep_tag;
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) pending += (unsigned)(wv[q] >> 32) != ept;
@@ -943,7 +1028,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
             if ((unsigned)(wv[q] >> 32) != ept) {
               const int i = ctid + q * kDlWarps * 32;
               const int t = i / EP, e = i - t * EP;
-              wv[q] = __ldcg(a.lgt + (size_t)t * E + e);
+              wv[q] = ld_relaxed_gpu(a.lgt + (size_t)t * E + e);
               pending += (unsigned)(wv[q] >> 32) != ept;
             }
           }
@@ -986,6 +1071,35 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
       }
       consumers_sync();
       if (ctid == 0) DL_STAMP(kEvSelected);
+      const int n = T * K;
+      if (n <= 32) {
+        // few assignments: one warp does the whole dispatch with shuffles.  Lane i = assignment i: its
+        // place in the stable counting sort (assignments with a smaller expert, plus the earlier ones
+        // with its expert), its slot (distinct experts below its own), its position in the slot.
+        if (warp == 0) {
+          const int e_i = lane < n ? idx_s[lane] : 0x7fffffff;
+          int start = 0, cnt_i = 0, before = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, e_i, j);
+            start += ej < e_i;
+            cnt_i += ej == e_i;
+            before += ej == e_i && j < lane;
+          }
+          const bool first = lane < n && before == 0;
+          const unsigned fm = __ballot_sync(0xffffffffu, first);
+          int slot = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) slot += ((fm >> j) & 1u) && __shfl_sync(0xffffffffu, e_i, j) < e_i;
+          if (lane < n) {
+            perm_s[start + before] = lane;
+            if (first) slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
+            tpos[(HS + slot) * kDlMaxT + lane / K] = (signed char)before;
+          }
+          if (HS && lane < T) tpos[lane] = (signed char)lane;
+          if (lane == 0) s_nact = __popc(fm);
+        }
+      } else {
       if (warp == 0) {
         // slot of expert e = number of selected experts below e: per-word prefix of the bitmap
         const uint32_t bw = s_bits[lane];
@@ -1000,7 +1114,6 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         if (lane == 31) s_nact = incl;
       }
       consumers_sync();
-      const int n = T * K;
       if (ctid < n) {
         // assignment ctid: its place in the stable counting sort by expert, its slot, its position
         // among the slot's tokens (tokens ascend with the assignment number)
@@ -1019,6 +1132,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         tpos[(HS + slot) * kDlMaxT + ctid / K] = (signed char)before;
       }
       if (HS && ctid < T) tpos[ctid] = (signed char)ctid;
+      }
       if (c == 0)
 #pragma unroll 1
         for (int i = ctid; i < n; i += kDlWarps * 32) {
@@ -1066,65 +1180,24 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     const int total_units = nslots * fu;
     const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
 
-    // ---- phase 3: gate/up units; team (i % 4) takes unit i of this CTA
-#pragma unroll 1
-    for (int i = team + (first_is_shared && team == 0 ? kDlTeams : 0); ok && i < nG; i += kDlTeams)
-      ok = gu_unit<NT>(*uc, i, team, tw, lane);
-    ok = consumers_all(ok && !s_abort);
-    if (!ok && ctid == 0) s_abort = 1;  // the producer stops issuing
-    if (ctid == 0) DL_STAMP(kEvUnitsDone);
-
-    // ---- phase 4: down rows [r0, r0 + nr) of every slot, all warps
+    // ---- phase 3: this CTA's items in order -- its gate/up units, then the down items of every
+    // slot; team (k % 4) takes item k.  A team finishes all its gate/up units before any of its down
+    // items, so the slots' h rows (everywhere) do not wait on a down item.
     float D[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
-    {
-      const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
-      const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
 #pragma unroll 1
-      for (int s = 0; ok && s < nslots; ++s) {
-        const int item = nG + s, st = item % NS;
-        const bool okw = tc::mbar_wait_warp(&full[st], (item / NS) & 1, &s_abort, kDlConsumerSleep);
-        if (!consumers_all(okw && !s_abort)) {
-          ok = false;
-          break;
-        }
-        if (s == 0 && ctid == 0) DL_STAMP(kEvFirstDown);
-        const uint8_t* stg = ring + (size_t)st * SB;
-        const uint32_t sbase = tc::smem_u32(stg);
-        const __half* dsc = reinterpret_cast<const __half*>(stg + dn_scale_off);  // [RB][GF]
-        const uint4* hrows = reinterpret_cast<const uint4*>(stg + dn_h_off);     // [n_s][f/8]
-        const signed char* tp = tpos + s * kDlMaxT;
-        int hpos[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int n = 8 * j + g8;
-          hpos[j] = n < T ? (int)tp[n] * (f / 8) : -1;
-        }
-#pragma unroll 1
-        for (int jg = warp; jg < GF; jg += kDlWarps) {
-          const int chd = jg >> 3, sub = jg & 7;
-          const uint32_t line = a.dn_swap ? (uint32_t)(chd * RB + rrow) : (uint32_t)(rrow * CHd + chd);
-          uint32_t wa, wb;
-          ldsm_x2(sbase + swz(line, (uint32_t)sub), wa, wb);
-          const float sa = __half2float(dsc[rga * GF + jg]), sb = __half2float(dsc[rgb * GF + jg]);
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const uint4 hb = hpos[j] >= 0 ? hrows[hpos[j] + 4 * jg + t4] : make_uint4(0u, 0u, 0u, 0u);
-            float dd[4];
-            mma_group(dd, wa, wb, hb);
-            D[j][0] = fmaf(sa, dd[0], D[j][0]);
-            D[j][1] = fmaf(sa, dd[1], D[j][1]);
-            D[j][2] = fmaf(sb, dd[2], D[j][2]);
-            D[j][3] = fmaf(sb, dd[3], D[j][3]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&empty[st]);
+    for (int k = team + (first_is_shared && team == 0 ? kDlTeams : 0); ok && k < nG + nslots; k += kDlTeams) {
+      if (k < nG) {
+        ok = gu_unit<NT>(*uc, k, team, tw, lane);
+        if (k + kDlTeams >= nG && tw == 0 && lane == 0) DL_STAMP(kEvUnitsDone);  // this team's last unit
+      } else {
+        if (k - nG < kDlTeams && tw == 0 && lane == 0 && team == 0) DL_STAMP(kEvFirstDown);
+        ok = down_item<NT>(*uc, k, k - nG, team, tw, lane, D);
       }
     }
     ok = consumers_all(ok && !s_abort);
-    if (!ok && ctid == 0) s_abort = 1;
+    if (!ok && ctid == 0) s_abort = 1;  // the producer stops issuing
     if (ctid == 0) DL_STAMP(kEvDownDone);
 
     // ---- y rows [r0, r0 + nr): the 16 warps' partial sums in warp order (+ residual)
