@@ -132,33 +132,97 @@ def traffic_from_profiles(kernel: str, source: str, workload: str):
     return ent["dram_bytes_per_launch"] if ent.get("source_sha16") == sha else None
 
 
-def cpu_baseline_decode(wl, budget_s=12.0, max_layers=48):
-    """The fp64 oracle on host cores: the same decode layer (route + 10 experts + shared) for one
-    token, cycling layers, until the time budget is spent.  Expert bytes are generated outside
-    the timed part."""
+def _oracle_decode_inputs(wl, n_layers):
+    """Per-layer oracle inputs of the decode workload (router, expert planes), generated outside any
+    timed region."""
     import oracle
     from routed_expert_ffn_07_b300 import inputs
     from routed_expert_ffn_07_b300.workloads import host_experts
-
     x = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)
-    tokens = 0
-    spent = 0.0
-    layers = 0
-    for l in range(max_layers):
+    out = []
+    for l in range(n_layers):
         Wr = inputs.gen_router(wl.seed, l, wl.E, wl.d)
         _, idx, _, _ = oracle.route(x, Wr, None, wl.K, nthreads=1)
         ex = host_experts(wl, l, sorted(set(idx.ravel().tolist())) + [wl.E])
+        out.append((Wr, ex))
+    return x, out
+
+
+def cpu_baseline_decode(wl, budget_s=10.0, max_layers=24):
+    """The fp64 oracle on the host cores: the decode layer (route + 10 experts + shared expert) for one
+    token, one distinct layer per call.  Single-threaded, and on all cores (one host thread per
+    layer call, several calls at once; the oracle's own OpenMP loop is over tokens, so it cannot
+    spread one token).  Expert bytes are generated outside the timed parts."""
+    import concurrent.futures
+    import oracle
+    cores = os.cpu_count() or 1
+    x, prep = _oracle_decode_inputs(wl, max_layers)
+
+    def one(i):
+        Wr, ex = prep[i % len(prep)]
+        ex = dict(ex)
         sh = ex.pop(wl.E)
-        t0 = time.perf_counter()
         oracle.layer(x, Wr, None, ex, wl.E, wl.K, shared=sh, nthreads=1)
+
+    one(0)  # warm
+    spent, calls = 0.0, 0
+    while spent < budget_s / 2 and calls < len(prep):
+        t0 = time.perf_counter()
+        one(calls)
         spent += time.perf_counter() - t0
-        tokens += wl.T
-        layers += 1
-        if spent > budget_s:
-            break
-    return {"value": tokens / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{layers} decode-layer calls (T={wl.T}, one per distinct layer), fp64, single thread; "
-                      f"{spent:.1f} s of oracle time"}
+        calls += 1
+    single = calls * wl.T / spent
+    n_par = max(cores, 1) * 2
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as pool:
+        list(pool.map(one, range(n_par)))
+    t_all = time.perf_counter() - t0
+    return {"value": single, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} decode-layer calls (T={wl.T}, one per distinct layer), fp64, one thread, "
+                      f"{spent:.1f} s",
+            "all_cores": {"value": n_par * wl.T / t_all, "unit": "tokens/s", "cores": cores,
+                          "sample": f"{n_par} decode-layer calls on {cores} host threads at once, {t_all:.1f} s"}}
+
+
+def cpu_baseline_prefill(wl, n_tokens=64):
+    """The oracle on all host cores (its OpenMP loop over tokens) for a sample of the prefill chunk:
+    the first n_tokens tokens of the 4096-token workload, routed and computed in fp64."""
+    import oracle
+    from routed_expert_ffn_07_b300 import inputs
+    from routed_expert_ffn_07_b300.workloads import host_experts
+    cores = os.cpu_count() or 1
+    x = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)[:n_tokens]
+    Wr = inputs.gen_router(wl.seed, 0, wl.E, wl.d)
+    _, idx, _, _ = oracle.route(x, Wr, None, wl.K, nthreads=0)
+    ex = host_experts(wl, 0, sorted(set(idx.ravel().tolist())) + [wl.E])
+    sh = ex.pop(wl.E)
+    t0 = time.perf_counter()
+    oracle.layer(x, Wr, None, ex, wl.E, wl.K, shared=sh, nthreads=0)
+    t = time.perf_counter() - t0
+    return {"value": n_tokens / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_tokens} of the 4096 prefill tokens through one layer, fp64, {cores} threads, {t:.1f} s"}
+
+
+def cpu_baseline_stack_layer(wl):
+    """The oracle for one layer of the T-token stack (RMSNorm, routing, experts), all host cores."""
+    import oracle
+    from routed_expert_ffn_07_b300 import inputs
+    from routed_expert_ffn_07_b300.workloads import host_experts
+    cores = os.cpu_count() or 1
+    x = inputs.gen_activations(wl.seed, wl.T, wl.d, wl.act)
+    Wr = inputs.gen_router(wl.seed, 0, wl.E, wl.d)
+    bias = inputs.gen_zipf_prior(wl.seed, 0, wl.E, wl.zipf) if wl.zipf > 0 else None
+    t0 = time.perf_counter()
+    oracle.rmsnorm(x, 1e-6)
+    t_norm = time.perf_counter() - t0
+    _, idx, _, _ = oracle.route(x, Wr, bias, wl.K, nthreads=0)
+    ex = host_experts(wl, 0, sorted(set(idx.ravel().tolist())) + [wl.E])
+    sh = ex.pop(wl.E)
+    t0 = time.perf_counter()
+    oracle.layer(x, Wr, bias, ex, wl.E, wl.K, shared=sh, nthreads=0)
+    t = time.perf_counter() - t0 + t_norm
+    return {"value": wl.T / t, "unit": "MoE-layer tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one layer of the stack (T={wl.T}), fp64, {cores} threads, {t:.2f} s"}
 
 
 def measure_decode_layer(wl, steps, warmup, rank, world):
@@ -171,7 +235,7 @@ def measure_decode_layer(wl, steps, warmup, rank, world):
     T, d, f = wl.T, wl.d, wl.f
     wts = alloc_and_fill(wl, n_layers=L)
     h = create_handle(wl, wts, max_tokens=max(T, 1), n_layers=L, prenorm=False)
-    fused = T <= capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, 4)  # the library default
+    fused = T <= capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, -1)  # the library default
     x_np = inputs.gen_activations(wl.seed, T, d, wl.act)
     x = torch.from_numpy(x_np.view(np.int16).copy()).cuda().view(torch.bfloat16)
     y = torch.empty_like(x)
@@ -238,10 +302,12 @@ def measure_decode_layer(wl, steps, warmup, rank, world):
     layer_us = ms_step * 1e3 / L
     router_bytes = wl.E * d * 4
     if fused:
-        # one kernel per layer: its event-timed duration is the "route" stage (the others are empty)
-        kname, ksrc, kbytes, kms = ("decode_layer_kernel (one-launch decode layer)", "decode_fused.cu",
-                                    bytes_layer, ms_route)
-        stages = {"one_launch_layer": ms_route * 1e3}
+        # one kernel per layer and nothing else in the step: the kernel's average duration inside the
+        # timed step is the step time over the 48 launches (programmatic dependent launch overlaps a
+        # launch's prologue with the previous one's tail, which the step time includes exactly once)
+        kname, ksrc, kbytes, kms = ("decode_layer_kernel (one-launch decode layer)", "decode_layer.cu",
+                                    bytes_layer, t_max / steps / L)
+        stages = {"one_launch_layer_event_bracketed": ms_route * 1e3}
         launches = steps * L
     else:
         kname, ksrc, kbytes, kms = ("gu_int4_kernel (expert gate/up GEMV + SwiGLU)", "experts_gemv.cu", bytes_gu,
@@ -262,7 +328,10 @@ def measure_decode_layer(wl, steps, warmup, rank, world):
                      "algorithmic_bytes_rule": "distinct selected experts + shared expert (int4 codes + fp16 "
                                                "scales) + activations in and out",
                      "router_bytes_not_counted": router_bytes,
-                     "avg_launch_us": kms * 1e3, "peak_source": f"{src} hbm_gbs (copy bandwidth)"},
+                     "avg_launch_us": kms * 1e3,
+                     "avg_launch_source": ("step time / launches (the kernel is the only launch of a layer)"
+                                           if fused else "CUDA events around the kernel in a timing pass"),
+                     "peak_source": f"{src} hbm_gbs (copy bandwidth)"},
         "layer": {"us_per_layer": layer_us, "algorithmic_bytes": bytes_layer,
                   "hbm_frac_of_" + src: bytes_layer / (layer_us * 1e-6) / 1e9 / hbm,
                   "stage_us": stages,
@@ -398,6 +467,104 @@ def measure_stack(wl, steps, warmup):
                                            "max": int(counts.max())}}
 
 
+def _time_decode_graph(h, x, T, L, reps, warmup):
+    """One CUDA graph of L layer calls with T tokens; returns ms per replay (median of reps)."""
+    import torch
+    from routed_expert_ffn_07_b300 import capi
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for l in range(L):
+            capi.moe_layer_forward(h, l, x, T, y, s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for l in range(L):
+            capi.moe_layer_forward(h, l, x, T, y, torch.cuda.current_stream().cuda_stream)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    del g
+    assert capi.moe_get_device_status(h) == 0
+    return float(np.median(times))
+
+
+def run_sweep(args):
+    """T sweep of the decode/verify layer on each expert path (one-launch layer, split-K GEMV,
+    grouped tensor-core GEMM) over 48 distinct layers, and the prefill chunk sweep on the tensor-core
+    path.  One JSON line (not a bench line)."""
+    import torch
+    from routed_expert_ffn_07_b300 import capi, inputs
+    from routed_expert_ffn_07_b300.workloads import WORKLOADS, alloc_and_fill, create_handle, expert_bytes
+    pk, src = peaks()
+    hbm, tf = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
+    out = {"peaks": {"hbm_gbs": hbm, "bf16_tflops": tf, "source": src}, "decode": [], "prefill": []}
+    wl = WORKLOADS[2]
+    L = 48
+    wts = alloc_and_fill(wl, n_layers=L)
+    h = create_handle(wl, wts, max_tokens=64, n_layers=L, prenorm=False)
+    paths = {"one_launch": (16, 16), "gemv": (0, 16), "tensor_core": (0, 0)}
+    for T in (1, 2, 4, 8, 16, 32, 64):
+        x = torch.from_numpy(inputs.gen_activations(wl.seed, T, wl.d, "bf16", layer=3).view(np.int16).copy()) \
+            .cuda().view(torch.bfloat16)
+        for path, (fz, gv) in paths.items():
+            if path != "tensor_core" and T > 16:
+                continue
+            capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, fz)
+            capi.moe_set_option(h, capi.MOE_OPT_GEMV_MAX_TOKENS, gv)
+            ms = _time_decode_graph(h, x, T, L, reps=7, warmup=3)
+            counts = capi.moe_get_active_counts(h, L)
+            byts = float(np.mean(counts + 1)) * expert_bytes(wl.d, wl.f) + 2 * T * wl.d * 2
+            us = ms * 1e3 / L
+            out["decode"].append({"T": T, "path": path, "us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
+                                  "distinct_experts": float(np.mean(counts)), "gb_per_s": byts / us / 1e3,
+                                  "hbm_frac": byts / us / 1e3 / hbm})
+            print(json.dumps(out["decode"][-1]), flush=True)
+    capi.moe_destroy(h)
+    del wts
+    torch.cuda.empty_cache()
+    wl = WORKLOADS[4]
+    wts = alloc_and_fill(wl)
+    Tmax = 16384
+    h = create_handle(wl, wts, max_tokens=Tmax)
+    x_all = torch.from_numpy(inputs.gen_activations(wl.seed, Tmax, wl.d, "bf16").view(np.int16).copy()) \
+        .cuda().view(torch.bfloat16)
+    for T in (512, 1024, 2048, 4096, 8192, 16384):
+        x = x_all[:T].contiguous()
+        y = torch.empty_like(x)
+        for _ in range(3):
+            capi.moe_layer_forward(h, 0, x, T, y)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            capi.moe_layer_forward(h, 0, x, T, y)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = float(np.median(times))
+        flops = 2.0 * (T * wl.K + T) * 3 * wl.d * wl.f
+        n_act = int(capi.moe_get_active_counts(h, 1)[0])
+        out["prefill"].append({"T": T, "ms_per_layer": ms, "tokens_per_s": T / (ms * 1e-3),
+                               "tflops": flops / (ms * 1e-3) / 1e12, "tensor_frac_layer": flops / (ms * 1e-3) / 1e12 / tf,
+                               "distinct_experts": n_act,
+                               "weights_gb_per_s": (n_act + 1) * expert_bytes(wl.d, wl.f) / (ms * 1e-3) / 1e9})
+        print(json.dumps(out["prefill"][-1]), flush=True)
+    assert capi.moe_get_device_status(h) == 0
+    capi.moe_destroy(h)
+    print(json.dumps({"sweep": out}), flush=True)
+
+
 def run_ours(args):
     rank, world, local = dist_init(args.gpus)
     import torch
@@ -440,6 +607,10 @@ def run_ours(args):
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(wl)
+        if not args.no_extras:
+            line["cpu_baseline"]["prefill_sample"] = cpu_baseline_prefill(WORKLOADS[4])
+            line["cpu_baseline"]["verify_stack_layer"] = cpu_baseline_stack_layer(WORKLOADS[3])
+            line["cpu_baseline"]["skewed_stack_layer"] = cpu_baseline_stack_layer(WORKLOADS[5])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -500,12 +671,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the prefill and stack workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="T sweep of the decode paths and prefill chunk sweep")
     ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
                     help="small case for ncu captures (not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.profile:
+    if args.sweep:
+        run_sweep(args)
+    elif args.profile:
         run_profile_case(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -19,8 +19,10 @@
  *   FFN_e(x) = W_down,e ( silu(W_gate,e x) * (W_up,e x) ),  silu(z) = z / (1 + exp(-z))
  *   y[t] = sum_{k=0..K-1} w[t,k] FFN_{idx[t,k]}(x[t])  (+ FFN_shared(x[t]) with weight 1),
  *   summed in fp32 in a fixed order and rounded once to the output type (the GEMV and prefill
- *   paths: ascending k, the shared expert last; the one-launch decode layer: the routing weights
- *   are folded into the down operand and the per-SM partial outputs are summed in SM order).
+ *   paths: ascending k, the shared expert last; the one-launch decode layer: the routing weight
+ *   is folded into h, each output row is owned by one CTA which sums the slots in slot order,
+ *   the shared expert first, then the distinct experts ascending, and its warps' partial sums in
+ *   warp order).
  *
  * Conventions (all entry points):
  *   - Pointers are DEVICE pointers owned by the caller unless a parameter says "host".
@@ -29,11 +31,9 @@
  *     moe_get_device_status and the *_host entry points.
  *   - Arguments are validated before anything is launched; on error nothing is launched and an
  *     error status is returned.  Status codes are returned, never printed.
- *   - The library allocates device memory in moe_create (workspace sized for max_tokens) and, when
- *     the one-launch decode layer serves the config (INT4, d % 512 == 0, d <= 2048, f % 32 == 0,
- *     f <= 1024), in moe_set_layer: a per-layer copy of that layer's expert weights in the
- *     one-launch layer's own fragment order (the same number of bytes as the layer's gate/up and
- *     down planes and scales).  Everything is freed in moe_destroy.
+ *   - The library allocates device memory only in moe_create (one workspace sized for
+ *     max_tokens) and frees it in moe_destroy.  Every kernel reads the caller's weight planes
+ *     where they are; there is no second copy of any weight.
  *   - A handle is not thread-safe, and calls made with one handle on different streams that
  *     overlap in time race on its workspace.
  *
@@ -109,12 +109,13 @@ typedef struct {
 moe_status moe_create(const moe_config* cfg, moe_handle* out);
 
 /* Register the weights of layer `layer` (0 <= layer < n_layers).  Stores the pointers (the memory
- * must stay valid while the handle uses it) and, when the one-launch decode layer serves the
- * config, writes the layer's expert copy in that layer's fragment order: the weights must hold
- * their final values when this is called (it synchronises the device before reading them and
- * the default stream after writing), and a layer whose weights change must be registered again.
- * Pointers are checked for NULL (scales only for INT4, shared planes only with has_shared) and
- * 16-byte alignment; MOE_ERR_OOM if the copy cannot be allocated. */
+ * must stay valid while the handle uses it) and encodes, in host memory, the TMA descriptors of
+ * the layer's planes for the tensor-core paths.  It neither allocates device memory, launches,
+ * copies nor synchronises, so the weights may be written before or after this call (before the
+ * first forward that uses them); a layer whose planes MOVE must be registered again.  Pointers
+ * are checked for NULL (scales only for INT4, shared planes only with has_shared) and 16-byte
+ * alignment; MOE_ERR_INVALID_ARG if a descriptor cannot be encoded, MOE_ERR_OOM if the host
+ * memory for the descriptors cannot be had. */
 moe_status moe_set_layer(moe_handle h, int layer, const moe_layer_weights* w);
 
 /* Router + top-K + dispatch of one layer for T tokens (1 <= T <= max_tokens):
@@ -184,6 +185,13 @@ moe_status moe_get_device_status(moe_handle h, void* stream);
 /* Free the workspace and any captured graphs.  Synchronises the device first. */
 moe_status moe_destroy(moe_handle h);
 
+/* Test hook (host-side fault injection): ORs `bits` (1 = a failed device-side check, 2 = a wait that
+ * gave up) into the handle's device status word, exactly as a kernel that hit the condition would.
+ * Synchronises `stream`.  A one-launch decode layer that finds the timeout bit set gives up at once
+ * and writes NaN to y, until moe_get_device_status has reported the status and reset the layer's
+ * launch state; nothing on the device faults or hangs. */
+moe_status moe_inject_device_status(moe_handle h, unsigned bits, void* stream);
+
 /* Self-test of the device-side bounded waits that every layer kernel uses (no model data, no
  * handle).  One small kernel waits on an mbarrier nobody arrives at and polls a counter nobody
  * bumps, each with a budget of `budget_cycles` SM clocks (1000 .. 2e9).  Returns MOE_ERR_TIMEOUT
@@ -193,7 +201,7 @@ moe_status moe_destroy(moe_handle h);
 moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream);
 
 /* Options (each returns the value in effect, or a negative moe_status on error; changing one
- * drops the handle's captured stack graphs).
+ * drops the handle's captured stack graphs; value -1 only queries the value in effect).
  * MOE_OPT_FUSED_MAX_TOKENS: calls with T <= value run the whole layer (router, selection,
  *   dispatch, experts on tensor cores, combine) as one kernel of one CTA per SM with grid-wide
  *   barriers (value 0..8, 0 = off; default 4; INT4 weights with d % 512 == 0, d <= 2048,

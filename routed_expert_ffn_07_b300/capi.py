@@ -72,6 +72,7 @@ def _load():
         "moe_route_noalloc": ([vp, vp, vp, ci, ci, ci, ci, ci, i32p, vp, i32p, i32p, vp], ci),
         "moe_set_option": ([vp, ci, ci], ci),
         "moe_selftest_bounded_waits": ([ctypes.c_longlong, vp], ci),
+        "moe_inject_device_status": ([vp, ctypes.c_uint, vp], ci),
         "moe_timing_enable": ([vp, ci], ci),
         "moe_timing_rewind": ([vp], ci),
         "moe_timing_read": ([vp, vp, ci, ctypes.POINTER(ci), vp], ci),
@@ -198,6 +199,11 @@ def moe_get_device_status(h, stream=None):
 
 def moe_destroy(h):
     _check("moe_destroy", lib.moe_destroy(h))
+
+
+def moe_inject_device_status(h, bits, stream=None):
+    """Test hook: OR `bits` into the handle's device status word (see include/moe.h)."""
+    _check("moe_inject_device_status", lib.moe_inject_device_status(h, bits, _stream(stream)))
 
 
 def moe_selftest_bounded_waits(budget_cycles=2_000_000, stream=None):

@@ -650,6 +650,18 @@ moe_status moe_get_device_status(moe_handle h, void* stream) {
   return MOE_OK;
 }
 
+moe_status moe_inject_device_status(moe_handle h, unsigned bits, void* stream) {
+  if (!h || bits == 0 || (bits & ~(kStatusBadIndex | kStatusTimeout))) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  CUDA_TRY(cudaMemcpyAsync(&v, h->status, 4, cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  v |= bits;
+  CUDA_TRY(cudaMemcpyAsync(h->status, &v, 4, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
 moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream) {
   if (budget_cycles < 1000 || budget_cycles > 2000000000ll) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -681,6 +693,12 @@ moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream) {
 
 int moe_set_option(moe_handle h, int option, int value) {
   if (!h) return -(int)MOE_ERR_INVALID_ARG;
+  if (value == -1) {  // query
+    if (option == MOE_OPT_GEMV_MAX_TOKENS) return h->gemv_max_tokens;
+    if (option == MOE_OPT_FUSED_MAX_TOKENS) return h->fused_max_tokens;
+    if (option == MOE_OPT_KERNEL_TIMELINE) return h->timeline_on ? 1 : 0;
+    return -(int)MOE_ERR_INVALID_ARG;
+  }
   if (option == MOE_OPT_GEMV_MAX_TOKENS) {
     if (value < 0 || value > kSmallT) return -(int)MOE_ERR_INVALID_ARG;
     h->gemv_max_tokens = h->gemm_ok ? value : kSmallT;

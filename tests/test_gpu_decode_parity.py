@@ -443,3 +443,24 @@ def test_usage_histogram_counts_every_forward_exactly(decode_layer):
         assert not capi.moe_usage_read(h, L, E).any()
     finally:
         capi.moe_usage_enable(h, False)
+
+
+def test_one_launch_layer_gives_up_on_a_reported_timeout_and_recovers(decode_layer):
+    """Host-side fault injection: with the status word's timeout bit set (as a launch whose wait gave
+    up leaves it), the one-launch layer returns NaN instead of a silently wrong y, the status call
+    reports MOE_ERR_TIMEOUT and resets, and the next launch is correct again.  No GPU fault."""
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl, wts, h = decode_layer
+    assert capi.moe_set_option(h, capi.MOE_OPT_FUSED_MAX_TOKENS, -1) >= 1
+    x_np = inputs.gen_activations(wl.seed, 1, wl.d, "bf16", layer=21)
+    x = to_torch_act(x_np)
+    y = torch.zeros_like(x)
+    capi.moe_inject_device_status(h, 2)
+    capi.moe_layer_forward(h, 0, x, 1, y)
+    capi.moe_layer_forward(h, 1, x, 1, y)   # still refused: the status has not been read yet
+    torch.cuda.synchronize()
+    assert torch.isnan(y.float()).all()
+    assert capi.moe_get_device_status(h) == 5  # MOE_ERR_TIMEOUT, then cleared
+    assert capi.moe_get_device_status(h) == 0
+    run_layer(h, wl, wts, x_np, 1, layer=0, gen_layer=0)
