@@ -193,8 +193,8 @@ moe_status moe_destroy(moe_handle h);
 moe_status moe_inject_device_status(moe_handle h, unsigned bits, void* stream);
 
 /* Self-test of the device-side bounded waits that every layer kernel uses (no model data, no
- * handle).  One small kernel waits on an mbarrier nobody arrives at and polls a counter nobody
- * bumps, each with a budget of `budget_cycles` SM clocks (1000 .. 2e9).  Returns MOE_ERR_TIMEOUT
+ * handle).  One small kernel waits on an mbarrier nobody arrives at and polls a word for an epoch
+ * tag nobody writes, each with a budget of `budget_cycles` SM clocks (1000 .. 2e9).  Returns MOE_ERR_TIMEOUT
  * when both waits gave up and recorded "timeout" (the expected outcome), MOE_ERR_DEVICE if a wait
  * reported success, MOE_ERR_CUDA on a CUDA error.  Synchronises `stream`; the GPU context stays
  * usable afterwards. */

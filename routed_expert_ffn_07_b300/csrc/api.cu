@@ -30,8 +30,8 @@ size_t decode_maps_bytes();
 cudaError_t decode_build_maps(void* maps, int E, int d, int f, int nsm, int has_shared, const void* gu_q,
                               const void* gu_s, const void* dn_q, const void* dn_s, const void* sh_gu_q,
                               const void* sh_gu_s, const void* sh_dn_q, const void* sh_dn_s);
-cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const void* maps, __half* hw,
-                                unsigned* ready, unsigned long long* lgt, unsigned long long* launches, int nsm,
+cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const void* maps, unsigned long long* hw,
+                                unsigned long long* lgt, unsigned long long* launches, int nsm,
                                 unsigned long long* timeline, cudaStream_t st);
 int decode_timeline_events();
 size_t gemm_workspace_bytes(int max_tokens, int d, int f, int E, int K);
@@ -49,7 +49,6 @@ constexpr int kDispatchBlockHost = 256;
 constexpr int kTimingEvents = 5;  // before route, after route, after stage A, after stage B, end
 constexpr int kFusedMaxTokensHost = 16;   // the one-launch decode layer's limit
 constexpr int kFusedDefaultTokens = 16;   // decode, 1 + 3 verify and small concurrent batches
-constexpr int kReadyCounters = 2 * 1024;  // the one-launch layer's per-slot counters (two launch parities)
 }  // namespace moe
 
 using namespace moe;
@@ -98,8 +97,8 @@ struct moe_ctx {
   unsigned long long* lgt = nullptr;  // the one-launch decode layer's published logits [16][E] (epoch-tagged)
   unsigned long long* launches = nullptr;  // and its launch counter (one per CTA per launch)
   bool fused_capable = false;    // the one-launch decode layer serves this config (T = 1 at least)
-  __half* hw = nullptr;          // its gate/up results [T + T*K][f] fp16 (T <= 16)
-  unsigned* ready = nullptr;     // its per-slot ready counters
+  unsigned long long* hw = nullptr;  // its gate/up results [T + T*K][f/2], epoch-tagged fp16 pairs (T <= 16)
+  size_t hw_bytes = 0;
   unsigned long long* timeline = nullptr;  // its in-kernel timeline [#SM][events] (ns)
   bool timeline_on = false;
   unsigned long long* usage = nullptr;  // per-layer expert usage histogram [n_layers][E]
@@ -231,8 +230,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   sz.push_back(up256((size_t)T * d * as));                // host x
   sz.push_back(up256((size_t)T * d * as));                // host y
   const int TF = T < kFusedMaxTokensHost ? T : kFusedMaxTokensHost;
-  sz.push_back(h->fused_capable ? up256((size_t)(TF + TF * K) * f * 2) : 0);   // one-launch gate/up results
-  sz.push_back(h->fused_capable ? up256((size_t)kReadyCounters * 4) : 0);     // its per-slot counters
+  sz.push_back(h->fused_capable ? up256((size_t)(TF + TF * K) * f * 4) : 0);   // one-launch gate/up results
   sz.push_back(h->fused_capable ? up256((size_t)kFusedMaxTokensHost * E * 8) : 0);  // its published logits
   sz.push_back(h->fused_capable ? up256((size_t)h->num_sms * decode_timeline_events() * 8) : 0);  // its timeline
   sz.push_back(up256((size_t)c.n_layers * E * 8));        // usage histogram
@@ -266,8 +264,9 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   h->stack_x = p; p += sz[i++];
   h->host_x = p; p += sz[i++];
   h->host_y = p; p += sz[i++];
-  h->hw = sz[i] ? reinterpret_cast<__half*>(p) : nullptr; p += sz[i++];
-  h->ready = sz[i] ? reinterpret_cast<unsigned*>(p) : nullptr; p += sz[i++];
+  h->hw = sz[i] ? reinterpret_cast<unsigned long long*>(p) : nullptr;
+  h->hw_bytes = sz[i];
+  p += sz[i++];
   h->lgt = sz[i] ? reinterpret_cast<unsigned long long*>(p) : nullptr; p += sz[i++];
   h->timeline = sz[i] ? reinterpret_cast<unsigned long long*>(p) : nullptr; p += sz[i++];
   h->usage = reinterpret_cast<unsigned long long*>(p); p += sz[i++];
@@ -414,7 +413,7 @@ static cudaError_t enqueue_layer(moe_ctx* h, int layer, const void* x, int T, vo
   if (T <= h->fused_max_tokens && h->layers[layer].dmaps) {
     // one launch for the whole layer; its stages are not separated (all of it counts as "route")
     ExpertArgs ea = make_expert_args(h, layer, x, T, y, resid);
-    e = launch_decode_layer(ra, ea, h->layers[layer].dmaps, h->hw, h->ready, h->lgt, h->launches, h->num_sms,
+    e = launch_decode_layer(ra, ea, h->layers[layer].dmaps, h->hw, h->lgt, h->launches, h->num_sms,
                             h->timeline_on ? h->timeline : nullptr, st);
     if (e != cudaSuccess) return e;
     for (int k = 1; ev && k < kTimingEvents; ++k)
@@ -639,11 +638,11 @@ moe_status moe_get_device_status(moe_handle h, void* stream) {
   CUDA_TRY(cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
   if (v) CUDA_TRY(cudaMemset(h->status, 0, 4));
   if (v & kStatusTimeout) {
-    // the one-launch layer's per-slot counters may hold partial sums and its published logits a
-    // stale epoch: start the next launch from zero
+    // the one-launch layer restarts its epochs from 1: clear the epoch-tagged logits and h words,
+    // whose old tags could otherwise match a new epoch
     CUDA_TRY(cudaMemset(h->launches, 0, 8));
-    if (h->ready) CUDA_TRY(cudaMemset(h->ready, 0, (size_t)kReadyCounters * 4));
     if (h->lgt) CUDA_TRY(cudaMemset(h->lgt, 0, (size_t)kFusedMaxTokensHost * h->cfg.n_experts * 8));
+    if (h->hw) CUDA_TRY(cudaMemset(h->hw, 0, h->hw_bytes));
     return MOE_ERR_TIMEOUT;
   }
   if (v) return MOE_ERR_DEVICE;

@@ -6,29 +6,34 @@
 // ('Strata はなぜ少ない VRAM でも速いのか' (modeldock.net), section '1 トークン、三者の分担';
 // verifying 1 + 3 drafted tokens adds only the experts the drafts pick, section
 // '予測してから検証する').  With every expert in HBM what remains besides those bytes is the chain
-// router -> selection -> experts -> combine, so it runs in one kernel of one CTA per SM:
+// router -> selection -> experts -> combine, so it runs in one kernel of one CTA per SM (16
+// consumer warps in 4 teams of 4, one producer warp that issues the TMA copies):
 //
 //   prologue  (may overlap the previous kernel) the CTA's router rows and, when the CTA's first
 //             gate/up unit belongs to the shared expert, that unit start streaming in;
 //   phase 1   x (optionally RMS-normalised) becomes fp16 tensor-core fragments in shared memory;
-//             the CTA scores its E / #CTA experts for all T tokens and stores the logits;
-//             [grid barrier]
-//   phase 2   every CTA reads all logits and repeats the selection and the dispatch (identical,
-//             deterministic); CTA 0 publishes them;
+//             the CTA scores its E / #CTA experts for all T tokens and publishes every logit as
+//             one 64-bit word (launch epoch << 32 | order-preserving key);
+//   phase 2   every CTA reads all T x E words, re-reading those whose tag is not yet this launch's,
+//             and repeats the selection and the dispatch (identical, deterministic); CTA 0
+//             publishes them;
 //   phase 3   gate/up.  The slots (the shared expert first, then the distinct routed experts in
 //             ascending order) are cut into units of 8 columns of f; unit g goes to CTA g mod
 //             #CTA.  A unit (8 gate + 8 up rows x d) arrives as one 128-byte-swizzled TMA box plus
 //             its scales; a team of 4 warps runs it as m16n8k16 tensor-core tiles (N = the slot's
-//             tokens), sums its 4 warps' partial tiles in a fixed order, and writes
-//             h = w silu(gate) up (fp16, routing weight folded in) for its 8 columns to global
-//             memory, then bumps the slot's ready counter (release);
+//             tokens), sums its 4 warps' partial tiles in a fixed order, and publishes
+//             h = w silu(gate) up (fp16, routing weight folded in) for its 8 columns as 64-bit
+//             words (launch epoch << 32 | two fp16), one strong store each;
 //   phase 4   down.  CTA c owns output rows [d c / #CTA, d (c + 1) / #CTA).  For every slot in
-//             order the producer waits until the slot's counter shows all its units done
-//             (acquire), then streams the slot's down rows of those outputs (TMA) and the slot's
-//             h rows (bulk copy); all 16 warps multiply them (N = all T tokens; a token that does
-//             not use the slot contributes zeros) into fp32 accumulators kept in registers across
-//             the slots.  The 16 warps' partial sums are added in warp order and the residual is
-//             added: y is written once, each element by one CTA.
+//             order the producer streams the slot's down rows of those outputs (TMA) as soon as a
+//             stage is free; a team copies the slot's h rows into the stage, re-reading words whose
+//             tag is not yet this launch's, and multiplies them (N = all T tokens; a token that
+//             does not use the slot contributes zeros) into fp32 accumulators kept in registers
+//             across the slots.  The 16 warps' partial sums are added in warp order and the
+//             residual is added: y is written once, each element by one CTA.
+//
+// Nothing waits on a counter or a grid barrier: a word's tag tells its reader that the word is this
+// launch's (a word is written and read as one single-copy-atomic access).
 //
 // Tensor-core operands: int4 codes become fp16 q exactly, x is fp16 (bf16 activations are exact in
 // fp16 inside its range) and w * h is rounded once to fp16; every 32-code group is summed in fp32
@@ -47,7 +52,7 @@
 namespace moe {
 
 constexpr int kDlWarps = 16;                     // consumer warps
-constexpr int kDlThreads = (kDlWarps + 2) * 32;  // + one producer warp + one flagger warp
+constexpr int kDlThreads = (kDlWarps + 1) * 32;  // + one producer warp
 constexpr int kDlTeams = 4;                      // gate/up teams
 constexpr int kDlTeamWarps = kDlWarps / kDlTeams;
 constexpr int kDlMaxT = 16;                      // tokens: two n8 tiles
@@ -56,10 +61,9 @@ constexpr int kDlSmemMax = 227 * 1024;
 constexpr int kDlStaticSlack = 12 * 1024;        // static shared memory, alignment and reserve
 constexpr int kDlRowsMax = 16;                   // down rows per CTA: one m16 tile
 constexpr int kDlUnit = 8;                       // f columns per gate/up unit
-constexpr unsigned kDlSpinLimit = 1u << 24;      // grid-barrier / ready-counter polls, >= 32 ns apart
+constexpr unsigned kDlSpinLimit = 1u << 24;      // polls of a tagged word, >= 32 ns apart
 constexpr unsigned kDlProducerSleep = 128;       // ns between polls of the producer's waits
 constexpr unsigned kDlConsumerSleep = 32;        // ns between polls of a waiting consumer warp
-constexpr int kDlReadyStride = 1024;             // per-slot ready counters per launch parity
 constexpr int kDlXPad = 4;                       // 16-byte blocks of padding per row of x fragments
 
 // TMA descriptors of one layer (routed planes, then the shared expert's).
@@ -94,8 +98,7 @@ struct DlArgs {
   int32_t* stat;
   int4* slots;
   unsigned long long* usage;
-  __half* hw;                    // [T (shared) + T*K][f]: w silu(g) u, fp16, 8-column blocks in fragment order
-  unsigned* ready;               // [2][kDlReadyStride] per-slot unit counters, one array per launch parity
+  unsigned long long* hw;        // [T (shared) + T*K][f/2]: (epoch << 32) | two fp16 of w silu(g) u, fragment order
   void* y;
   const void* resid;
   unsigned long long* lgt;       // [T][E] published logits: (launch epoch << 32) | order-preserving key
@@ -113,16 +116,16 @@ enum DlEvent {
   kEvStart = 0,        // kernel entered
   kEvDepWait,          // griddepcontrol.wait passed
   kEvLogits,           // logits stored
-  kEvBarrier,          // grid barrier passed (consumers learn it)
+  kEvReserved3,
   kEvRouted,           // selection and dispatch done
   kEvFirstUnit,        // first gate/up unit's bytes landed (team 0)
   kEvUnitsDone,        // all of the CTA's gate/up units done
-  kEvFirstDown,        // first down item's bytes landed
+  kEvFirstDown,        // first down item's weights landed
   kEvDownDone,         // all down items done
   kEvEnd,              // y written
   kEvLastUnitIssued,   // producer: last gate/up unit issued
-  kEvFirstDownIssued,  // producer: first down item issued
-  kEvLastDownIssued,   // producer: last down item issued
+  kEvFirstDownIssued,  // producer: first down item's weights issued
+  kEvLastDownIssued,   // producer: last down item's weights issued
   kEvFirstUnitIssued,  // producer: first gate/up unit issued after the routing
   kClkStart = 14,      // SM clock (clock64) at kernel entry
   kClkEnd = 15,        // SM clock when y is written
@@ -132,8 +135,13 @@ enum DlEvent {
   kEvSelected,         // top-K chosen
   kEvDispatched,       // dispatch done
   kEvProducerRouted,   // producer learned the routing
-  kEvLastDownWeights,  // producer: last down weights issued
-  kEvFirstH,           // producer: first h rows issued
+  kEvReserved22,
+  kEvFirstDownDone,    // first down item done (its h rows were complete)
+  kEvProducerGo,       // producer: routing broadcast to its warp, issue loop starts
+  kEvGatherStart,      // consumers start reading the published logits
+  kEvFirstRoutedLanded,  // first routed gate/up unit's bytes landed
+  kEvFirstRoutedDone,    // first routed gate/up unit's h published
+  kEvLastDownDone,       // the last slot's down item done
   kDlEvents = 32
 };
 __device__ __forceinline__ unsigned long long gtimer() {
@@ -150,11 +158,11 @@ __device__ __forceinline__ unsigned long long gtimer() {
     if (a.timeline) a.timeline[(size_t)blockIdx.x * kDlEvents + (ev)] = (unsigned long long)clock64(); \
   } while (0)
 
-// ------------------------------------------------------------------ grid barrier and counters
-__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
+// ------------------------------------------------------------------ epoch-tagged words
+// Two strong (relaxed, GPU scope) 64-bit loads as one vector access (each word single-copy atomic).
+__device__ __forceinline__ void ld_relaxed_gpu_v2(const unsigned long long* p, unsigned long long& a,
+                                                  unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 // Strong (relaxed, GPU scope) load: a poll of a word that another SM writes must be a strong
 // operation to be sure to see the new value.
@@ -166,35 +174,9 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long
 __device__ __forceinline__ void st_relaxed_gpu(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_gpu_u32(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Grid barrier on a 64-bit arrival counter that only ever increases.  At the start (after
-// griddepcontrol.wait) one thread per CTA reads the counter and rounds it down to a multiple of
-// gridDim.x: the previous launch's barrier is complete and fewer than gridDim.x arrivals of this
-// launch can precede the read, so every CTA gets the same base; the barrier is complete when the
-// counter reaches base + gridDim.x.  Arrival is a release reduction, the wait polls with acquire
-// loads (cumulative: the writes the CTA's other threads made before the CTA barrier that precedes
-// the arrival are released too).
-__device__ __forceinline__ void red_relaxed_gpu_u32(unsigned* p, unsigned v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ void st_release_cta(unsigned* p, unsigned v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(tc::smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(tc::smem_u32(p)) : "memory");
-  return v;
-}
 
-// Named barriers: 1 = the 512 consumer threads, 2 + team = the 128 threads of a gate/up team.
+// Named barriers: 1 = the 512 consumer threads, 2 + team = the 128 threads of a gate/up team,
+// 6 = the routing group (below).
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDlWarps * 32) : "memory"); }
 __device__ __forceinline__ bool consumers_all(bool v) {
   uint32_t r;
@@ -203,6 +185,18 @@ __device__ __forceinline__ bool consumers_all(bool v) {
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v), "n"(kDlWarps * 32)
+      : "memory");
+  return r != 0;
+}
+// Barrier 6: the routing group (the consumer threads [512 - n, 512)), n a multiple of 32.
+__device__ __forceinline__ void group_sync(int n) { asm volatile("bar.sync 6, %0;" ::"r"(n) : "memory"); }
+__device__ __forceinline__ bool group_all(int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 6, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(n)
       : "memory");
   return r != 0;
 }
@@ -278,73 +272,52 @@ __device__ __forceinline__ void mma_group(float (&dg)[4], uint32_t wa, uint32_t 
   mma_16816(dg, q_lo(wa >> 8), q_lo(wb >> 8), q_hi(wa >> 8), q_hi(wb >> 8), b.z, b.w);
 }
 
+__device__ __forceinline__ uint32_t max16(const uint32_t (&k)[16]) {  // a balanced tree
+  uint32_t m8[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m8[j] = max(k[2 * j], k[2 * j + 1]);
+  const uint32_t a = max(max(m8[0], m8[1]), max(m8[2], m8[3])), b = max(max(m8[4], m8[5]), max(m8[6], m8[7]));
+  return max(a, b);
+}
+
 // Top-K of one token by one warp from its keys in shared memory (key[e] = order-preserving key of
-// logit e, never 0; 0 past E; E <= 512): lane l holds keys l + 32 j in registers.  The K-th
-// largest of the 32 lane maxima is a lower bound of the K-th largest key (the K largest lane maxima
-// are K keys), so the keys at or above it hold the selection; when there are at most 64 of them,
-// each is ranked against the others (larger key, then lower expert) and rank k < K is the k-th
-// choice; otherwise (many equal logits) the K rounds of topk_warp decide.  Weights: exp(l - l_max)
-// renormalised over the K kept (the full softmax's normaliser cancels).  scratch: 96 uint2 of this
-// warp.  Lane k < K returns the k-th expert and its weight.
-__device__ __forceinline__ void topk_select_warp(uint32_t* key, int E, int K, uint2* scratch, int& my_i, float& my_w) {
+// logit e, never 0; 0 past E; E <= 512): lane l holds keys l + 32 j in registers and its maximum.
+// Round r takes the largest remaining key (a warp max-reduction) and, among the lanes holding it,
+// the lowest expert index (a min-reduction over each holder's lowest j), i.e. larger logit first,
+// ties to the lower expert; the holder clears it.  Weights: exp(l - l_max) renormalised over the K
+// kept (the full softmax's normaliser cancels).  Lane k < K returns the k-th expert and its weight.
+__device__ __forceinline__ void topk_select_warp(const uint32_t* key, int E, int K, int& my_i, float& my_w) {
   const int lane = threadIdx.x & 31;
   const int nj = (E + 31) >> 5;
   uint32_t k[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) k[j] = j < nj ? key[j * 32 + lane] : 0u;
-  uint32_t lm = 0u;
+  uint32_t lm = max16(k);
+  uint32_t my_key = 0u, top_key = 0u;
+  my_i = 0;
+#pragma unroll 1
+  for (int r = 0; r < K; ++r) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, lm);
+    uint32_t hit = 0u;  // bit j: k[j] holds the maximum (independent tests, an OR tree)
 #pragma unroll
-  for (int j = 0; j < 16; ++j) lm = max(lm, k[j]);
-  int rk = 0;  // rank of this lane's maximum among the lane maxima, ties to the lower lane
+    for (int j = 0; j < 16; ++j) hit |= (k[j] == mx ? 1u : 0u) << j;
+    const int jm = __ffs(hit) - 1;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, hit ? (uint32_t)(jm * 32 + lane) : 0xFFFFFFFFu);
+    if (r == 0) top_key = mx;
+    if (lane == r) {
+      my_key = mx;
+      my_i = (int)win;
+    }
+    if ((int)(win & 31u) == lane) {
 #pragma unroll
-  for (int l = 0; l < 32; ++l) {
-    const uint32_t o = __shfl_sync(0xffffffffu, lm, l);
-    rk += (o > lm) || (o == lm && l < lane);
-  }
-  const uint32_t tau = __reduce_max_sync(0xffffffffu, rk == K - 1 ? lm : 0u);
-  int cnt = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) cnt += (k[j] != 0u && k[j] >= tau);
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  const int total = __shfl_sync(0xffffffffu, incl, 31);
-  uint2* cand = scratch;        // [64]
-  uint2* sel = scratch + 64;    // [32]
-  if (total > 64) {
-    topk_warp(key, E, K, my_i, my_w);
-    return;
-  }
-  int pos = incl - cnt;
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (k[j] != 0u && k[j] >= tau) cand[pos++] = make_uint2(k[j], (uint32_t)(j * 32 + lane));
-  __syncwarp();
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int ci = lane + 32 * h;
-    if (ci < total) {
-      const uint2 me = cand[ci];
-      int rank = 0;
-#pragma unroll 4
-      for (int q = 0; q < total; ++q) {
-        const uint2 o = cand[q];
-        rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
-      }
-      if (rank < K) sel[rank] = me;
+      for (int j = 0; j < 16; ++j) k[j] = j == jm ? 0u : k[j];
+      lm = max16(k);
     }
   }
-  __syncwarp();
-  const uint2 mine = lane < K ? sel[lane] : make_uint2(0u, 0u);
-  const float top = topk_key_value(sel[0].x);
-  const float p = lane < K ? expf(topk_key_value(mine.x) - top) : 0.f;
+  const float top = topk_key_value(top_key);
+  const float p = lane < K ? expf(topk_key_value(my_key) - top) : 0.f;
   const float psum = warp_sum(p);
-  my_i = (int)mine.y;
   my_w = lane < K ? p / psum : 0.f;
-  __syncwarp();
 }
 
 // What a gate/up unit needs to know about the launch and the CTA (one copy in shared memory).
@@ -357,11 +330,12 @@ struct UnitCtx {
   const float* w_s;
   uint64_t* full;
   uint64_t* empty;
-  unsigned* s_done;       // per team: units finished (release / acquire, read by the flagger)
   volatile int* abort;
-  __half* hw;
+  unsigned long long* hw;   // [T + T*K][f/2] h, two fp16 columns per word under the launch's epoch tag
+  unsigned long long ep_tag;  // this launch's epoch << 32
   unsigned long long* timeline;
   int NS, SB, XS, CH, d, f, fu, T, K, HS, c, nc, gu_code_bytes;
+  int i0;  // the first routed unit's item index (timeline only)
   // down items
   const signed char* tpos;  // [slot][kDlMaxT] slot-local position of every token (-1: not in the slot)
   int RB, CHd, GF, dn_swap, dn_scale_off, dn_h_off;
@@ -369,15 +343,18 @@ struct UnitCtx {
 
 // One gate/up unit (item i of this CTA) by the 4 warps of team `team`: wait for its bytes, run its
 // 16 rows x d as m16n8k16 tiles over this warp's quarter of d, free the stage, sum the team's 4
-// partial tiles in warp order, write h = w silu(gate) up (fp16) for its 8 columns and tokens, and
-// hand the unit to the flagger.  Returns false when a wait gave up (uniform over the team).
+// partial tiles in warp order, and publish h = w silu(gate) up (fp16) of its 8 columns and tokens.
+// Returns false when a wait gave up (uniform over the team).
 template <int NT>
 __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, int lane) {
   const int g8 = lane >> 2, t4 = lane & 3;
   const int st = i % u.NS;
   const bool okw = tc::mbar_wait_warp(&u.full[st], (i / u.NS) & 1, u.abort, kDlConsumerSleep);
   if (!team_all(team, okw && !*u.abort)) return false;
-  if (i == 0 && tw == 0 && lane == 0 && u.timeline) u.timeline[(size_t)u.c * kDlEvents + kEvFirstUnit] = gtimer();
+  if (tw == 0 && lane == 0 && u.timeline) {
+    if (i == 0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstUnit] = gtimer();
+    if (i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstRoutedLanded] = gtimer();
+  }
   const int g = u.c + i * u.nc, s = g / u.fu, un = g - s * u.fu;
   int n_s, start = 0;
   if (s < u.HS) {
@@ -440,9 +417,11 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
   team_sync(team);
   // team thread (j, ln): column ln / 4 of the unit, slot-local tokens 8 j + 2 (ln % 4) (+ 1); the
-  // team's 4 partial tiles are summed in warp order
+  // team's 4 partial tiles are summed in warp order.  The words of h pair the unit's columns c and
+  // c + 4 (fragment positions 2c, 2c + 1); each is published under the launch's epoch tag with one
+  // strong store, so a reader that sees the tag sees the values.
   const int tt = tw * 32 + lane;
-  if (tt < NT * 32) {
+  if (tt < NT * 32) {  // whole warps
     const int j = tt >> 5, ln = tt & 31;
     const int col = ln >> 2, n0 = 8 * j + 2 * (ln & 3);
     float4 sum = u.pgu[((size_t)(team * kDlTeamWarps) * NT + j) * 32 + ln];
@@ -454,32 +433,37 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
       sum.z += pp.z;
       sum.w += pp.w;
     }
-    const int pos = 2 * (col & 3) + (col >> 2);  // fragment order of the 8 columns
+    float hv[2];
 #pragma unroll
     for (int o = 0; o < 2; ++o) {
       const int n = n0 + o;
-      if (n < n_s) {
-        const float gte = o ? sum.y : sum.x, upv = o ? sum.w : sum.z;
-        float wt = 1.f;
-        size_t row = (size_t)n;
-        if (s >= u.HS) {
-          wt = u.w_s[u.perm_s[start + n]];
-          row = (size_t)u.HS * u.T + start + n;
+      const float gte = o ? sum.y : sum.x, upv = o ? sum.w : sum.z;
+      const float wt = (s >= u.HS && n < n_s) ? u.w_s[u.perm_s[start + n]] : 1.f;
+      hv[o] = wt * (silu(gte) * upv);
+    }
+    const float hp0 = __shfl_xor_sync(0xffffffffu, hv[0], 16), hp1 = __shfl_xor_sync(0xffffffffu, hv[1], 16);
+    if (col < 4) {
+#pragma unroll
+      for (int o = 0; o < 2; ++o) {
+        const int n = n0 + o;
+        if (n < n_s) {
+          const size_t row = s < u.HS ? (size_t)n : (size_t)u.HS * u.T + start + n;
+          const uint32_t pair = pack_h2(o ? hv[1] : hv[0], o ? hp1 : hp0);
+          st_relaxed_gpu(u.hw + row * (u.f / 2) + 4 * un + col, u.ep_tag | pair);
         }
-        u.hw[row * u.f + 8 * un + pos] = __float2half_rn(wt * (silu(gte) * upv));
       }
     }
   }
-  team_sync(team);
-  // hand the unit to the flagger (which publishes it GPU-wide); after the team's stores
-  if (tw == 0 && lane == 0) st_release_cta(&u.s_done[team], (unsigned)((i - team) / kDlTeams + 1));
+  if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstRoutedDone] = gtimer();
   return true;
 }
 
 // One down item (slot s, item k of this CTA) by the 4 warps of team `team`: wait for the slot's down
-// rows of this CTA's outputs and its h rows, and add this warp's quarter of the slot's 32-column
-// groups into the warp's accumulators D (rows g / g + 8 of the CTA's output tile, all T tokens as N;
-// a token not in the slot contributes zeros); free the stage.  Returns false when the wait gave up.
+// rows of this CTA's outputs, copy the slot's h rows from their epoch-tagged words into the stage
+// (polling words whose tag is not yet this launch's), and add this warp's quarter of the slot's
+// 32-column groups into the warp's accumulators D (rows g / g + 8 of the CTA's output tile, all T
+// tokens as N; a token not in the slot contributes zeros); free the stage.  Returns false when a
+// wait gave up.
 template <int NT>
 __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int team, int tw, int lane,
                                           float (&D)[NT][4]) {
@@ -487,7 +471,62 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
   const int st = k % u.NS;
   const bool okw = tc::mbar_wait_warp(&u.full[st], (k / u.NS) & 1, u.abort, kDlConsumerSleep);
   if (!team_all(team, okw && !*u.abort)) return false;
-  const uint8_t* stg = u.ring + (size_t)st * u.SB;
+  uint8_t* stg = u.ring + (size_t)st * u.SB;
+  {
+    // the stage is this item's (its weights landed, so its previous item is done with it)
+    int n_s, hrow0;
+    if (s < u.HS) {
+      n_s = u.T;
+      hrow0 = 0;
+    } else {
+      const int4 sl = u.slot_s[s - u.HS];
+      n_s = sl.z;
+      hrow0 = u.HS * u.T + sl.y;
+    }
+    const unsigned ept = (unsigned)(u.ep_tag >> 32);
+    const unsigned long long* src = u.hw + (size_t)hrow0 * (u.f / 2);
+    uint2* hdst = reinterpret_cast<uint2*>(stg + u.dn_h_off);  // [n_s][f/4] pairs of words' payloads
+    const int npair = n_s * (u.f / 4), tt = tw * 32 + lane;
+    bool okh = true;
+#pragma unroll 1
+    for (int base = 0; okh && base < npair; base += 4 * kDlTeamWarps * 32) {
+      unsigned long long w[8];
+      int pending = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pi = base + tt + q * kDlTeamWarps * 32;
+        if (pi < npair)
+          ld_relaxed_gpu_v2(src + 2 * pi, w[2 * q], w[2 * q + 1]);
+        else
+          w[2 * q] = w[2 * q + 1] = u.ep_tag;
+        pending += ((unsigned)(w[2 * q] >> 32) != ept) + ((unsigned)(w[2 * q + 1] >> 32) != ept);
+      }
+      unsigned polls = 0;
+      while (pending) {
+        if (++polls > kDlSpinLimit || *u.abort) {
+          okh = false;
+          break;
+        }
+        __nanosleep(32);
+        pending = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int pi = base + tt + q * kDlTeamWarps * 32;
+          if ((unsigned)(w[2 * q] >> 32) != ept || (unsigned)(w[2 * q + 1] >> 32) != ept) {
+            ld_relaxed_gpu_v2(src + 2 * pi, w[2 * q], w[2 * q + 1]);
+            pending += ((unsigned)(w[2 * q] >> 32) != ept) + ((unsigned)(w[2 * q + 1] >> 32) != ept);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pi = base + tt + q * kDlTeamWarps * 32;
+        if (pi < npair) hdst[pi] = make_uint2((uint32_t)w[2 * q], (uint32_t)w[2 * q + 1]);
+      }
+    }
+    // (also the team barrier that makes the h rows visible to the team)
+    if (!team_all(team, okh && !*u.abort)) return false;
+  }
   const uint32_t sbase = tc::smem_u32(stg);
   const __half* dsc = reinterpret_cast<const __half*>(stg + u.dn_scale_off);  // [RB][GF]
   const uint4* hrows = reinterpret_cast<const uint4*>(stg + u.dn_h_off);     // [n_s][f/8]
@@ -570,10 +609,10 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
   __shared__ volatile int s_abort;
   __shared__ unsigned s_ep;
   __shared__ int s_nact, s_issued;
-  __shared__ unsigned s_par;
-  __shared__ unsigned s_done[kDlTeams];  // gate/up units finished per team (release / acquire)
   __shared__ float lpart[kDlWarps * kDlMaxT];
   __shared__ float inv_s[kDlMaxT];
+  __shared__ float bias_s[kDlRowsMax];                 // this CTA's router bias entries
+  __shared__ float resid_s[kDlMaxT * kDlRowsMax];      // the residual of this CTA's output rows
 
   // This launch may start while the previous kernel in the stream is still finishing
   // (programmatic dependent launch): before griddepcontrol.wait only this CTA's shared memory and
@@ -582,7 +621,6 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
   if (threadIdx.x == 0) {
     DL_STAMP(kEvStart);
     DL_CLOCK(kClkStart);
-    for (int q = 0; q < kDlTeams; ++q) s_done[q] = 0u;
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], kDlWarps);
@@ -600,7 +638,6 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     u.w_s = w_s;
     u.full = full;
     u.empty = empty;
-    u.s_done = s_done;
     u.abort = &s_abort;
     u.hw = a.hw;
     u.timeline = a.timeline;
@@ -617,6 +654,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     u.c = c;
     u.nc = nc;
     u.gu_code_bytes = gu_code_bytes;
+    u.i0 = (HS && c < fu) ? 1 : 0;
     u.tpos = tpos;
     u.RB = RB;
     u.CHd = CHd;
@@ -634,10 +672,10 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 
   if (warp == kDlWarps) {
     // ================================================================ producer
-    int k = 0;            // items issued
+    // The whole warp runs the control flow (converged: a lane that loops alone while the others
+    // wait at a warp-synchronous point runs far slower); lane 0 issues the copies.
+    const int k = first_is_shared ? 1 : 0;  // items issued before the routing is known
     bool ok = true;
-    unsigned par = 0;
-    int nact = 0;
     if (lane == 0) {
       // warm the routed experts' descriptors in the TMA unit: a small L2 prefetch through each (the
       // rows of expert 0 that this CTA would read; harmless if unused)
@@ -656,207 +694,101 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         tc::mbar_arrive_expect_tx(&full[0], (uint32_t)(gu_code_bytes + 2 * 8 * (d / 32) * 2));
         tc::tma_load_4d(ring, &m.sh_gu_q, 0, 8 * c, 0, 0, &full[0]);
         tc::tma_load_3d(ring + gu_code_bytes, &m.sh_gu_s, 0, 8 * c, 0, &full[0]);
-        k = 1;
         s_issued = 1;
       }
-      ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, 32);
-      par = s_par;
-      nact = ok ? s_nact : 0;
-      DL_STAMP(kEvProducerRouted);
     }
-    k = __shfl_sync(0xffffffffu, k, 0);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    par = __shfl_sync(0xffffffffu, par, 0);
-    nact = __shfl_sync(0xffffffffu, nact, 0);
+    __syncwarp();
+    ok = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, 32);
+    ok = __all_sync(0xffffffffu, ok);
+    const int nact = ok ? s_nact : 0;
+    if (lane == 0) DL_STAMP(kEvProducerRouted);
     const int nslots = HS + nact;
     const int total_units = nslots * fu;
     const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
-    unsigned* ready = a.ready + (size_t)par * kDlReadyStride;
-    // gate/up units: lane 0 alone, a tight loop (this warp shares its scheduler with busy consumer
-    // warps, so every instruction here is slow); a stage is waited for only once the ring wraps
-    if (lane == 0) {
+    if (lane == 0) DL_STAMP(kEvProducerGo);
+    // gate/up units in order; a stage is waited for only once the ring wraps
+    {
       const uint32_t gu_bytes = (uint32_t)(gu_code_bytes + 2 * 8 * (d / 32) * 2);
       int st = k % NS, ph = (k / NS) & 1;
-      int g = c + k * nc, s = g / fu, u = g - s * fu;
+      int g = c + k * nc, sl = g / fu, u = g - sl * fu;
       const int step_s = nc / fu, step_u = nc - step_s * fu;  // g += nc in (slot, unit) coordinates
       int i = k;
+#pragma unroll 1
       for (; i < nG; ++i) {
-        if (i >= NS && !tc::mbar_wait_sleepy(&empty[st], ph ^ 1u, &s_abort, kDlProducerSleep)) {
+        if (i >= NS && !__all_sync(0xffffffffu, tc::mbar_wait_sleepy(&empty[st], ph ^ 1u, &s_abort, kDlProducerSleep))) {
           ok = false;
           break;
         }
-        uint8_t* dst = ring + (size_t)st * SB;
-        tc::mbar_arrive_expect_tx(&full[st], gu_bytes);
-        if (s < HS) {
-          tc::tma_load_4d(dst, &m.sh_gu_q, 0, 8 * u, 0, 0, &full[st]);
-          tc::tma_load_3d(dst + gu_code_bytes, &m.sh_gu_s, 0, 8 * u, 0, &full[st]);
-        } else {
-          const int row = slot_s[s - HS].x * 2 * f + 8 * u;
-          tc::tma_load_4d(dst, &m.gu_q, 0, row, 0, 0, &full[st]);
-          tc::tma_load_3d(dst + gu_code_bytes, &m.gu_s, 0, row, 0, &full[st]);
+        if (lane == 0) {
+          uint8_t* dst = ring + (size_t)st * SB;
+          tc::mbar_arrive_expect_tx(&full[st], gu_bytes);
+          if (sl < HS) {
+            tc::tma_load_4d(dst, &m.sh_gu_q, 0, 8 * u, 0, 0, &full[st]);
+            tc::tma_load_3d(dst + gu_code_bytes, &m.sh_gu_s, 0, 8 * u, 0, &full[st]);
+          } else {
+            const int row = slot_s[sl - HS].x * 2 * f + 8 * u;
+            tc::tma_load_4d(dst, &m.gu_q, 0, row, 0, 0, &full[st]);
+            tc::tma_load_3d(dst + gu_code_bytes, &m.gu_s, 0, row, 0, &full[st]);
+          }
+          if (i == k) DL_STAMP(kEvFirstUnitIssued);
         }
-        if (i == k) DL_STAMP(kEvFirstUnitIssued);
         if (++st == NS) {
           st = 0;
           ph ^= 1;
         }
-        s += step_s;
+        sl += step_s;
         u += step_u;
         if (u >= fu) {
           u -= fu;
-          ++s;
+          ++sl;
         }
       }
-      s_issued = i;
-      DL_STAMP(kEvLastUnitIssued);
+      if (lane == 0) {
+        s_issued = i;
+        DL_STAMP(kEvLastUnitIssued);
+      }
     }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    // down items: the weights of slot s's down rows as soon as a ring stage is free (they depend
-    // only on the routing); the slot's h rows once its ready counter shows all its units done
-    // everywhere (one proxy fence per batch of newly ready slots: the h rows were written with
-    // ordinary stores and are read by the bulk copies)
+    __syncwarp();
+    // down items: the weights of slot s's down rows (this CTA's outputs) as soon as a ring stage is
+    // free; the slots' h rows are read by the teams themselves
     {
-      int nw = 0, nh = 0, known = 0;
-      unsigned polls = 0;
-      while (ok && nh < nslots) {
-        // as many down weights as there are free stages, back to back (lane 0 alone)
-        int nw_new = nw;
+      int q = 0;
+#pragma unroll 1
+      for (; ok && q < nslots; ++q) {
+        const int item = nG + q, st = item % NS;
+        if (item >= NS &&
+            !__all_sync(0xffffffffu, tc::mbar_wait_sleepy(&empty[st], ((item / NS) & 1) ^ 1u, &s_abort, kDlProducerSleep))) {
+          ok = false;
+          break;
+        }
         if (lane == 0) {
-          while (nw_new < nslots) {
-            const int item = nG + nw_new, st = item % NS;
-            if (!tc::mbar_try_wait(&empty[st], ((item / NS) & 1) ^ 1u)) break;
-            int n_s, drow;
-            const CUtensorMap *mq, *ms;
-            if (nw_new < HS) {
-              n_s = T;
-              mq = &m.sh_dn_q;
-              ms = &m.sh_dn_s;
-              drow = r0;
-            } else {
-              const int4 sl = slot_s[nw_new - HS];
-              n_s = sl.z;
-              mq = &m.dn_q;
-              ms = &m.dn_s;
-              drow = sl.x * d + r0;
-            }
-            uint8_t* dst = ring + (size_t)st * SB;
-            // the phase completes once the weights and, later, the h rows have landed
-            tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(dn_code_bytes + RB * GF * 2) + (uint32_t)n_s * f * 2);
-            if (a.dn_swap)
-              tc::tma_load_3d(dst, mq, 0, drow, 0, &full[st]);
-            else
-              tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
-            tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
-            ++nw_new;
+          const CUtensorMap *mq, *ms;
+          int drow;
+          if (q < HS) {
+            mq = &m.sh_dn_q;
+            ms = &m.sh_dn_s;
+            drow = r0;
+          } else {
+            mq = &m.dn_q;
+            ms = &m.dn_s;
+            drow = slot_s[q - HS].x * d + r0;
           }
-          if (nw_new == nslots && nw < nslots) DL_STAMP(kEvLastDownWeights);
-        }
-        nw_new = __shfl_sync(0xffffffffu, nw_new, 0);
-        bool progress = nw_new > nw;
-        nw = nw_new;
-        if (nh < nw) {
-          if (nh >= known) {
-            const int j = known + lane;
-            const bool r = j >= nslots || ld_acquire_gpu_u32(ready + j) >= (unsigned)fu;
-            const unsigned bal = __ballot_sync(0xffffffffu, r);
-            known += bal == 0xffffffffu ? 32 : __ffs(~bal) - 1;
-          }
-          __syncwarp();  // the acquires (by any lane) are ordered before lane 0's copies below
-          if (nh < known) {
-            const int hi = min(known, nw);
-            if (lane == 0) {
-              tc::fence_proxy_async_global();
-              if (nh == 0) DL_STAMP(kEvFirstH);
-              for (int q = nh; q < hi; ++q) {
-                const int item = nG + q, st = item % NS;
-                int n_s, hrow;
-                if (q < HS) {
-                  n_s = T;
-                  hrow = 0;
-                } else {
-                  const int4 sl = slot_s[q - HS];
-                  n_s = sl.z;
-                  hrow = HS * T + sl.y;
-                }
-                tc::bulk_g2s(ring + (size_t)st * SB + dn_h_off, a.hw + (size_t)hrow * f, (uint32_t)n_s * f * 2,
-                             &full[st]);
-                s_issued = item + 1;
-              }
-              if (hi == nslots) DL_STAMP(kEvLastDownIssued);
-              if (nh == 0) DL_STAMP(kEvFirstDownIssued);
-            }
-            nh = hi;
-            progress = true;
-          }
-        }
-        if (!progress) {
-          if (__any_sync(0xffffffffu, ++polls > kDlSpinLimit || s_abort)) ok = false;
-          __nanosleep(64);
-        } else {
-          polls = 0;
+          uint8_t* dst = ring + (size_t)st * SB;
+          tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(dn_code_bytes + RB * GF * 2));
+          if (a.dn_swap)
+            tc::tma_load_3d(dst, mq, 0, drow, 0, &full[st]);
+          else
+            tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
+          tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
+          if (q == 0) DL_STAMP(kEvFirstDownIssued);
+          if (q == nslots - 1) DL_STAMP(kEvLastDownIssued);
         }
       }
-      if (nh < nw && lane == 0) {
-        // giving up: complete the stages whose weights are in flight (their h rows are read as they
-        // are, in bounds) so that the exit can wait for every copy to land
-        for (int q = nh; q < nw; ++q) {
-          const int item = nG + q, st = item % NS;
-          const int n_s = q < HS ? T : slot_s[q - HS].z;
-          const int hrow = q < HS ? 0 : HS * T + slot_s[q - HS].y;
-          tc::bulk_g2s(ring + (size_t)st * SB + dn_h_off, a.hw + (size_t)hrow * f, (uint32_t)n_s * f * 2, &full[st]);
-        }
-        s_issued = nG + nw;
-      }
+      if (lane == 0) s_issued = nG + q;
     }
     if (!ok && lane == 0) {
       atomicOr(a.status, kStatusTimeout);
       s_abort = 1;
-    }
-    __syncwarp();
-  } else if (warp == kDlWarps + 1) {
-    // ================================================================ flagger
-    // Publishes this CTA's finished gate/up units to the whole GPU: per batch of units the teams
-    // have finished (acquired from s_done), one GPU-scope fence and a relaxed add per unit to its
-    // slot's ready counter (the release pattern), off the teams' critical path.  Team q finishes
-    // its units in the order q, q + 4, q + 8, ... of this CTA's unit list.
-    if (lane == 0) {
-      bool okf = tc::mbar_wait_sleepy(&route_ready, 0, &s_abort, 64);
-      const int nslots = HS + (okf ? s_nact : 0);
-      const int total_units = nslots * fu;
-      const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
-      unsigned* ready = a.ready + (size_t)s_par * kDlReadyStride;
-      unsigned rel[kDlTeams] = {0u, 0u, 0u, 0u};
-      int total = 0;
-      unsigned spins = 0;
-      while (okf && total < nG) {
-        unsigned got[kDlTeams];
-        int nnew = 0;
-#pragma unroll
-        for (int q = 0; q < kDlTeams; ++q) {
-          got[q] = ld_acquire_cta(&s_done[q]);
-          nnew += (int)(got[q] - rel[q]);
-        }
-        if (nnew == 0) {
-          if (++spins > kDlSpinLimit || s_abort) okf = false;
-          __nanosleep(32);
-          continue;
-        }
-        spins = 0;
-        fence_acq_rel_gpu();
-#pragma unroll
-        for (int q = 0; q < kDlTeams; ++q)
-          for (unsigned mm = rel[q]; mm < got[q]; ++mm) {
-            const int g = c + (q + kDlTeams * (int)mm) * nc;
-            red_relaxed_gpu_u32(ready + g / fu, 1u);
-          }
-#pragma unroll
-        for (int q = 0; q < kDlTeams; ++q) rel[q] = got[q];
-        total += nnew;
-      }
-      if (!okf && !s_abort) {
-        atomicOr(a.status, kStatusTimeout);
-        s_abort = 1;
-      }
     }
     __syncwarp();
   } else {
@@ -865,7 +797,11 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     const int team = warp / kDlTeamWarps, tw = warp % kDlTeamWarps;
     bool ok = true;
 
+    // the router bias rows are weights: read before the previous kernel has finished
+    if (a.bias && ctid < ne) bias_s[ctid] = __ldg(a.bias + e0 + ctid);
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are visible
+    // ctid 0 reads the launch state while the others load x; the barrier after the x staging
+    // publishes it
     if (ctid == 0) {
       DL_STAMP(kEvDepWait);
       // this launch's epoch: 1 + the number of complete launches.  Every CTA adds 1 to the counter
@@ -876,16 +812,8 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
       const unsigned ep = (unsigned)(__ldcg(a.launches) / (unsigned long long)nc) + 1u, stw = __ldcg(a.status);
       if (stw & kStatusTimeout) s_abort = 1;
       s_ep = ep;
-      s_par = ep & 1u;
+      uc_s.ep_tag = (unsigned long long)ep << 32;
     }
-    consumers_sync();
-    const unsigned lpar = s_par;  // this launch's ready counters: parity lpar
-    const unsigned long long ep_tag = (unsigned long long)s_ep << 32;
-    ok = !s_abort;
-    if (c == 0)
-      // zero the other parity's counters for the next launch (the previous launch, which used them,
-      // is complete: griddepcontrol.wait)
-      for (int i = ctid; i < kDlReadyStride; i += kDlWarps * 32) a.ready[(size_t)(lpar ^ 1u) * kDlReadyStride + i] = 0u;
 
     // ---- phase 1: x (optionally RMS-normalised) as fp16 fragments, then the logits
     if (a.prenorm) {
@@ -937,8 +865,16 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         xh[(size_t)ti * XS + b] =
             make_uint4(pack_h2(v[0], v[4]), pack_h2(v[1], v[5]), pack_h2(v[2], v[6]), pack_h2(v[3], v[7]));
       }
+      // the residual of this CTA's output rows, for the end
+      if (a.resid)
+        for (int i = ctid; i < T * nr; i += kDlWarps * 32) {
+          const int n = i / nr, r = i - n * nr;
+          resid_s[i] = load_act(a.resid, a.act, (size_t)n * d + r0 + r);
+        }
     }
     consumers_sync();
+    const unsigned long long ep_tag = (unsigned long long)s_ep << 32;
+    ok = !s_abort;
     if (ctid == 0) DL_STAMP(kEvXStaged);
     {
       // logits of the router rows [e0, e0 + ne): warp = (row, part of the columns), tokens 4 at a time
@@ -989,191 +925,202 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 #pragma unroll 1
           for (int p = 0; p < nparts; ++p) v += lpart[(p * ne + le) * kDlMaxT + t];
           // published as one 64-bit word (epoch, key): a reader sees both or neither
-          st_relaxed_gpu(a.lgt + (size_t)t * E + e0 + le, ep_tag | topk_order_key(v + (a.bias ? a.bias[e0 + le] : 0.f)));
+          st_relaxed_gpu(a.lgt + (size_t)t * E + e0 + le, ep_tag | topk_order_key(v + (a.bias ? bias_s[le] : 0.f)));
         }
       consumers_sync();
       if (ctid == 0) DL_STAMP(kEvLogits);
     }
 
     // ---- team 0 runs the shared expert's unit of this CTA (routing-independent) while the other
-    // CTAs publish their logits
-    if (first_is_shared && team == 0 && ok) ok = gu_unit<NT>(*uc, 0, 0, tw, lane);
-
-    // ---- phase 2: every CTA gathers all logits of this launch (polling their epoch tags), then
-    // repeats the selection and the dispatch
-    ok = consumers_all(ok && !s_abort);
-    if (ok) {
+    // teams (the routing group) gather the logits, select and dispatch; it joins them afterwards
+    const bool t0_busy = false;
+    const int gb = t0_busy ? kDlTeamWarps * 32 : 0;  // the routing group: threads [gb, 512)
+    const int gn = kDlWarps * 32 - gb;
+    if (t0_busy && team == 0) {
+      if (ok) ok = gu_unit<NT>(*uc, 0, 0, tw, lane);
+    } else {
+      // ---- phase 2: the routing group gathers all logits of this launch (polling their epoch
+      // tags), then repeats the selection and the dispatch
+      const int gt = ctid - gb, gw = gt >> 5, gnw = gn >> 5;
+      if (gt == 0) DL_STAMP(kEvGatherStart);
       const int EP = (E + 31) & ~31;
       uint32_t* keys = reinterpret_cast<uint32_t*>(scratch);  // [T][EP] order-preserving keys, 0 = none
-      {
-        // at most 16 words per thread (T * EP <= 8192), all loads in flight, then re-poll the stale
-        unsigned long long wv[16];
+      if (ok) {
+        // rounds of 8 words per thread, all loads of a round in flight, then re-poll the stale ones
         const unsigned ept = (unsigned)(ep_tag >> 32);
-        int pending = 0;
+#pragma unroll 1
+        for (int base = 0; ok && base < T * EP; base += 8 * gn) {
+          unsigned long long wv[8];
+          int pending = 0;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int i = ctid + q * kDlWarps * 32;
-          const int t = i / EP, e = i - t * EP;
-          wv[q] = (i < T * EP && e < E) ? ld_relaxed_gpu(a.lgt + (size_t)t * E + e) : ep_tag;
-        }
+          for (int q = 0; q < 8; ++q) {
+            const int i = base + gt + q * gn;
+            const int t = i / EP, e = i - t * EP;
+            wv[q] = (i < T * EP && e < E) ? ld_relaxed_gpu(a.lgt + (size_t)t * E + e) : ep_tag;
+          }
 #pragma unroll
-        for (int q = 0; q < 16; ++q) pending += (unsigned)(wv[q] >> 32) != ept;
-        unsigned polls = 0;
-        while (pending) {
-          if (++polls > kDlSpinLimit || s_abort) break;
-          __nanosleep(64);
-          pending = 0;
+          for (int q = 0; q < 8; ++q) pending += (unsigned)(wv[q] >> 32) != ept;
+          unsigned polls = 0;
+          while (pending) {
+            if (++polls > kDlSpinLimit || s_abort) break;
+            __nanosleep(64);
+            pending = 0;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            if ((unsigned)(wv[q] >> 32) != ept) {
-              const int i = ctid + q * kDlWarps * 32;
-              const int t = i / EP, e = i - t * EP;
-              wv[q] = ld_relaxed_gpu(a.lgt + (size_t)t * E + e);
-              pending += (unsigned)(wv[q] >> 32) != ept;
+            for (int q = 0; q < 8; ++q) {
+              if ((unsigned)(wv[q] >> 32) != ept) {
+                const int i = base + gt + q * gn;
+                const int t = i / EP, e = i - t * EP;
+                wv[q] = ld_relaxed_gpu(a.lgt + (size_t)t * E + e);
+                pending += (unsigned)(wv[q] >> 32) != ept;
+              }
             }
           }
-        }
-        ok = pending == 0;
+          ok = pending == 0;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int i = ctid + q * kDlWarps * 32;
-          if (i < T * EP) keys[i] = (i - (i / EP) * EP) < E ? (uint32_t)wv[q] : 0u;
+          for (int q = 0; q < 8; ++q) {
+            const int i = base + gt + q * gn;
+            if (i < T * EP) keys[i] = (i - (i / EP) * EP) < E ? (uint32_t)wv[q] : 0u;
+          }
         }
       }
       // the dispatch's expert bitmap and the slot-local position table start cleared
-      if (ctid < 32) s_bits[ctid] = 0u;
-      for (int i = ctid; i < HS + T * K; i += kDlWarps * 32)
+      if (gt < 32) s_bits[gt] = 0u;
+      for (int i = gt; i < HS + T * K; i += gn)
         reinterpret_cast<uint4*>(tpos)[i] = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-      ok = consumers_all(ok && !s_abort);
-      if (!ok && ctid == 0) {
+      ok = group_all(gn, ok && !s_abort);
+      if (!ok && gt == 0) {
         atomicOr(a.status, kStatusTimeout);
         s_abort = 1;
       }
-      if (ctid == 0) DL_STAMP(kEvKeys);
+      if (gt == 0) DL_STAMP(kEvKeys);
+      if (ok) {
+        // one warp per token
+#pragma unroll 1
+        for (int t = gw; t < T; t += gnw) {
+          int my_i;
+          float my_w;
+          if (E <= 512)
+            topk_select_warp(keys + (size_t)t * EP, E, K, my_i, my_w);
+          else
+            topk_warp(keys + (size_t)t * EP, E, K, my_i, my_w);
+          if (lane < K) {
+            idx_s[t * K + lane] = my_i;
+            w_s[t * K + lane] = my_w;
+            atomicOr(&s_bits[my_i >> 5], 1u << (my_i & 31));
+          }
+        }
+        group_sync(gn);
+        if (gt == 0) DL_STAMP(kEvSelected);
+        const int n = T * K;
+        if (n <= 32) {
+          // few assignments: one warp does the whole dispatch with shuffles.  Lane i = assignment i:
+          // its place in the stable counting sort (assignments with a smaller expert, plus the
+          // earlier ones with its expert), its slot (distinct experts below its own), its position in
+          // the slot.
+          if (gw == 0) {
+            const int e_i = lane < n ? idx_s[lane] : 0x7fffffff;
+            int start = 0, cnt_i = 0, before = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int ej = __shfl_sync(0xffffffffu, e_i, j);
+              start += ej < e_i;
+              cnt_i += ej == e_i;
+              before += ej == e_i && j < lane;
+            }
+            const bool first = lane < n && before == 0;
+            const unsigned fm = __ballot_sync(0xffffffffu, first);
+            int slot = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) slot += ((fm >> j) & 1u) && __shfl_sync(0xffffffffu, e_i, j) < e_i;
+            if (lane < n) {
+              perm_s[start + before] = lane;
+              if (first) slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
+              tpos[(HS + slot) * kDlMaxT + lane / K] = (signed char)before;
+            }
+            if (HS && lane < T) tpos[lane] = (signed char)lane;
+            if (lane == 0) s_nact = __popc(fm);
+          }
+        } else {
+          if (gw == 0) {
+            // slot of expert e = number of selected experts below e: per-word prefix of the bitmap
+            const uint32_t bw = s_bits[lane];
+            const int pc = __popc(bw);
+            int incl = pc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            s_bpre[lane] = incl - pc;
+            if (lane == 31) s_nact = incl;
+          }
+          group_sync(gn);
+#pragma unroll 1
+          for (int ai = gt; ai < n; ai += gn) {
+            // assignment ai: its place in the stable counting sort by expert, its slot, its position
+            // among the slot's tokens (tokens ascend with the assignment number)
+            const int e_i = idx_s[ai];
+            int start = 0, cnt_i = 0, before = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+              const int ej = idx_s[j];
+              start += ej < e_i;
+              cnt_i += ej == e_i;
+              before += ej == e_i && j < ai;
+            }
+            perm_s[start + before] = ai;
+            const int slot = s_bpre[e_i >> 5] + __popc(s_bits[e_i >> 5] & ((1u << (e_i & 31)) - 1u));
+            if (before == 0) slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
+            tpos[(HS + slot) * kDlMaxT + ai / K] = (signed char)before;
+          }
+          if (HS && gt < T) tpos[gt] = (signed char)gt;
+        }
+        // the keys are done with: the producer's bulk copies may overwrite them
+        tc::fence_proxy_async_smem();
+        group_sync(gn);
+        if (gt == 0) {
+          DL_STAMP(kEvDispatched);
+          DL_STAMP(kEvRouted);
+          tc::mbar_arrive(&route_ready);
+        }
+        if (c == 0) {
+          // the full outputs: idx, w; offs[e] = assignments with an expert below e
+          const int na = s_nact;
+#pragma unroll 1
+          for (int i = gt; i < n; i += gn) {
+            a.idx[i] = idx_s[i];
+            a.w[i] = w_s[i];
+            a.perm[i] = perm_s[i];
+          }
+#pragma unroll 1
+          for (int e = gt; e <= E; e += gn) {
+            int o = 0, ce = 0;
+#pragma unroll 4
+            for (int q = 0; q < n; ++q) {
+              o += idx_s[q] < e;
+              ce += idx_s[q] == e;
+            }
+            a.offs[e] = o;
+            if (e < E) a.counts[e] = ce;
+            if (e < E && ce && a.usage) a.usage[e] += (unsigned long long)ce;
+          }
+#pragma unroll 1
+          for (int q = gt; q < na; q += gn) {
+            a.active[q] = slot_s[q].x;
+            a.slots[q] = slot_s[q];
+          }
+          if (gt == 0) {
+            *a.n_active = na;
+            if (a.stat) *a.stat = na;
+          }
+        }
+      }
     }
-    if (ok) {
-      const int EP = (E + 31) & ~31;
-      uint32_t* keys = reinterpret_cast<uint32_t*>(scratch);
-      // one warp per token
-      if (warp < T) {
-        int my_i;
-        float my_w;
-        uint2* tk_scratch = reinterpret_cast<uint2*>(keys + (size_t)T * EP) + (size_t)warp * 96;
-        if (E <= 512)
-          topk_select_warp(keys + (size_t)warp * EP, E, K, tk_scratch, my_i, my_w);
-        else
-          topk_warp(keys + (size_t)warp * EP, E, K, my_i, my_w);
-        if (lane < K) {
-          idx_s[warp * K + lane] = my_i;
-          w_s[warp * K + lane] = my_w;
-          atomicOr(&s_bits[my_i >> 5], 1u << (my_i & 31));
-        }
-      }
-      consumers_sync();
-      if (ctid == 0) DL_STAMP(kEvSelected);
-      const int n = T * K;
-      if (n <= 32) {
-        // few assignments: one warp does the whole dispatch with shuffles.  Lane i = assignment i: its
-        // place in the stable counting sort (assignments with a smaller expert, plus the earlier ones
-        // with its expert), its slot (distinct experts below its own), its position in the slot.
-        if (warp == 0) {
-          const int e_i = lane < n ? idx_s[lane] : 0x7fffffff;
-          int start = 0, cnt_i = 0, before = 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int ej = __shfl_sync(0xffffffffu, e_i, j);
-            start += ej < e_i;
-            cnt_i += ej == e_i;
-            before += ej == e_i && j < lane;
-          }
-          const bool first = lane < n && before == 0;
-          const unsigned fm = __ballot_sync(0xffffffffu, first);
-          int slot = 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) slot += ((fm >> j) & 1u) && __shfl_sync(0xffffffffu, e_i, j) < e_i;
-          if (lane < n) {
-            perm_s[start + before] = lane;
-            if (first) slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
-            tpos[(HS + slot) * kDlMaxT + lane / K] = (signed char)before;
-          }
-          if (HS && lane < T) tpos[lane] = (signed char)lane;
-          if (lane == 0) s_nact = __popc(fm);
-        }
-      } else {
-      if (warp == 0) {
-        // slot of expert e = number of selected experts below e: per-word prefix of the bitmap
-        const uint32_t bw = s_bits[lane];
-        const int pc = __popc(bw);
-        int incl = pc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        s_bpre[lane] = incl - pc;
-        if (lane == 31) s_nact = incl;
-      }
-      consumers_sync();
-      if (ctid < n) {
-        // assignment ctid: its place in the stable counting sort by expert, its slot, its position
-        // among the slot's tokens (tokens ascend with the assignment number)
-        const int e_i = idx_s[ctid];
-        int start = 0, cnt_i = 0, before = 0;
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-          const int ej = idx_s[j];
-          start += ej < e_i;
-          cnt_i += ej == e_i;
-          before += ej == e_i && j < ctid;
-        }
-        perm_s[start + before] = ctid;
-        const int slot = s_bpre[e_i >> 5] + __popc(s_bits[e_i >> 5] & ((1u << (e_i & 31)) - 1u));
-        if (before == 0) slot_s[slot] = make_int4(e_i, start, cnt_i, 0);
-        tpos[(HS + slot) * kDlMaxT + ctid / K] = (signed char)before;
-      }
-      if (HS && ctid < T) tpos[ctid] = (signed char)ctid;
-      }
-      if (c == 0)
-#pragma unroll 1
-        for (int i = ctid; i < n; i += kDlWarps * 32) {
-          a.idx[i] = idx_s[i];
-          a.w[i] = w_s[i];
-        }
-      // the keys are done with: the producer's bulk copies may overwrite them
-      tc::fence_proxy_async_smem();
-      consumers_sync();
-      if (ctid == 0) {
-        DL_STAMP(kEvDispatched);
-        DL_STAMP(kEvRouted);
-        tc::mbar_arrive(&route_ready);
-      }
-      if (c == 0) {
-        // the full outputs: offs[e] = assignments with an expert below e
-        const int na = s_nact;
-#pragma unroll 1
-        for (int e = ctid; e <= E; e += kDlWarps * 32) {
-          int o = 0, ce = 0;
-#pragma unroll 4
-          for (int q = 0; q < n; ++q) {
-            o += idx_s[q] < e;
-            ce += idx_s[q] == e;
-          }
-          a.offs[e] = o;
-          if (e < E) a.counts[e] = ce;
-          if (e < E && ce && a.usage) a.usage[e] += (unsigned long long)ce;
-        }
-#pragma unroll 1
-        for (int q = ctid; q < na; q += kDlWarps * 32) {
-          a.active[q] = slot_s[q].x;
-          a.slots[q] = slot_s[q];
-        }
-#pragma unroll 1
-        for (int q = ctid; q < n; q += kDlWarps * 32) a.perm[q] = perm_s[q];
-        if (ctid == 0) {
-          *a.n_active = na;
-          if (a.stat) *a.stat = na;
-        }
-      }
+    // team 0 joins: the routing (or its failure) is known to all consumers
+    ok = consumers_all(ok && !s_abort);
+    if (!ok && ctid == 0) {
+      atomicOr(a.status, kStatusTimeout);
+      s_abort = 1;
     }
 
     const int nslots = HS + (ok ? s_nact : 0);
@@ -1187,13 +1134,17 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 #pragma unroll
     for (int j = 0; j < NT; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
 #pragma unroll 1
-    for (int k = team + (first_is_shared && team == 0 ? kDlTeams : 0); ok && k < nG + nslots; k += kDlTeams) {
+    for (int k = team; ok && k < nG + nslots; k += kDlTeams) {
       if (k < nG) {
         ok = gu_unit<NT>(*uc, k, team, tw, lane);
         if (k + kDlTeams >= nG && tw == 0 && lane == 0) DL_STAMP(kEvUnitsDone);  // this team's last unit
       } else {
         if (k - nG < kDlTeams && tw == 0 && lane == 0 && team == 0) DL_STAMP(kEvFirstDown);
         ok = down_item<NT>(*uc, k, k - nG, team, tw, lane, D);
+        if (tw == 0 && lane == 0) {
+          if (k == nG) DL_STAMP(kEvFirstDownDone);
+          if (k == nG + nslots - 1) DL_STAMP(kEvLastDownDone);
+        }
       }
     }
     ok = consumers_all(ok && !s_abort);
@@ -1217,7 +1168,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
       }
       const size_t o = (size_t)n * d + r0 + r;
       if (ok) {
-        if (a.resid) v = load_act(a.resid, a.act, o) + v;
+        if (a.resid) v = resid_s[n * nr + r] + v;
       } else {
         v = __int_as_float(0x7fc00000);  // NaN: this CTA gave up, its rows are not a result
       }
@@ -1246,10 +1197,10 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 }
 
 // ------------------------------------------------------------------ self-test of the bounded waits
-// One CTA: thread 0 waits on an mbarrier nobody arrives at and on a barrier counter nobody bumps,
-// each with a small budget, exactly as the layer kernels wait.  Bit 0 of *result: the mbarrier
-// wait gave up; bit 1: the counter wait gave up; bit 2: a wait returned success (a bug).
-__global__ void bounded_wait_selftest_kernel(unsigned long long* counter, long long budget, unsigned* result) {
+// One CTA: thread 0 waits on an mbarrier nobody arrives at and for a tag nobody writes on a word,
+// each with a small budget, exactly as the layer kernel waits.  Bit 0 of *result: the mbarrier
+// wait gave up; bit 1: the tagged-word wait gave up; bit 2: a wait returned success (a bug).
+__global__ void bounded_wait_selftest_kernel(unsigned long long* word, long long budget, unsigned* result) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ volatile int never;
   if (threadIdx.x == 0) {
@@ -1261,10 +1212,10 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long* counter, long l
   if (threadIdx.x == 0) {
     unsigned r = 0;
     if (!tc::mbar_wait(&bar, 0, &never, budget)) r |= 1u; else r |= 4u;
-    // the counter never reaches this target; the poll limit bounds the wait
-    const unsigned long long target = ld_acquire_gpu(counter) + (1ull << 40);
+    // the word never carries this tag (nothing writes it); the poll limit bounds the wait
+    const unsigned tag = (unsigned)(ld_relaxed_gpu(word) >> 32) + 1u;
     bool ok = true;
-    for (unsigned n = 0; ok && ld_acquire_gpu(counter) < target; ++n) {
+    for (unsigned n = 0; ok && (unsigned)(ld_relaxed_gpu(word) >> 32) != tag; ++n) {
       if (n > (unsigned)(budget >> 6)) ok = false;
       __nanosleep(32);
     }
@@ -1336,12 +1287,11 @@ bool decode_shape_ok(int T, int d, int f, int E, int K, int nsm) {
   if (nsm <= 0 || T < 1 || T > kDlMaxT) return false;
   if ((d != 1024 && d != 2048) || f % 256 || f > 2048 || E > kMaxE || K > kMaxK) return false;
   if (T * K > kDlWarps * 32 || E > 2 * kDlWarps * 32) return false;  // dispatch / selection thread maps
-  if (T * K + 1 > 1024) return false;                                 // ready counters
-  if (rows_box_for(d, nsm) > kDlRowsMax) return false;
+  if (rows_box_for(d, nsm) > kDlRowsMax || (E + nsm - 1) / nsm > kDlRowsMax) return false;
   const DlPlan p = dl_plan(T, d, f, E, K, nsm);
   if (p.ns < 3) return false;  // stage 0 (first unit) + stages 1-2 (router rows, then the selection's keys)
   if ((size_t)((E + nsm - 1) / nsm) * d * 4 > 2 * (size_t)p.stage_bytes) return false;
-  if ((size_t)T * ((E + 31) & ~31) * 4 + (size_t)kDlWarps * 96 * 8 > 2 * (size_t)p.stage_bytes) return false;
+  if ((size_t)T * ((E + 31) & ~31) * 4 > 2 * (size_t)p.stage_bytes) return false;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, T > 8 ? dl_fn<2>() : dl_fn<1>(), kDlThreads, p.smem) !=
           cudaSuccess ||
@@ -1424,8 +1374,8 @@ cudaError_t decode_build_maps(void* maps, int E, int d, int f, int nsm, int has_
 
 int decode_timeline_events() { return kDlEvents; }
 
-cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const void* maps, __half* hw,
-                                unsigned* ready, unsigned long long* lgt, unsigned long long* launches, int nsm,
+cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const void* maps, unsigned long long* hw,
+                                unsigned long long* lgt, unsigned long long* launches, int nsm,
                                 unsigned long long* timeline, cudaStream_t st) {
   DlArgs a;
   a.x = r.x;
@@ -1452,7 +1402,6 @@ cudaError_t launch_decode_layer(const RouteArgs& r, const ExpertArgs& x, const v
   a.slots = r.slots;
   a.usage = r.usage;
   a.hw = hw;
-  a.ready = ready;
   a.y = x.y;
   a.resid = x.resid;
   a.lgt = lgt;
