@@ -21,10 +21,10 @@ SMALL_T = 16  # T <= SMALL_T can run the split-K GEMV path
 MOE_OPT_GEMV_MAX_TOKENS = 1
 MOE_OPT_FUSED_MAX_TOKENS = 2
 MOE_OPT_KERNEL_TIMELINE = 3
-TIMELINE_EVENTS = ("start", "dep_wait", "logits", "reserved3", "routed", "first_unit", "units_done", "first_down",
+TIMELINE_EVENTS = ("start", "dep_wait", "logits", "unit_computed", "routed", "first_unit", "units_done", "first_down",
                    "down_done", "end", "last_unit_issued", "first_down_issued", "last_down_issued",
                    "first_unit_issued", "clk_start", "clk_end", "x_staged", "router_rows", "keys", "selected",
-                   "dispatched", "producer_routed", "reserved22", "first_down_done", "producer_go",
+                   "dispatched", "producer_routed", "unit_reduced", "first_down_done", "producer_go",
                    "gather_start", "first_routed_landed", "first_routed_done", "last_down_done")
 
 

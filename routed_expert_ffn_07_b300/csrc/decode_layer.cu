@@ -116,7 +116,7 @@ enum DlEvent {
   kEvStart = 0,        // kernel entered
   kEvDepWait,          // griddepcontrol.wait passed
   kEvLogits,           // logits stored
-  kEvReserved3,
+  kEvUnitComputed,     // first routed unit: warp 0 of its team finished its tensor-core loop
   kEvRouted,           // selection and dispatch done
   kEvFirstUnit,        // first gate/up unit's bytes landed (team 0)
   kEvUnitsDone,        // all of the CTA's gate/up units done
@@ -135,7 +135,7 @@ enum DlEvent {
   kEvSelected,         // top-K chosen
   kEvDispatched,       // dispatch done
   kEvProducerRouted,   // producer learned the routing
-  kEvReserved22,
+  kEvUnitReduced,      // first routed unit: its team's partial tiles are in shared memory
   kEvFirstDownDone,    // first down item done (its h rows were complete)
   kEvProducerGo,       // producer: routing broadcast to its warp, issue loop starts
   kEvGatherStart,      // consumers start reading the published logits
@@ -349,12 +349,7 @@ template <int NT>
 __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, int lane) {
   const int g8 = lane >> 2, t4 = lane & 3;
   const int st = i % u.NS;
-  const bool okw = tc::mbar_wait_warp(&u.full[st], (i / u.NS) & 1, u.abort, kDlConsumerSleep);
-  if (!team_all(team, okw && !*u.abort)) return false;
-  if (tw == 0 && lane == 0 && u.timeline) {
-    if (i == 0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstUnit] = gtimer();
-    if (i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstRoutedLanded] = gtimer();
-  }
+  // the unit's slot and tokens, while its bytes may still be landing
   const int g = u.c + i * u.nc, s = g / u.fu, un = g - s * u.fu;
   int n_s, start = 0;
   if (s < u.HS) {
@@ -364,9 +359,6 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
     n_s = sl.z;
     start = sl.y;
   }
-  const uint8_t* stg = u.ring + (size_t)st * u.SB;
-  const uint32_t sbase = tc::smem_u32(stg);
-  const int CH = u.CH, d = u.d;
   // B fragments: the lane's column g8 of n-tile j is slot-local token 8 j + g8
   int xrow[NT];
 #pragma unroll
@@ -374,6 +366,24 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
     const int n = 8 * j + g8;
     xrow[j] = n < n_s ? (s < u.HS ? n : u.perm_s[start + n] / u.K) * u.XS : -1;
   }
+  // the epilogue's routing weights (warps tw < NT): slot-local tokens 8 tw + 2 (lane % 4) (+ 1)
+  float wt[2] = {1.f, 1.f};
+  if (tw < NT && s >= u.HS) {
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      const int n = 8 * tw + 2 * (lane & 3) + o;
+      if (n < n_s) wt[o] = u.w_s[u.perm_s[start + n]];
+    }
+  }
+  const bool okw = tc::mbar_wait_warp(&u.full[st], (i / u.NS) & 1, u.abort, kDlConsumerSleep);
+  if (!team_all(team, okw && !*u.abort)) return false;
+  if (tw == 0 && lane == 0 && u.timeline) {
+    if (i == 0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstUnit] = gtimer();
+    if (i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstRoutedLanded] = gtimer();
+  }
+  const uint8_t* stg = u.ring + (size_t)st * u.SB;
+  const uint32_t sbase = tc::smem_u32(stg);
+  const int CH = u.CH, d = u.d;
   float C[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) C[j][0] = C[j][1] = C[j][2] = C[j][3] = 0.f;
@@ -412,10 +422,12 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   }
   __syncwarp();
   if (lane == 0) tc::mbar_arrive_cnt(&u.empty[st], kDlWarps / kDlTeamWarps);  // the stage is free
+  if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvUnitComputed] = gtimer();
   float4* my_p = u.pgu + (size_t)(team * kDlTeamWarps + tw) * NT * 32;
 #pragma unroll
   for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
   team_sync(team);
+  if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvUnitReduced] = gtimer();
   // team thread (j, ln): column ln / 4 of the unit, slot-local tokens 8 j + 2 (ln % 4) (+ 1); the
   // team's 4 partial tiles are summed in warp order.  The words of h pair the unit's columns c and
   // c + 4 (fragment positions 2c, 2c + 1); each is published under the launch's epoch tag with one
@@ -436,10 +448,9 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
     float hv[2];
 #pragma unroll
     for (int o = 0; o < 2; ++o) {
-      const int n = n0 + o;
       const float gte = o ? sum.y : sum.x, upv = o ? sum.w : sum.z;
-      const float wt = (s >= u.HS && n < n_s) ? u.w_s[u.perm_s[start + n]] : 1.f;
-      hv[o] = wt * (silu(gte) * upv);
+      // silu with the fast exponential and division: h is rounded to fp16 right after
+      hv[o] = wt[o] * (__fdividef(gte, 1.0f + __expf(-gte)) * upv);
     }
     const float hp0 = __shfl_xor_sync(0xffffffffu, hv[0], 16), hp1 = __shfl_xor_sync(0xffffffffu, hv[1], 16);
     if (col < 4) {
