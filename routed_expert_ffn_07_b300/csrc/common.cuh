@@ -23,6 +23,7 @@ constexpr int kRouterExpertsPerBlock = 4;  // small-T router: 2 warps per expert
 // bits of the device status word
 constexpr unsigned kStatusBadIndex = 1u;
 constexpr unsigned kStatusTimeout = 2u;
+constexpr unsigned kStatusRange = 4u;  // an fp16 tensor-core operand was out of the fp16 range
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -60,8 +60,6 @@ template <int KIND> struct Stages {
   static constexpr int B = KIND == 0 ? 7 : 10;   // activation stages: deep, the TMA latency is long
   static constexpr int J = KIND == 0 ? 4 : 8;    // TMEM A stages (NA*32 columns each, 256 columns in all)
 };
-constexpr unsigned kStatusRange = 4u;
-
 struct GemmMaps {
   CUtensorMap gu_q, gu_s, sh_gu_q, sh_gu_s, dn_q, dn_s, sh_dn_q, sh_dn_s;
 };

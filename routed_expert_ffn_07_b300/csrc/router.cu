@@ -15,6 +15,7 @@
 
 #include "../../include/moe.h"
 #include "common.cuh"
+#include "tc_ptx.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -404,6 +405,152 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const void* x, int a
   }
 }
 
+// logits[T][E] = X[T][d] Wr[E][d]^T (+ bias) for bf16 activations on fp16 tensor cores (mma.sync
+// m16n8k16, fp32 accumulation).  X is one fp16 operand (bf16 values are exact in fp16 inside its
+// range; |x| > 65504 sets the range status bit).  The fp32 router rows become two fp16 operands,
+// hi = fp16(w) and lo = fp16((w - hi) 2^11), so that |w - hi - 2^-11 lo| <= 2^-22 |w| (up to fp16
+// subnormals for |w| < 2^-3 of the smallest normal): logits = X hi^T + 2^-11 X lo^T, each product
+// exact; every k16 partial product is added to fp32 running sums with round-to-nearest additions
+// (fp32-level accuracy as the SIMT kernel above, in another order).
+// CTA tile 128 tokens x 128 experts, k-step 32, 512 threads (16 warps of 32 x 32), operands staged
+// through registers into padded shared rows (80 bytes: conflict-free ldmatrix), double-buffered.
+constexpr int kRmBM = 128, kRmBN = 128, kRmBK = 32, kRmRow = kRmBK + 8;  // row stride in halves
+constexpr size_t kRmSmem = (size_t)2 * 3 * kRmBM * kRmRow * 2;           // x, hi, lo; two buffers
+__device__ __forceinline__ void rm_ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void rm_mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__global__ void __launch_bounds__(512, 1) router_logits_mma_kernel(const __nv_bfloat16* x, const float* Wr,
+                                                                   const float* bias, float* logits, int T, int d,
+                                                                   int E, unsigned* status) {
+  extern __shared__ __align__(16) uint8_t rm_smem[];
+  __half* xs = reinterpret_cast<__half*>(rm_smem);  // [2][BM][kRmRow]
+  __half* hs = xs + 2 * kRmBM * kRmRow;              // [2][BN][kRmRow]
+  __half* ls = hs + 2 * kRmBN * kRmRow;              // [2][BN][kRmRow]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.y * kRmBM, e0 = blockIdx.x * kRmBN;
+  // staging: thread tid takes row tid / 4 and k (tid % 4) * 8 .. + 7 of each operand
+  const int lr = tid >> 2, lk = (tid & 3) * 8;
+  const bool a_on = t0 + lr < T, b_on = e0 + lr < E;
+  const __nv_bfloat16* xrow = x + (size_t)(t0 + lr) * d + lk;
+  const float* wrow = Wr + (size_t)(e0 + lr) * d + lk;
+  uint4 ra;
+  float4 rb0, rb1;
+  bool range_bad = false;
+  auto load = [&](int k0) {
+    ra = a_on ? __ldg(reinterpret_cast<const uint4*>(xrow + k0)) : make_uint4(0u, 0u, 0u, 0u);
+    rb0 = b_on ? __ldg(reinterpret_cast<const float4*>(wrow + k0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    rb1 = b_on ? __ldg(reinterpret_cast<const float4*>(wrow + k0 + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto store = [&](int buf) {
+    const uint32_t xw[4] = {ra.x, ra.y, ra.z, ra.w};
+    uint32_t xo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float v0 = __uint_as_float(xw[q] << 16), v1 = __uint_as_float(xw[q] & 0xFFFF0000u);
+      range_bad |= !(fabsf(v0) <= 65504.f) || !(fabsf(v1) <= 65504.f);
+      const __half2 h2 = __floats2half2_rn(v0, v1);
+      xo[q] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(xs + ((size_t)buf * kRmBM + lr) * kRmRow + lk) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+    const float wv[8] = {rb0.x, rb0.y, rb0.z, rb0.w, rb1.x, rb1.y, rb1.z, rb1.w};
+    uint32_t ho[4], lo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half h0 = __float2half_rn(wv[2 * q]), h1 = __float2half_rn(wv[2 * q + 1]);
+      const __half l0 = __float2half_rn((wv[2 * q] - __half2float(h0)) * 2048.f);
+      const __half l1 = __float2half_rn((wv[2 * q + 1] - __half2float(h1)) * 2048.f);
+      ho[q] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+      lo[q] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    }
+    *reinterpret_cast<uint4*>(hs + ((size_t)buf * kRmBN + lr) * kRmRow + lk) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+    *reinterpret_cast<uint4*>(ls + ((size_t)buf * kRmBN + lr) * kRmRow + lk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  };
+  const int wm = warp >> 2, wn = warp & 3;  // warp tile: tokens wm*32 .. +31, experts wn*32 .. +31
+  float ch[2][4][4], cl[2][4][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ch[i][j][q] = cl[i][j][q] = 0.f;
+  // ldmatrix lane addresses (element offsets within a buffer)
+  const int a_off = (wm * 32 + (lane & 15)) * kRmRow + (lane >> 4) * 8;
+  const int b_off = (wn * 32 + ((lane >> 4) << 3) + (lane & 7)) * kRmRow + ((lane >> 3) & 1) * 8;
+  const uint32_t xs_u = tc::smem_u32(xs), hs_u = tc::smem_u32(hs), ls_u = tc::smem_u32(ls);
+  load(0);
+  store(0);
+  __syncthreads();
+  const int nk = d / kRmBK;
+#pragma unroll 1
+  for (int kt = 0; kt < nk; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nk) load((kt + 1) * kRmBK);
+    const uint32_t xb = xs_u + (uint32_t)(buf * kRmBM * kRmRow) * 2, hb = hs_u + (uint32_t)(buf * kRmBN * kRmRow) * 2,
+                   lb = ls_u + (uint32_t)(buf * kRmBN * kRmRow) * 2;
+#pragma unroll
+    for (int kk = 0; kk < kRmBK; kk += 16) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        rm_ldsm_x4(xb + (uint32_t)(a_off + i * 16 * kRmRow + kk) * 2, a[i][0], a[i][1], a[i][2], a[i][3]);
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {  // pairs of n8 tiles
+        uint32_t bh[4], bl[4];
+        rm_ldsm_x4(hb + (uint32_t)(b_off + jp * 16 * kRmRow + kk) * 2, bh[0], bh[1], bh[2], bh[3]);
+        rm_ldsm_x4(lb + (uint32_t)(b_off + jp * 16 * kRmRow + kk) * 2, bl[0], bl[1], bl[2], bl[3]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          // each k16 product from zero, then added in fp32 (round to nearest): the tensor core's own
+          // accumulation covers 16 terms only
+          float p[4][4] = {};
+          rm_mma(p[0], a[i][0], a[i][1], a[i][2], a[i][3], bh[0], bh[1]);
+          rm_mma(p[1], a[i][0], a[i][1], a[i][2], a[i][3], bh[2], bh[3]);
+          rm_mma(p[2], a[i][0], a[i][1], a[i][2], a[i][3], bl[0], bl[1]);
+          rm_mma(p[3], a[i][0], a[i][1], a[i][2], a[i][3], bl[2], bl[3]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            ch[i][2 * jp][q] += p[0][q];
+            ch[i][2 * jp + 1][q] += p[1][q];
+            cl[i][2 * jp][q] += p[2][q];
+            cl[i][2 * jp + 1][q] += p[3][q];
+          }
+        }
+      }
+    }
+    if (kt + 1 < nk) {
+      // the other buffer was last read in the previous step, before its closing barrier
+      store(buf ^ 1);
+      __syncthreads();
+    }
+  }
+  if (range_bad) atomicOr(status, kStatusRange);
+  const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = t0 + wm * 32 + i * 16 + g + 8 * h;
+        if (t >= T) continue;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int e = e0 + wn * 32 + j * 8 + 2 * t4 + c;
+          if (e < E)
+            logits[(size_t)t * E + e] =
+                ch[i][j][2 * h + c] + cl[i][j][2 * h + c] * (1.0f / 2048.f) + (bias ? bias[e] : 0.f);
+        }
+      }
+}
+
 // Top-K for T tokens, one warp per token.  Dynamic shared memory: 8*E floats.
 __global__ void __launch_bounds__(256) topk_kernel(RouteArgs a) {
   extern __shared__ float smem[];
@@ -508,8 +655,14 @@ cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t 
     rmsnorm_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a.x, a.xnorm, a.act, a.T, a.d, a.eps);
     xin = a.xnorm;
   }
-  dim3 g((a.E + kRlBN - 1) / kRlBN, (a.T + kRlBM - 1) / kRlBM);
-  router_logits_kernel<<<g, 256, 0, st>>>(xin, a.act, a.Wr, a.bias, a.logits, a.T, a.d, a.E);
+  if (a.act == kActBf16 && a.d % kRmBK == 0) {
+    dim3 g((a.E + kRmBN - 1) / kRmBN, (a.T + kRmBM - 1) / kRmBM);
+    router_logits_mma_kernel<<<g, 512, kRmSmem, st>>>(static_cast<const __nv_bfloat16*>(xin), a.Wr, a.bias,
+                                                      a.logits, a.T, a.d, a.E, a.status);
+  } else {
+    dim3 g((a.E + kRlBN - 1) / kRlBN, (a.T + kRlBM - 1) / kRlBM);
+    router_logits_kernel<<<g, 256, 0, st>>>(xin, a.act, a.Wr, a.bias, a.logits, a.T, a.d, a.E);
+  }
   topk_kernel<<<(a.T + kRouterWarps - 1) / kRouterWarps, 256, (size_t)kRouterWarps * a.E * sizeof(float), st>>>(a);
   dispatch_hist_kernel<<<nblocks_dispatch, kDispatchBlock, 0, st>>>(a);
   dispatch_scan_kernel<<<1, 1024, 0, st>>>(a, nblocks_dispatch);
@@ -519,6 +672,8 @@ cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t 
 
 cudaError_t route_kernels_init() {
   cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_logits_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRmSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
 }
