@@ -54,6 +54,7 @@ constexpr int kKA = 256;            // K per weight stage (128-byte int4 rows)
 constexpr int kSub = kKA / kKS;     // MMA stages per weight stage
 constexpr int kAStages = 3;         // weight stages in SMEM (int4 rows + their fp16 scales)
 constexpr int kScB = kKA / 32 * 2;  // scale bytes per weight row per weight stage (8 groups)
+constexpr int kBPrefetch = 16;      // activation stages prefetched into L2 ahead of the loads
 // activation stages in SMEM and dequantised A stages in TMEM, per kind (0 gate/up, 1 down)
 template <int KIND> struct Stages {
   static constexpr int NA = KIND == 0 ? 2 : 1;   // A matrices per tile
@@ -197,20 +198,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // The whole warp runs this loop converged (all values warp-uniform); one elected lane issues.
     uint32_t gs = 0, it = 0;
     bool ok = true;
+    const uint32_t leader = tc::elect_one();
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
       const int tile = item / nblk;
       const int nmma = (g.tile_n[tile] + 15) & ~15;
       const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
       const int b = it % NB;
-      if (!tc::mbar_wait_warp(&acc_empty[b], ((it / NB) & 1) ^ 1, &s_abort)) { ok = false; break; }
+      if (!tc::mbar_wait_all(&acc_empty[b], ((it / NB) & 1) ^ 1, &s_abort)) { ok = false; break; }
       tc::tc_fence_after();
       const uint32_t dcol0 = KIND == 0 ? 0u : (uint32_t)b * 128u;
       for (int s = 0; s < KS; ++s, ++gs) {
         const int slot = gs % BS;
         const uint32_t ph = (gs / BS) & 1;
-        // tfull completes after the dequant warps also saw this stage's activations arrive; the
-        // second wait then returns at once but keeps the TMA -> MMA ordering explicit
-        if (!tc::mbar_wait_warp(&tfull[slot], ph, &s_abort) || !tc::mbar_wait_warp(&fb[slot], ph, &s_abort)) {
+        // tfull completes after every dequant warp of the stage's team saw the stage's activations
+        // arrive (its fb phase) and stored its part of A: acquiring it orders the MMAs after both
+        if (!tc::mbar_wait_all(&tfull[slot], ph, &s_abort)) {
           ok = false;
           break;
         }
@@ -221,13 +223,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kk = 0; kk < kKS / 16; ++kk) {
 #pragma unroll
           for (int m = 0; m < NA; ++m)
-            tc::mma_ts_elect(tmem + dcol0 + (KIND == 0 ? m * 128 : 0), a0 + m * 32 + kk * 8,
-                             bd0 + (uint64_t)(kk * 2), idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_ts_pred(tmem + dcol0 + (KIND == 0 ? m * 128 : 0), a0 + m * 32 + kk * 8, bd0 + (uint64_t)(kk * 2),
+                            idesc, (s > 0 || kk > 0) ? 1u : 0u, leader);
         }
-        tc::mma_commit_elect(&sdone[slot]);
+        tc::mma_commit_pred(&sdone[slot], leader);
       }
       if (!ok) break;
-      tc::mma_commit_elect(&acc_full[b]);
+      tc::mma_commit_pred(&acc_full[b], leader);
     }
     if (!ok && lane == 0) give_up();
     __syncwarp();
@@ -283,6 +285,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!tc::mbar_wait(&sdone[slot], ((gs / BS) & 1) ^ 1, &s_abort)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&fb[slot], kNT * 128);
           tc::tma_load_2d(sB + slot * kNT * 128, &mb, s * kKS, brow, &fb[slot]);
+          // the activation tile kBPrefetch stages ahead into L2, so that its load (issued once a slot
+          // frees) finds it there: the slots alone look too few stages ahead to hide the HBM latency
+          int s2 = s + kBPrefetch, item2 = item;
+          while (s2 >= KS) {
+            s2 -= KS;
+            item2 += gridDim.x;
+          }
+          if (item2 < n_items) tc::tma_prefetch_l2_2d(&mb, s2 * kKS, g.tile_row[item2 / nblk]);
         }
       }
       if (!ok) give_up();

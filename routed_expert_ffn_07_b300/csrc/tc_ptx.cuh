@@ -37,30 +37,57 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase is not complete is suspended until it
+// completes or about `hint_ns` nanoseconds have passed, instead of spinning on the barrier.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, "
+      "0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up (returns false) after
-// ~`budget` SM clocks or as soon as *abort is set by another thread.
+// ~`budget` SM clocks or as soon as *abort is set by another thread.  Between checks of the abort
+// flag and the budget the thread is suspended on the barrier (at most ~1 us at a time), so waiting
+// warps do not take issue slots from the warps that compute.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           long long budget = 4000000000ll) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_for(bar, parity, 1000u)) return true;
     if (*abort) return false;
     if (clock64() - t0 > budget) return false;
   }
 }
 
-// The same for waiters with nothing else to do on an SM whose other warps compute: between polls
-// the thread sleeps about `sleep_ns`, so the spin does not take issue slots from them.
+// The same for waiters that should also yield between checks (kept for the callers' intent: the
+// suspend hint already keeps the wait off the issue slots).
 __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                  unsigned sleep_ns, long long budget = 4000000000ll) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_for(bar, parity, sleep_ns > 1000u ? sleep_ns : 1000u)) return true;
     if (*abort) return false;
     if (clock64() - t0 > budget) return false;
+  }
+}
+
+// Warp-wide bounded wait in which every lane polls the barrier (one instruction for the warp: the
+// lanes see the same phase), so the warp stays converged without a broadcast.  Call from a
+// converged warp; returns false (uniformly) when it gave up.
+__device__ __forceinline__ bool mbar_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              long long budget = 4000000000ll) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_for(bar, parity, 1000u))) return true;
+    if (__any_sync(0xffffffffu, *abort != 0 || clock64() - t0 > budget)) return false;
   }
 }
 
@@ -178,6 +205,28 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// One lane of a converged warp (1 there, 0 elsewhere), for the *_pred forms below: the warp
+// elects once and every lane runs the predicated instructions, without a branch.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void mma_ts_pred(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t acc, uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pred(uint64_t* bar, uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "r"(leader)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
