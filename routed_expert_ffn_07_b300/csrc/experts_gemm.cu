@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sA = sB + BS * kNT * 128;                // kAStages x NA x [128 rows x 128 B] int4
   uint8_t* sS = sA + kAStages * NA * kBM * 128;     // kAStages x NA x [128 rows x 8 fp16]
   // fa/ea: weight stages; fb: activation stages; tfull: stage gs dequantised into TMEM A stage
-  // gs % J and its activations seen by the dequant warps; sdone: the MMAs of stage gs finished,
+  // gs % J; sdone: the MMAs of stage gs finished,
   // which frees activation slot gs % BS and (J stages later) TMEM A stage gs % J
   __shared__ __align__(8) uint64_t fa[kAStages], ea[kAStages], fb[BS], tfull[BS], sdone[BS], acc_full[2],
       acc_empty[2], fin;
@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < KS; ++s, ++gs) {
         const int slot = gs % BS;
         const uint32_t ph = (gs / BS) & 1;
-        // tfull completes after every dequant warp of the stage's team saw the stage's activations
-        // arrive (its fb phase) and stored its part of A: acquiring it orders the MMAs after both
-        if (!tc::mbar_wait_all(&tfull[slot], ph, &s_abort)) {
+        // the stage's activations landed (fb) and every dequant warp of its team stored its part of
+        // A (tfull); the whole warp polls each barrier
+        if (!tc::mbar_wait_all(&fb[slot], ph, &s_abort) || !tc::mbar_wait_all(&tfull[slot], ph, &s_abort)) {
           ok = false;
           break;
         }
@@ -430,16 +430,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
-        int fb_ok = 1;
         if (lane == 0) {
-          fb_ok = tc::mbar_wait(&fb[slot], (gs / BS) & 1, &s_abort) ? 1 : 0;  // activations landed too
           tc::mbar_arrive(&tfull[slot]);
           if (sub_k >= kSub - 2) tc::mbar_arrive(&ea[aslot]);  // this warp's last part of the weight stage
         }
-        if (!__shfl_sync(0xffffffffu, fb_ok, 0)) {  // keep the warp converged for the .aligned ops
-          ok = false;
-          break;
-        }
+        __syncwarp();
       }
       if (!ok) break;
       p_item = item;
