@@ -54,7 +54,7 @@ constexpr int kKA = 256;            // K per weight stage (128-byte int4 rows)
 constexpr int kSub = kKA / kKS;     // MMA stages per weight stage
 constexpr int kAStages = 3;         // weight stages in SMEM (int4 rows + their fp16 scales)
 constexpr int kScB = kKA / 32 * 2;  // scale bytes per weight row per weight stage (8 groups)
-constexpr int kBPrefetch = 16;      // activation stages prefetched into L2 ahead of the loads
+constexpr int kBPrefetch = 16;      // gate/up: activation stages prefetched into L2 ahead of the loads
 // activation stages in SMEM and dequantised A stages in TMEM, per kind (0 gate/up, 1 down)
 template <int KIND> struct Stages {
   static constexpr int NA = KIND == 0 ? 2 : 1;   // A matrices per tile
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             s2 -= KS;
             item2 += gridDim.x;
           }
-          if (item2 < n_items) tc::tma_prefetch_l2_2d(&mb, s2 * kKS, g.tile_row[item2 / nblk]);
+          if (KIND == 0 && item2 < n_items) tc::tma_prefetch_l2_2d(&mb, s2 * kKS, g.tile_row[item2 / nblk]);
         }
       }
       if (!ok) give_up();
