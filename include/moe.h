@@ -197,7 +197,8 @@ moe_status moe_inject_device_status(moe_handle h, unsigned bits, void* stream);
  * tag nobody writes, each with a budget of `budget_cycles` SM clocks (1000 .. 2e9).  Returns MOE_ERR_TIMEOUT
  * when both waits gave up and recorded "timeout" (the expected outcome), MOE_ERR_DEVICE if a wait
  * reported success, MOE_ERR_CUDA on a CUDA error.  Synchronises `stream`; the GPU context stays
- * usable afterwards. */
+ * usable afterwards.  Allocates nothing: the word and the result live in file-scope device memory
+ * (concurrent self-tests on one device race on them). */
 moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream);
 
 /* Options (each returns the value in effect, or a negative moe_status on error; changing one

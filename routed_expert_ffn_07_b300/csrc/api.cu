@@ -17,14 +17,13 @@
 namespace moe {
 cudaError_t launch_route(const RouteArgs& a, int nblocks_dispatch, cudaStream_t st);
 cudaError_t route_kernels_init();
-cudaError_t gemv_kernels_init(int num_sms);
+cudaError_t gemv_kernels_init();
 cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, cudaEvent_t mid, cudaEvent_t mid2);
 size_t gemv_smem_gu(int wfmt, int T, int d, int E, int K);
 size_t gemv_smem_dn(int T, int K, int E);
-cudaError_t gemm_kernels_init(int num_sms);
+cudaError_t gemm_kernels_init();
 cudaError_t decode_kernels_init();
-cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
-                                         cudaStream_t st);
+cudaError_t launch_bounded_wait_selftest(long long budget, unsigned* result_host, cudaStream_t st);
 bool decode_shape_ok(int T, int d, int f, int E, int K, int nsm);
 size_t decode_maps_bytes();
 cudaError_t decode_build_maps(void* maps, int E, int d, int f, int nsm, int has_shared, const void* gu_q,
@@ -195,8 +194,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle* out) {
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   h->gemm_ok = c.wfmt == MOE_W_INT4_G32 && gemm_shape_ok(c.d, c.f);
   if (!h->gemm_ok) h->gemv_max_tokens = kSmallT;
-  if (route_kernels_init() != cudaSuccess || gemv_kernels_init(h->num_sms) != cudaSuccess ||
-      (h->gemm_ok && gemm_kernels_init(h->num_sms) != cudaSuccess) ||
+  if (route_kernels_init() != cudaSuccess || gemv_kernels_init() != cudaSuccess ||
+      (h->gemm_ok && gemm_kernels_init() != cudaSuccess) ||
       (c.wfmt == MOE_W_INT4_G32 && decode_kernels_init() != cudaSuccess)) {
     delete h;
     return MOE_ERR_CUDA;
@@ -376,6 +375,7 @@ static ExpertArgs make_expert_args(moe_ctx* h, int layer, const void* x, int T, 
   a.act = c.act;
   a.has_shared = c.has_shared;
   a.max_tokens = c.max_tokens;
+  a.num_sms = h->num_sms;
   a.x = x;
   a.gu_q = w.gu_q;
   a.gu_s = static_cast<const __half*>(w.gu_s);
@@ -663,24 +663,8 @@ moe_status moe_inject_device_status(moe_handle h, unsigned bits, void* stream) {
 
 moe_status moe_selftest_bounded_waits(long long budget_cycles, void* stream) {
   if (budget_cycles < 1000 || budget_cycles > 2000000000ll) return MOE_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  unsigned long long* counter = nullptr;
-  unsigned* res = nullptr;
-  CUDA_TRY(cudaMalloc(&counter, 8));
-  cudaError_t e = cudaMalloc(&res, 8);
-  if (e != cudaSuccess) {
-    cudaFree(counter);
-    g_last_cuda_error = (int)e;
-    return MOE_ERR_CUDA;
-  }
   unsigned hres[2] = {0, 0};
-  e = cudaMemsetAsync(counter, 0, 8, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(res, 0, 8, st);
-  if (e == cudaSuccess) e = launch_bounded_wait_selftest(counter, budget_cycles, res, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(hres, res, 8, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  cudaFree(counter);
-  cudaFree(res);
+  const cudaError_t e = launch_bounded_wait_selftest(budget_cycles, hres, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     g_last_cuda_error = (int)e;
     return MOE_ERR_CUDA;

@@ -156,6 +156,7 @@ struct RouteArgs {
 struct ExpertArgs {
   int T, d, f, E, K, act, has_shared;
   int max_tokens;         // the handle's max_tokens (fixes the workspace layout)
+  int num_sms;            // the handle's device: SMs (persistent grids)
   const void* x;          // [T][d] expert input (normalised input in the stack)
   const void* gu_q;       // [E][2f][..] routed gate/up
   const __half* gu_s;

@@ -1236,10 +1236,24 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long* word, long long
   }
 }
 
-cudaError_t launch_bounded_wait_selftest(unsigned long long* counter, long long budget, unsigned* result,
-                                         cudaStream_t st) {
-  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(counter, budget, result);
-  return cudaGetLastError();
+// The self-test's word and result, file-scope device memory (no allocation).
+__device__ unsigned long long g_selftest_word;
+__device__ unsigned g_selftest_result[2];
+
+cudaError_t launch_bounded_wait_selftest(long long budget, unsigned* result_host, cudaStream_t st) {
+  void* wp = nullptr;
+  void* rp = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&wp, g_selftest_word);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(&rp, g_selftest_result);
+  if (e == cudaSuccess) e = cudaMemsetAsync(wp, 0, sizeof(unsigned long long), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(rp, 0, 2 * sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(static_cast<unsigned long long*>(wp), budget,
+                                                 static_cast<unsigned*>(rp));
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyAsync(result_host, rp, 2 * sizeof(unsigned), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e;
 }
 
 // ------------------------------------------------------------------ host side

@@ -563,7 +563,6 @@ __global__ void combine_kernel(const __nv_bfloat16* P, int T, int d, int K, int 
 
 // ------------------------------------------------------------------ host side
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-static int g_sms = 148;
 
 constexpr int kGemmSmemMax = 226 * 1024;
 
@@ -573,8 +572,7 @@ constexpr size_t gemm_smem_bytes() {
 }
 static_assert(gemm_smem_bytes<0>() <= kGemmSmemMax && gemm_smem_bytes<1>() <= kGemmSmemMax, "shared memory");
 
-cudaError_t gemm_kernels_init(int num_sms) {
-  g_sms = num_sms;
+cudaError_t gemm_kernels_init() {
   if (!g_encode) {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -704,10 +702,10 @@ cudaError_t launch_experts_gemm(const ExpertArgs& a, const void* maps_v, const v
   g.tile_row = w.tile_row;
   g.tile_n = w.tile_n;
   g.status = a.status;
-  gemm_kernel<0><<<g_sms, kGemmThreads, gemm_smem_bytes<0>(), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s,
+  gemm_kernel<0><<<a.num_sms, kGemmThreads, gemm_smem_bytes<0>(), st>>>(g, mp.gu_q, mp.gu_s, mp.sh_gu_q, mp.sh_gu_s,
                                                                         am.xs);
   if (mid) record_timing_event(mid, st);
-  gemm_kernel<1><<<g_sms, kGemmThreads, gemm_smem_bytes<1>(), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s,
+  gemm_kernel<1><<<a.num_sms, kGemmThreads, gemm_smem_bytes<1>(), st>>>(g, mp.dn_q, mp.dn_s, mp.sh_dn_q, mp.sh_dn_s,
                                                                         am.hs);
   if (mid2) record_timing_event(mid2, st);
   const size_t nblk8 = (size_t)T * d / 8;

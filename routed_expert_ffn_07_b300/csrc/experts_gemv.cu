@@ -456,10 +456,7 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) dn_f32_kernel(ExpertArgs a) 
 }
 
 // ------------------------------------------------------------------ launchers
-static int g_num_sms = 148;
-
-cudaError_t gemv_kernels_init(int num_sms) {
-  g_num_sms = num_sms;
+cudaError_t gemv_kernels_init() {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gu_int4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
   if ((e = cudaFuncSetAttribute(gu_int4_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))) return e;
@@ -490,7 +487,7 @@ cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, 
   if (wfmt == kWInt4) {
     const int G = a.d / 32;
     const int ng = (G + 31) / 32;
-    const int grid = g_num_sms;
+    const int grid = a.num_sms;
     switch (ng) {
       case 1: gu_int4_kernel<1><<<grid, kGuThreads, sm_gu, st>>>(a); break;
       case 2: gu_int4_kernel<2><<<grid, kGuThreads, sm_gu, st>>>(a); break;
@@ -502,7 +499,7 @@ cudaError_t launch_experts_gemv(const ExpertArgs& a, int wfmt, cudaStream_t st, 
     dn_int4_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
     if (mid2) record_timing_event(mid2, st);
   } else {
-    gu_f32_kernel<<<g_num_sms, 256, sm_gu, st>>>(a);
+    gu_f32_kernel<<<a.num_sms, 256, sm_gu, st>>>(a);
     if (mid) record_timing_event(mid, st);
     dn_f32_kernel<<<dn_grid, kDnWarps * 32, sm_dn, st>>>(a);
     if (mid2) record_timing_event(mid2, st);

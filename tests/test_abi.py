@@ -99,3 +99,26 @@ def test_noalloc_route_validates_before_touching_the_device(lib):
 def test_selftest_rejects_bad_budget_before_the_device(lib):
     assert lib.lib.moe_selftest_bounded_waits(10, None) == 1
     assert lib.lib.moe_selftest_bounded_waits(10 ** 12, None) == 1
+
+
+def test_device_memory_is_allocated_and_synchronised_only_in_create_and_destroy():
+    """The boundary stores pointers: cudaMalloc / cudaFree / cudaDeviceSynchronize appear only in the
+    bodies of moe_create and moe_destroy (a scan of the library's sources)."""
+    import re
+    csrc = os.path.join(ROOT, "routed_expert_ffn_07_b300", "csrc")
+    calls = re.compile(r"\b(cudaMalloc|cudaMallocAsync|cudaFree|cudaFreeAsync|cudaDeviceSynchronize)\s*\(")
+    opener = re.compile(r"^[A-Za-z_][\w:<>\*& ]*\b(\w+)\s*\([^;]*$")
+    found = []
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh")):
+            continue
+        func = None
+        for line in open(os.path.join(csrc, name)):
+            m = opener.match(line)
+            if m and not line.startswith((" ", "\t", "#", "//")):
+                func = m.group(1)
+            code = line.split("//")[0]
+            if calls.search(code):
+                found.append((name, func))
+    assert found, "the scan found no allocation at all"
+    assert {f for _, f in found} <= {"moe_create", "moe_destroy"}, found
