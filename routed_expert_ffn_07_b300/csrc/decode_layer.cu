@@ -280,6 +280,54 @@ __device__ __forceinline__ uint32_t max16(const uint32_t (&k)[16]) {  // a balan
   return max(a, b);
 }
 
+// Top-K of one token by all 16 consumer warps (T = 1, E <= 512, K <= 16): warp w holds keys
+// 32 w + lane.  The K-th largest of the 16 warp maxima is a lower bound of the K-th largest key (the
+// K largest warp maxima are K keys), so the keys at or above it hold the selection; when there are
+// at most 64 of them, warp w ranks candidates w, w + 16, ... against all the others (larger key,
+// then lower expert: one ballot per half of the candidate list) and rank r < K is the r-th choice,
+// written to sel[r].  Returns false (uniformly) when there were more candidates (many equal
+// logits): the caller then selects with one warp.  Ends with the group barrier.
+__device__ __forceinline__ bool topk_select_cta(const uint32_t* key, int EP, int K, int gw, int lane, int gt,
+                                                uint32_t* wmax, uint2* cand, int* ncand, uint2* sel, int gn) {
+  const uint32_t k = gt < EP ? key[gt] : 0u;
+  const uint32_t wm = __reduce_max_sync(0xffffffffu, k);
+  if (lane == 0) wmax[gw] = wm;
+  if (gt == 0) *ncand = 0;
+  group_sync(gn);
+  const uint32_t mv = lane < kDlWarps ? wmax[lane] : 0u;
+  int rk = 0;  // rank of this lane's warp maximum among the 16, ties to the lower warp
+#pragma unroll
+  for (int j = 0; j < kDlWarps; ++j) {
+    const uint32_t o = __shfl_sync(0xffffffffu, mv, j);
+    rk += (o > mv) || (o == mv && j < lane);
+  }
+  const uint32_t tau = __reduce_max_sync(0xffffffffu, lane < kDlWarps && rk == K - 1 ? mv : 0u);
+  const bool is_c = k != 0u && k >= tau;
+  const unsigned bal = __ballot_sync(0xffffffffu, is_c);
+  int base = 0;
+  if (lane == 0 && bal) base = atomicAdd(ncand, __popc(bal));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (is_c) {
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (pos < 64) cand[pos] = make_uint2(k, (uint32_t)gt);
+  }
+  group_sync(gn);
+  const int nc = *ncand;
+  if (nc > 64) return false;
+  const uint2 c0 = lane < nc ? cand[lane] : make_uint2(0u, 0u);
+  const uint2 c1 = lane + 32 < nc ? cand[lane + 32] : make_uint2(0u, 0u);
+#pragma unroll 1
+  for (int m = gw; m < nc; m += kDlWarps) {
+    const uint2 me = cand[m];
+    const bool g0 = lane < nc && (c0.x > me.x || (c0.x == me.x && c0.y < me.y));
+    const bool g1 = lane + 32 < nc && (c1.x > me.x || (c1.x == me.x && c1.y < me.y));
+    const int rank = __popc(__ballot_sync(0xffffffffu, g0)) + __popc(__ballot_sync(0xffffffffu, g1));
+    if (rank < K && lane == 0) sel[rank] = me;
+  }
+  group_sync(gn);
+  return true;
+}
+
 // Top-K of one token by one warp from its keys in shared memory (key[e] = order-preserving key of
 // logit e, never 0; 0 past E; E <= 512): lane l holds keys l + 32 j in registers and its maximum.
 // Round r takes the largest remaining key (a warp max-reduction) and, among the lanes holding it,
@@ -617,6 +665,9 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
   __shared__ __align__(8) uint64_t full[kDlMaxStages], empty[kDlMaxStages], wr_full, route_ready;
   __shared__ UnitCtx uc_s;
   __shared__ uint32_t s_bits[32], s_bpre[32];  // dispatch: bitmap of the selected experts, its prefix counts
+  __shared__ uint32_t s_wmax[kDlWarps];          // one-token selection: the warps' maximum keys,
+  __shared__ uint2 s_cand[64], s_sel[kDlWarps];  // the candidates (key, expert) and the ranked choices
+  __shared__ int s_ncand;
   __shared__ volatile int s_abort;
   __shared__ unsigned s_ep;
   __shared__ int s_nact, s_issued;
@@ -1005,19 +1056,38 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
       }
       if (gt == 0) DL_STAMP(kEvKeys);
       if (ok) {
-        // one warp per token
+        // one token and all 16 warps: a threshold from the warp maxima, then every candidate ranked
+        // by a warp (at most 64 candidates; otherwise the one-warp selection below)
+        bool cta_done = false;
+        if (T == 1 && E <= kDlWarps * 32 && gn == kDlWarps * 32 && K <= kDlWarps)
+          cta_done = topk_select_cta(keys, EP, K, gw, lane, gt, s_wmax, s_cand, &s_ncand, s_sel, gn);
+        if (cta_done) {
+          if (gw == 0) {
+            const uint2 mine = lane < K ? s_sel[lane] : make_uint2(0u, 0u);
+            const float top = topk_key_value(s_sel[0].x);
+            const float p = lane < K ? expf(topk_key_value(mine.x) - top) : 0.f;
+            const float psum = warp_sum(p);
+            if (lane < K) {
+              idx_s[lane] = (int)mine.y;
+              w_s[lane] = p / psum;
+              atomicOr(&s_bits[mine.y >> 5], 1u << (mine.y & 31));
+            }
+          }
+        } else {
+          // one warp per token
 #pragma unroll 1
-        for (int t = gw; t < T; t += gnw) {
-          int my_i;
-          float my_w;
-          if (E <= 512)
-            topk_select_warp(keys + (size_t)t * EP, E, K, my_i, my_w);
-          else
-            topk_warp(keys + (size_t)t * EP, E, K, my_i, my_w);
-          if (lane < K) {
-            idx_s[t * K + lane] = my_i;
-            w_s[t * K + lane] = my_w;
-            atomicOr(&s_bits[my_i >> 5], 1u << (my_i & 31));
+          for (int t = gw; t < T; t += gnw) {
+            int my_i;
+            float my_w;
+            if (E <= 512)
+              topk_select_warp(keys + (size_t)t * EP, E, K, my_i, my_w);
+            else
+              topk_warp(keys + (size_t)t * EP, E, K, my_i, my_w);
+            if (lane < K) {
+              idx_s[t * K + lane] = my_i;
+              w_s[t * K + lane] = my_w;
+              atomicOr(&s_bits[my_i >> 5], 1u << (my_i & 31));
+            }
           }
         }
         group_sync(gn);
