@@ -1093,7 +1093,32 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         group_sync(gn);
         if (gt == 0) DL_STAMP(kEvSelected);
         const int n = T * K;
-        if (n <= 32) {
+        if (T == 1 && E <= 1024) {
+          // one token: its K experts are distinct, so expert e's slot (= its place in the stable
+          // sort) is the number of selected experts below e, read off the selection bitmap with a
+          // prefix count over its words (lane w: word w; 32 words cover E <= 1024)
+          if (gw == 0) {
+            const uint32_t bw = s_bits[lane];
+            const int pc = __popc(bw);
+            int incl = pc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const int e_i = lane < K ? idx_s[lane] : 0;
+            const int wpre = __shfl_sync(0xffffffffu, incl - pc, e_i >> 5);
+            const uint32_t wbits = __shfl_sync(0xffffffffu, bw, e_i >> 5);
+            if (lane < K) {
+              const int slot = wpre + __popc(wbits & ((1u << (e_i & 31)) - 1u));
+              perm_s[slot] = lane;
+              slot_s[slot] = make_int4(e_i, slot, 1, 0);
+              tpos[(HS + slot) * kDlMaxT] = (signed char)0;
+            }
+            if (HS && lane == 0) tpos[0] = (signed char)0;
+            if (lane == 0) s_nact = K;
+          }
+        } else if (n <= 32) {
           // few assignments: one warp does the whole dispatch with shuffles.  Lane i = assignment i:
           // its place in the stable counting sort (assignments with a smaller expert, plus the
           // earlier ones with its expert), its slot (distinct experts below its own), its position in
