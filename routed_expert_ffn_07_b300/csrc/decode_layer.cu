@@ -1196,17 +1196,14 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
           DL_STAMP(kEvRouted);
           tc::mbar_arrive(&route_ready);
         }
-        if (c == 0) {
-          // the full outputs: idx, w; offs[e] = assignments with an expert below e
-          const int na = s_nact;
+        // the full outputs (every CTA holds the same routing): offs[e] = assignments with an expert
+        // below e, counts and the usage histogram for this CTA's share of the experts (offs[E] by the
+        // last CTA); idx, w, perm, the distinct experts and the slots by CTA 0
+        {
+          const int eb = (int)((long long)E * c / nc);
+          const int ee = (int)((long long)E * (c + 1) / nc) + (c == nc - 1 ? 1 : 0);
 #pragma unroll 1
-          for (int i = gt; i < n; i += gn) {
-            a.idx[i] = idx_s[i];
-            a.w[i] = w_s[i];
-            a.perm[i] = perm_s[i];
-          }
-#pragma unroll 1
-          for (int e = gt; e <= E; e += gn) {
+          for (int e = eb + gt; e < ee; e += gn) {
             int o = 0, ce = 0;
 #pragma unroll 4
             for (int q = 0; q < n; ++q) {
@@ -1216,6 +1213,15 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
             a.offs[e] = o;
             if (e < E) a.counts[e] = ce;
             if (e < E && ce && a.usage) a.usage[e] += (unsigned long long)ce;
+          }
+        }
+        if (c == 0) {
+          const int na = s_nact;
+#pragma unroll 1
+          for (int i = gt; i < n; i += gn) {
+            a.idx[i] = idx_s[i];
+            a.w[i] = w_s[i];
+            a.perm[i] = perm_s[i];
           }
 #pragma unroll 1
           for (int q = gt; q < na; q += gn) {
