@@ -25,7 +25,8 @@ TIMELINE_EVENTS = ("start", "dep_wait", "logits", "unit_computed", "routed", "fi
                    "down_done", "end", "last_unit_issued", "first_down_issued", "last_down_issued",
                    "first_unit_issued", "clk_start", "clk_end", "x_staged", "router_rows", "keys", "selected",
                    "dispatched", "producer_routed", "unit_reduced", "first_down_done", "producer_go",
-                   "gather_start", "first_routed_landed", "first_routed_done", "last_down_done")
+                   "gather_start", "first_routed_landed", "first_routed_done", "last_down_done",
+                   "second_landed", "second_computed", "second_done")
 
 
 class MoeError(RuntimeError):

@@ -142,6 +142,9 @@ enum DlEvent {
   kEvFirstRoutedLanded,  // first routed gate/up unit's bytes landed
   kEvFirstRoutedDone,    // first routed gate/up unit's h published
   kEvLastDownDone,       // the last slot's down item done
+  kEvSecondLanded,       // the same team's next gate/up unit: its bytes landed (the team saw them)
+  kEvSecondComputed,     // ... its tensor-core loop finished (warp 0 of the team)
+  kEvSecondDone,         // ... its h published
   kDlEvents = 32
 };
 __device__ __forceinline__ unsigned long long gtimer() {
@@ -428,6 +431,7 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   if (tw == 0 && lane == 0 && u.timeline) {
     if (i == 0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstUnit] = gtimer();
     if (i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstRoutedLanded] = gtimer();
+    if (i == u.i0 + kDlTeams) u.timeline[(size_t)u.c * kDlEvents + kEvSecondLanded] = gtimer();
   }
   const uint8_t* stg = u.ring + (size_t)st * u.SB;
   const uint32_t sbase = tc::smem_u32(stg);
@@ -471,6 +475,8 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   __syncwarp();
   if (lane == 0) tc::mbar_arrive_cnt(&u.empty[st], kDlWarps / kDlTeamWarps);  // the stage is free
   if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvUnitComputed] = gtimer();
+  if (tw == 0 && lane == 0 && u.timeline && i == u.i0 + kDlTeams)
+    u.timeline[(size_t)u.c * kDlEvents + kEvSecondComputed] = gtimer();
   float4* my_p = u.pgu + (size_t)(team * kDlTeamWarps + tw) * NT * 32;
 #pragma unroll
   for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
@@ -514,6 +520,8 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
     }
   }
   if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvFirstRoutedDone] = gtimer();
+  if (tw == 0 && lane == 0 && u.timeline && i == u.i0 + kDlTeams)
+    u.timeline[(size_t)u.c * kDlEvents + kEvSecondDone] = gtimer();
   return true;
 }
 
