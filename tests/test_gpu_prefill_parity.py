@@ -167,3 +167,18 @@ def test_prefill_chunk_T4096_skewed_multi_tile():
         capi.moe_destroy(h)
         del wts
         torch.cuda.empty_cache()
+
+
+def test_prefill_fp32_activations_T40():
+    """int4 experts with fp32 activations above the small-T limit: the fp32 SIMT router GEMM (the
+    tensor-core router serves bf16 activations) and the grouped GEMM's fp32 -> fp16 staging."""
+    from routed_expert_ffn_07_b300 import capi
+    wl = Workload(420, "prefill_fp32_act", 40, 256, 16, 4, 256, True, "int4", "f32", 1, False)
+    wts = alloc_and_fill(wl)
+    h = create_handle(wl, wts)
+    try:
+        x = inputs.gen_activations(wl.seed, 40, wl.d, "f32")
+        run_prefill(h, wl, wts, x, 40, repeat=True)
+        run_prefill(h, wl, wts, x[:17], 17)
+    finally:
+        capi.moe_destroy(h)
