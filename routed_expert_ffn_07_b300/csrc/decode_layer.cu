@@ -178,6 +178,48 @@ __device__ __forceinline__ void st_relaxed_gpu(unsigned long long* p, unsigned l
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// ------------------------------------------------------------------ shared-memory accesses
+// Explicit shared-space loads and stores by 32-bit shared address.  The kernel's dynamic shared
+// memory is reached through pointers the compiler cannot prove to be shared (aligned at run time,
+// kept in the shared context of the units), and its generic loads from shared memory cost several
+// times an ld.shared on this part; the hot paths use these instead.
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int lds_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int lds_s8(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s8 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_h2f(uint32_t a) {  // one fp16 value, widened
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return __half2float(__ushort_as_half(v));
+}
+__device__ __forceinline__ void sts_f4(uint32_t a, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+__device__ __forceinline__ void sts_v2(uint32_t a, uint2 v) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // Named barriers: 1 = the 512 consumer threads, 2 + team = the 128 threads of a gate/up team,
 // 6 = the routing group (below).
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kDlWarps * 32) : "memory"); }
@@ -376,6 +418,7 @@ struct UnitCtx {
   uint8_t* ring;
   const uint4* xh;        // [T][XS] x fragments
   float4* pgu;            // [16 warps][NT][32] partial tiles
+  uint32_t ring_a, xh_a, pgu_a, perm_a, w_a, tpos_a;  // the same regions as shared addresses
   const int4* slot_s;     // routed slots {expert, start, count, 0}
   const int* perm_s;
   const float* w_s;
@@ -415,7 +458,7 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int n = 8 * j + g8;
-    xrow[j] = n < n_s ? (s < u.HS ? n : u.perm_s[start + n] / u.K) * u.XS : -1;
+    xrow[j] = n < n_s ? (s < u.HS ? n : lds_s32(u.perm_a + 4u * (start + n)) / u.K) * u.XS : -1;
   }
   // the epilogue's routing weights (warps tw < NT): slot-local tokens 8 tw + 2 (lane % 4) (+ 1)
   float wt[2] = {1.f, 1.f};
@@ -423,7 +466,7 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
 #pragma unroll
     for (int o = 0; o < 2; ++o) {
       const int n = 8 * tw + 2 * (lane & 3) + o;
-      if (n < n_s) wt[o] = u.w_s[u.perm_s[start + n]];
+      if (n < n_s) wt[o] = lds_f32(u.w_a + 4u * lds_s32(u.perm_a + 4u * (start + n)));
     }
   }
   const bool okw = tc::mbar_wait_warp(&u.full[st], (i / u.NS) & 1, u.abort, kDlConsumerSleep);
@@ -440,12 +483,12 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
 #pragma unroll
   for (int j = 0; j < NT; ++j) C[j][0] = C[j][1] = C[j][2] = C[j][3] = 0.f;
   const int cb = tw * CH / kDlTeamWarps, cend = (tw + 1) * CH / kDlTeamWarps;  // this warp's chunks of K
-  const __half* scl = reinterpret_cast<const __half*>(stg + u.gu_code_bytes);  // [gate|up][8][d/32]
+  const uint32_t scl = sbase + (uint32_t)u.gu_code_bytes;  // [gate|up][8][d/32] fp16
   const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll 1
   for (int ch = cb; ch < cend; ++ch) {
-    const uint4 sgv = *reinterpret_cast<const uint4*>(scl + (size_t)g8 * (d / 32) + ch * 8);
-    const uint4 suv = *reinterpret_cast<const uint4*>(scl + (size_t)(8 + g8) * (d / 32) + ch * 8);
+    const uint4 sgv = lds_v4(scl + 2u * (uint32_t)(g8 * (d / 32) + ch * 8));
+    const uint4 suv = lds_v4(scl + 2u * (uint32_t)((8 + g8) * (d / 32) + ch * 8));
     const uint32_t sgw[4] = {sgv.x, sgv.y, sgv.z, sgv.w}, suw[4] = {suv.x, suv.y, suv.z, suv.w};
     const uint32_t line = (uint32_t)(((mi & 1) * CH + ch) * 8 + rr);
 #pragma unroll
@@ -461,7 +504,7 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
         const float sgf = h2 ? sg.y : sg.x, suf = h2 ? su.y : su.x;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          const uint4 xb = xrow[j] >= 0 ? u.xh[xrow[j] + 4 * J + t4] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 xb = xrow[j] >= 0 ? lds_v4(u.xh_a + 16u * (uint32_t)(xrow[j] + 4 * J + t4)) : make_uint4(0u, 0u, 0u, 0u);
           float dg[4];
           mma_group(dg, h2 ? wg1 : wg0, h2 ? wu1 : wu0, xb);
           C[j][0] = fmaf(sgf, dg[0], C[j][0]);
@@ -477,9 +520,9 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvUnitComputed] = gtimer();
   if (tw == 0 && lane == 0 && u.timeline && i == u.i0 + kDlTeams)
     u.timeline[(size_t)u.c * kDlEvents + kEvSecondComputed] = gtimer();
-  float4* my_p = u.pgu + (size_t)(team * kDlTeamWarps + tw) * NT * 32;
+  const uint32_t my_p = u.pgu_a + 16u * (uint32_t)((team * kDlTeamWarps + tw) * NT * 32);
 #pragma unroll
-  for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
+  for (int j = 0; j < NT; ++j) sts_f4(my_p + 16u * (uint32_t)(j * 32 + lane), make_float4(C[j][0], C[j][1], C[j][2], C[j][3]));
   team_sync(team);
   if (tw == 0 && lane == 0 && u.timeline && i == u.i0) u.timeline[(size_t)u.c * kDlEvents + kEvUnitReduced] = gtimer();
   // team thread (j, ln): column ln / 4 of the unit, slot-local tokens 8 j + 2 (ln % 4) (+ 1); the
@@ -490,10 +533,10 @@ __device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, 
   if (tt < NT * 32) {  // whole warps
     const int j = tt >> 5, ln = tt & 31;
     const int col = ln >> 2, n0 = 8 * j + 2 * (ln & 3);
-    float4 sum = u.pgu[((size_t)(team * kDlTeamWarps) * NT + j) * 32 + ln];
+    float4 sum = lds_f4(u.pgu_a + 16u * (uint32_t)(((team * kDlTeamWarps) * NT + j) * 32 + ln));
 #pragma unroll
     for (int q = 1; q < kDlTeamWarps; ++q) {
-      const float4 pp = u.pgu[((size_t)(team * kDlTeamWarps + q) * NT + j) * 32 + ln];
+      const float4 pp = lds_f4(u.pgu_a + 16u * (uint32_t)(((team * kDlTeamWarps + q) * NT + j) * 32 + ln));
       sum.x += pp.x;
       sum.y += pp.y;
       sum.z += pp.z;
@@ -552,7 +595,7 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
     }
     const unsigned ept = (unsigned)(u.ep_tag >> 32);
     const unsigned long long* src = u.hw + (size_t)hrow0 * (u.f / 2);
-    uint2* hdst = reinterpret_cast<uint2*>(stg + u.dn_h_off);  // [n_s][f/4] pairs of words' payloads
+    const uint32_t hdst = tc::smem_u32(stg) + (uint32_t)u.dn_h_off;  // [n_s][f/4] pairs of words' payloads
     const int npair = n_s * (u.f / 4), tt = tw * 32 + lane;
     bool okh = true;
 #pragma unroll 1
@@ -588,22 +631,22 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int pi = base + tt + q * kDlTeamWarps * 32;
-        if (pi < npair) hdst[pi] = make_uint2((uint32_t)w[2 * q], (uint32_t)w[2 * q + 1]);
+        if (pi < npair) sts_v2(hdst + 8u * (uint32_t)pi, make_uint2((uint32_t)w[2 * q], (uint32_t)w[2 * q + 1]));
       }
     }
     // (also the team barrier that makes the h rows visible to the team)
     if (!team_all(team, okh && !*u.abort)) return false;
   }
   const uint32_t sbase = tc::smem_u32(stg);
-  const __half* dsc = reinterpret_cast<const __half*>(stg + u.dn_scale_off);  // [RB][GF]
-  const uint4* hrows = reinterpret_cast<const uint4*>(stg + u.dn_h_off);     // [n_s][f/8]
-  const signed char* tp = u.tpos + s * kDlMaxT;
+  const uint32_t dsc = sbase + (uint32_t)u.dn_scale_off;  // [RB][GF] fp16
+  const uint32_t hrows = sbase + (uint32_t)u.dn_h_off;    // [n_s][f/8] 16-byte blocks
+  const uint32_t tp = u.tpos_a + (uint32_t)(s * kDlMaxT);
   const int RB = u.RB, GF = u.GF;
   int hpos[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int n = 8 * j + g8;
-    hpos[j] = n < u.T ? (int)tp[n] * (u.f / 8) : -1;
+    hpos[j] = n < u.T ? lds_s8(tp + (uint32_t)n) * (u.f / 8) : -1;
   }
   const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
   const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
@@ -614,10 +657,10 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
     const uint32_t line = u.dn_swap ? (uint32_t)(chd * RB + rrow) : (uint32_t)(rrow * u.CHd + chd);
     uint32_t wa, wb;
     ldsm_x2(sbase + swz(line, (uint32_t)sub), wa, wb);
-    const float sa = __half2float(dsc[rga * GF + jg]), sb = __half2float(dsc[rgb * GF + jg]);
+    const float sa = lds_h2f(dsc + 2u * (uint32_t)(rga * GF + jg)), sb = lds_h2f(dsc + 2u * (uint32_t)(rgb * GF + jg));
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const uint4 hb = hpos[j] >= 0 ? hrows[hpos[j] + 4 * jg + t4] : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 hb = hpos[j] >= 0 ? lds_v4(hrows + 16u * (uint32_t)(hpos[j] + 4 * jg + t4)) : make_uint4(0u, 0u, 0u, 0u);
       float dd[4];
       mma_group(dd, wa, wb, hb);
       D[j][0] = fmaf(sa, dd[0], D[j][0]);
@@ -635,7 +678,7 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
 template <int NT>  // n8 token tiles: 1 (T <= 8) or 2 (T <= 16)
 __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArgs a, const __grid_constant__ DlMaps m) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   const int T = a.T, d = a.d, E = a.E, K = a.K, f = a.f;
   const int nc = gridDim.x, c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -710,6 +753,12 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     u.ring = ring;
     u.xh = xh;
     u.pgu = pgu;
+    u.ring_a = tc::smem_u32(ring);
+    u.xh_a = tc::smem_u32(xh);
+    u.pgu_a = tc::smem_u32(pgu);
+    u.perm_a = tc::smem_u32(perm_s);
+    u.w_a = tc::smem_u32(w_s);
+    u.tpos_a = tc::smem_u32(tpos);
     u.slot_s = slot_s;
     u.perm_s = perm_s;
     u.w_s = w_s;
@@ -1279,20 +1328,19 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     if (ctid == 0) DL_STAMP(kEvDownDone);
 
     // ---- y rows [r0, r0 + nr): the 16 warps' partial sums in warp order (+ residual)
-    float4* my_p = pgu + (size_t)warp * NT * 32;
+    const uint32_t pgu_a = tc::smem_u32(pgu);
 #pragma unroll
-    for (int j = 0; j < NT; ++j) my_p[j * 32 + lane] = make_float4(D[j][0], D[j][1], D[j][2], D[j][3]);
+    for (int j = 0; j < NT; ++j)
+      sts_f4(pgu_a + 16u * (uint32_t)((warp * NT + j) * 32 + lane), make_float4(D[j][0], D[j][1], D[j][2], D[j][3]));
     consumers_sync();
     for (int i = ctid; i < nr * T; i += kDlWarps * 32) {
       const int n = i / nr, r = i - n * nr;
       const int j = n >> 3, nn = n & 7;
       const int ln = (r & 7) * 4 + (nn >> 1), comp = (r >> 3) * 2 + (nn & 1);
       float v = 0.f;
-#pragma unroll 4
-      for (int q = 0; q < kDlWarps; ++q) {
-        const float4 pp = pgu[((size_t)q * NT + j) * 32 + ln];
-        v += comp == 0 ? pp.x : comp == 1 ? pp.y : comp == 2 ? pp.z : pp.w;
-      }
+      const uint32_t pb = pgu_a + (uint32_t)((j * 32 + ln) * 16 + comp * 4);
+#pragma unroll
+      for (int q = 0; q < kDlWarps; ++q) v += lds_f32(pb + (uint32_t)(q * NT * 32 * 16));
       const size_t o = (size_t)n * d + r0 + r;
       if (ok) {
         if (a.resid) v = resid_s[n * nr + r] + v;
