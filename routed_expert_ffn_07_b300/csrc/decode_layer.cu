@@ -1011,17 +1011,19 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
       if (ctid == 0) DL_STAMP(kEvRouterRows);
       if (ok && r_on) {
         const int bb = (int)((long long)NB * my_pt / nparts), be = (int)((long long)NB * (my_pt + 1) / nparts);
-        const float4* wr = reinterpret_cast<const float4*>(wr_s + (size_t)my_e * d);
+        const uint32_t wr = tc::smem_u32(wr_s) + (uint32_t)(my_e * d * 4);
+        const uint32_t xa = tc::smem_u32(xh);
 #pragma unroll 1
         for (int t0 = 0; t0 < T; t0 += 4) {
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
           for (int b = bb + lane; b < be; b += 32) {
-            const float4 wa = wr[2 * b], wb = wr[2 * b + 1];
+            const float4 wa = lds_f4(wr + 32u * (uint32_t)b), wb = lds_f4(wr + 32u * (uint32_t)b + 16u);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int t = min(t0 + q, T - 1);  // past T: a repeated token, not stored
-              const uint4 xv = xh[(size_t)t * XS + b];
+              if (t0 + q >= T) break;  // (warp-uniform)
+              const int t = t0 + q;
+              const uint4 xv = lds_v4(xa + 16u * (uint32_t)(t * XS + b));
               const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));  // x0, x4
               const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));  // x1, x5
               const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&xv.z));  // x2, x6
