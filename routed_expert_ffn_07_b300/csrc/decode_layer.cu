@@ -179,10 +179,10 @@ __device__ __forceinline__ void st_relaxed_gpu(unsigned long long* p, unsigned l
 }
 
 // ------------------------------------------------------------------ shared-memory accesses
-// Explicit shared-space loads and stores by 32-bit shared address.  The kernel's dynamic shared
-// memory is reached through pointers the compiler cannot prove to be shared (aligned at run time,
-// kept in the shared context of the units), and its generic loads from shared memory cost several
-// times an ld.shared on this part; the hot paths use these instead.
+// Explicit shared-space loads and stores by 32-bit shared address.  The units' code reaches the
+// kernel's dynamic shared memory through pointers kept in their shared context, which the compiler
+// cannot prove to be shared, and generic loads from shared memory cost several times an ld.shared
+// on this part; the hot paths use these instead.
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -440,7 +440,7 @@ struct UnitCtx {
 // partial tiles in warp order, and publish h = w silu(gate) up (fp16) of its 8 columns and tokens.
 // Returns false when a wait gave up (uniform over the team).
 template <int NT>
-__device__ __noinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, int lane) {
+__device__ __forceinline__ bool gu_unit(const UnitCtx& u, int i, int team, int tw, int lane) {
   const int g8 = lane >> 2, t4 = lane & 3;
   const int st = i % u.NS;
   // the unit's slot and tokens, while its bytes may still be landing
