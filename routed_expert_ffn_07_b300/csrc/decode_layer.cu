@@ -572,10 +572,11 @@ __device__ __forceinline__ bool gu_unit(const UnitCtx& u, int i, int team, int t
 // rows of this CTA's outputs, copy the slot's h rows from their epoch-tagged words into the stage
 // (polling words whose tag is not yet this launch's), and add this warp's quarter of the slot's
 // 32-column groups into the warp's accumulators D (rows g / g + 8 of the CTA's output tile, all T
-// tokens as N; a token not in the slot contributes zeros); free the stage.  Returns false when a
-// wait gave up.
+// tokens as N; a token not in the slot contributes zeros); free the stage.  With two token tiles
+// (T > 8) an item covers at most 8 of the slot's tokens, slot-local 8 half .. 8 half + 7, so that a
+// stage holds the h rows of 8 tokens at most.  Returns false when a wait gave up.
 template <int NT>
-__device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int team, int tw, int lane,
+__device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int half, int team, int tw, int lane,
                                           float (&D)[NT][4]) {
   const int g8 = lane >> 2, t4 = lane & 3;
   const int st = k % u.NS;
@@ -592,6 +593,10 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
       const int4 sl = u.slot_s[s - u.HS];
       n_s = sl.z;
       hrow0 = u.HS * u.T + sl.y;
+    }
+    if constexpr (NT == 2) {  // the item's half of the slot: slot-local tokens 8 half .. 8 half + 7
+      n_s = half ? n_s - 8 : min(n_s, 8);
+      hrow0 += 8 * half;
     }
     const unsigned ept = (unsigned)(u.ep_tag >> 32);
     const unsigned long long* src = u.hw + (size_t)hrow0 * (u.f / 2);
@@ -646,7 +651,12 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int te
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int n = 8 * j + g8;
-    hpos[j] = n < u.T ? lds_s8(tp + (uint32_t)n) * (u.f / 8) : -1;
+    if constexpr (NT == 2) {  // the token's row among the item's staged rows, or -1
+      const int pr = n < u.T ? lds_s8(tp + (uint32_t)n) - 8 * half : -1;
+      hpos[j] = pr >= 0 && pr < 8 ? pr * (u.f / 8) : -1;
+    } else {
+      hpos[j] = n < u.T ? lds_s8(tp + (uint32_t)n) * (u.f / 8) : -1;
+    }
   }
   const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
   const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
@@ -722,6 +732,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
   __shared__ volatile int s_abort;
   __shared__ unsigned s_ep;
   __shared__ int s_nact, s_issued;
+  __shared__ int s_big[64], s_nbig;  // T > 8: the slots with more than 8 tokens (their second down items)
   __shared__ float lpart[kDlWarps * kDlMaxT];
   __shared__ float inv_s[kDlMaxT];
   __shared__ float bias_s[kDlRowsMax];                 // this CTA's router bias entries
@@ -749,6 +760,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     tc::mbar_init(&route_ready, 1);
     s_abort = 0;
     s_issued = 0;
+    s_nbig = 0;
     UnitCtx& u = uc_s;
     u.ring = ring;
     u.xh = xh;
@@ -829,6 +841,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     const int nact = ok ? s_nact : 0;
     if (lane == 0) DL_STAMP(kEvProducerRouted);
     const int nslots = HS + nact;
+    const int nitems = nslots + (NT == 2 && ok ? s_nbig : 0);  // down items
     const int total_units = nslots * fu;
     const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
     if (lane == 0) DL_STAMP(kEvProducerGo);
@@ -880,8 +893,9 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     {
       int q = 0;
 #pragma unroll 1
-      for (; ok && q < nslots; ++q) {
+      for (; ok && q < nitems; ++q) {
         const int item = nG + q, st = item % NS;
+        const int sq = q < nslots ? q : s_big[q - nslots];  // the item's slot
         if (item >= NS &&
             !__all_sync(0xffffffffu, tc::mbar_wait_sleepy(&empty[st], ((item / NS) & 1) ^ 1u, &s_abort, kDlProducerSleep))) {
           ok = false;
@@ -890,14 +904,14 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         if (lane == 0) {
           const CUtensorMap *mq, *ms;
           int drow;
-          if (q < HS) {
+          if (sq < HS) {
             mq = &m.sh_dn_q;
             ms = &m.sh_dn_s;
             drow = r0;
           } else {
             mq = &m.dn_q;
             ms = &m.dn_s;
-            drow = slot_s[q - HS].x * d + r0;
+            drow = slot_s[sq - HS].x * d + r0;
           }
           uint8_t* dst = ring + (size_t)st * SB;
           tc::mbar_arrive_expect_tx(&full[st], (uint32_t)(dn_code_bytes + RB * GF * 2));
@@ -907,7 +921,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
             tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
           tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
           if (q == 0) DL_STAMP(kEvFirstDownIssued);
-          if (q == nslots - 1) DL_STAMP(kEvLastDownIssued);
+          if (q == nitems - 1) DL_STAMP(kEvLastDownIssued);
         }
       }
       if (lane == 0) s_issued = nG + q;
@@ -1250,6 +1264,21 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
         // the keys are done with: the producer's bulk copies may overwrite them
         tc::fence_proxy_async_smem();
         group_sync(gn);
+        if (NT == 2 && gw == 0) {
+          // the slots with more than 8 tokens, ascending: each has a second down item (tokens 8..)
+          const int ns_all = HS + s_nact;
+          int nb = 0;
+#pragma unroll 1
+          for (int b = 0; b < ns_all; b += 32) {
+            const int sl = b + lane;
+            const bool big = sl < ns_all && (sl < HS ? T : slot_s[sl - HS].z) > 8;
+            const unsigned bm = __ballot_sync(0xffffffffu, big);
+            if (big) s_big[nb + __popc(bm & ((1u << lane) - 1u))] = sl;
+            nb += __popc(bm);
+          }
+          if (lane == 0) s_nbig = nb;
+          __syncwarp();
+        }
         if (gt == 0) {
           DL_STAMP(kEvDispatched);
           DL_STAMP(kEvRouted);
@@ -1302,6 +1331,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     }
 
     const int nslots = HS + (ok ? s_nact : 0);
+    const int nitems = nslots + (NT == 2 && ok ? s_nbig : 0);  // down items: every slot, then second halves
     const int total_units = nslots * fu;
     const int nG = total_units > c ? (total_units - c + nc - 1) / nc : 0;
 
@@ -1312,16 +1342,17 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 #pragma unroll
     for (int j = 0; j < NT; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
 #pragma unroll 1
-    for (int k = team; ok && k < nG + nslots; k += kDlTeams) {
+    for (int k = team; ok && k < nG + nitems; k += kDlTeams) {
       if (k < nG) {
         ok = gu_unit<NT>(*uc, k, team, tw, lane);
         if (k + kDlTeams >= nG && tw == 0 && lane == 0) DL_STAMP(kEvUnitsDone);  // this team's last unit
       } else {
         if (k - nG < kDlTeams && tw == 0 && lane == 0 && team == 0) DL_STAMP(kEvFirstDown);
-        ok = down_item<NT>(*uc, k, k - nG, team, tw, lane, D);
+        const int q = k - nG;
+        ok = down_item<NT>(*uc, k, q < nslots ? q : s_big[q - nslots], q < nslots ? 0 : 1, team, tw, lane, D);
         if (tw == 0 && lane == 0) {
           if (k == nG) DL_STAMP(kEvFirstDownDone);
-          if (k == nG + nslots - 1) DL_STAMP(kEvLastDownDone);
+          if (k == nG + nitems - 1) DL_STAMP(kEvLastDownDone);
         }
       }
     }
@@ -1437,8 +1468,9 @@ static DlPlan dl_plan(int T, int d, int f, int E, int K, int nsm) {
   const int RB = p.rows_box;
   const size_t gu = (size_t)(d / 256) * 2048 + 2 * 8 * (d / 32) * 2;
   const size_t dn_codes = (size_t)RB * (f / 2);
+  // a down item stages the h rows of at most 8 tokens (a slot with more tokens is two items)
   const size_t dn = ((((dn_codes + 127) & ~size_t(127)) + (size_t)RB * (f / 32) * 2 + 127) & ~size_t(127)) +
-                    (size_t)T * f * 2;
+                    (size_t)std::min(T, 8) * f * 2;
   p.stage_bytes = (int)((std::max(gu, dn) + 1023) & ~size_t(1023));
   const int NT = T > 8 ? 2 : 1;
   const size_t fixed = 1024 /* alignment */ + (size_t)T * (d / 8 + kDlXPad) * 16 + (size_t)kDlWarps * NT * 32 * 16 +
