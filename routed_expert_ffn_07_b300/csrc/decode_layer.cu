@@ -504,7 +504,6 @@ __device__ __forceinline__ bool gu_unit(const UnitCtx& u, int i, int team, int t
         const float sgf = h2 ? sg.y : sg.x, suf = h2 ? su.y : su.x;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          if (NT == 2 && j == 1 && n_s <= 8) break;  // the slot's tokens fit in the first n8 tile
           const uint4 xb = xrow[j] >= 0 ? lds_v4(u.xh_a + 16u * (uint32_t)(xrow[j] + 4 * J + t4)) : make_uint4(0u, 0u, 0u, 0u);
           float dg[4];
           mma_group(dg, h2 ? wg1 : wg0, h2 ? wu1 : wu0, xb);
@@ -659,9 +658,6 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int ha
       hpos[j] = n < u.T ? lds_s8(tp + (uint32_t)n) * (u.f / 8) : -1;
     }
   }
-  bool tile_on[NT];  // n8 token tiles holding a token of the item (the others add zeros)
-#pragma unroll
-  for (int j = 0; j < NT; ++j) tile_on[j] = NT == 1 || __any_sync(0xffffffffu, hpos[j] >= 0);
   const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
   const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
   const int jb = tw * GF / kDlTeamWarps, je = (tw + 1) * GF / kDlTeamWarps;
@@ -674,7 +670,6 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int ha
     const float sa = lds_h2f(dsc + 2u * (uint32_t)(rga * GF + jg)), sb = lds_h2f(dsc + 2u * (uint32_t)(rgb * GF + jg));
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      if (!tile_on[j]) continue;
       const uint4 hb = hpos[j] >= 0 ? lds_v4(hrows + 16u * (uint32_t)(hpos[j] + 4 * jg + t4)) : make_uint4(0u, 0u, 0u, 0u);
       float dd[4];
       mma_group(dd, wa, wb, hb);
