@@ -168,8 +168,12 @@ moe_status moe_usage_enable(moe_handle h, int on);
 moe_status moe_usage_read(moe_handle h, unsigned long long* counts_host, int reset, void* stream);
 
 /* End-to-end form of moe_layer_forward for HOST buffers: copies x_host to the device, runs the
- * layer, copies the result to y_host and synchronises `stream`.  x_host / y_host should be
- * page-locked for the copies to be asynchronous.  Blocks the calling thread until done. */
+ * layer, copies the result to y_host and synchronises `stream`.  When both buffers are page-locked
+ * and mapped into the device's address space (cudaHostAlloc / cudaHostRegister under unified
+ * addressing) and hold at most 256 KiB, a small kernel moves the bytes over the host link with loads
+ * and stores; otherwise two cudaMemcpyAsync transfers do (pageable buffers work, synchronously).
+ * Either way x_host is read and y_host written exactly once per call.  Blocks the calling thread
+ * until done. */
 moe_status moe_layer_forward_host(moe_handle h, int layer, const void* x_host, int T, void* y_host,
                                   void* stream);
 

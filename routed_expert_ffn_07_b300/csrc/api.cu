@@ -52,6 +52,52 @@ constexpr int kFusedDefaultTokens = 16;   // decode, 1 + 3 verify and small conc
 
 using namespace moe;
 
+// ------------------------------------------------------------------ host-link copies
+// Page-locked host memory mapped into the device's address space is read and written by a kernel
+// directly; for the few KB of a decode step's activations this avoids two copy-engine transfers.
+constexpr size_t kHostLinkMaxBytes = 256 * 1024;
+
+__global__ void __launch_bounds__(256) host_link_copy_kernel(uint8_t* dst, const uint8_t* src, size_t n, int vec) {
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x, nt = (size_t)gridDim.x * blockDim.x;
+  size_t done = 0;
+  if (vec) {  // both ends 16-byte aligned
+    const size_t nw = n / 16;
+    for (size_t i = t; i < nw; i += nt) reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    done = nw * 16;
+  }
+  for (size_t i = done + t; i < n; i += nt) dst[i] = src[i];
+}
+
+static cudaError_t launch_host_link_copy(void* dst, const void* src, size_t n, cudaStream_t st) {
+  const int vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+  const size_t units = vec ? (n + 15) / 16 : n;
+  const unsigned grid = (unsigned)std::max<size_t>(1, std::min<size_t>(64, (units + 255) / 256));
+  host_link_copy_kernel<<<grid, 256, 0, st>>>(static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src), n, vec);
+  return cudaGetLastError();
+}
+
+// The device address of page-locked, device-mapped host memory p, or null when p is anything else
+// (pageable memory, device memory, another device's allocation).
+static void* host_device_view(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  int mapped = 0;
+  if (cudaDeviceGetAttribute(&mapped, cudaDevAttrCanMapHostMemory, dev) != cudaSuccess || !mapped) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.devicePointer;
+}
+
 struct LayerW {
   moe_layer_weights w;
   bool set = false;
@@ -484,9 +530,19 @@ moe_status moe_layer_forward_host(moe_handle h, int layer, const void* x_host, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)T * h->cfg.d * act_size(h->cfg.act);
   CUDA_TRY(cudaGetLastError());
-  CUDA_TRY(cudaMemcpyAsync(h->host_x, x_host, bytes, cudaMemcpyHostToDevice, st));
-  CUDA_TRY(enqueue_layer(h, layer, h->host_x, T, h->host_y, nullptr, false, st));
-  CUDA_TRY(cudaMemcpyAsync(y_host, h->host_y, bytes, cudaMemcpyDeviceToHost, st));
+  // A decode step's few KB cross the host link faster as loads and stores of a small kernel than as
+  // two copy-engine transfers, when both buffers are page-locked and mapped into the device's space
+  void* xd = bytes <= kHostLinkMaxBytes ? host_device_view(x_host) : nullptr;
+  void* yd = xd ? host_device_view(y_host) : nullptr;
+  if (xd && yd) {
+    CUDA_TRY(launch_host_link_copy(h->host_x, xd, bytes, st));
+    CUDA_TRY(enqueue_layer(h, layer, h->host_x, T, h->host_y, nullptr, false, st));
+    CUDA_TRY(launch_host_link_copy(yd, h->host_y, bytes, st));
+  } else {
+    CUDA_TRY(cudaMemcpyAsync(h->host_x, x_host, bytes, cudaMemcpyHostToDevice, st));
+    CUDA_TRY(enqueue_layer(h, layer, h->host_x, T, h->host_y, nullptr, false, st));
+    CUDA_TRY(cudaMemcpyAsync(y_host, h->host_y, bytes, cudaMemcpyDeviceToHost, st));
+  }
   CUDA_TRY(cudaStreamSynchronize(st));
   return MOE_OK;
 }

@@ -219,6 +219,40 @@ def test_decode_layer_full_size(decode_layer):
         np.testing.assert_array_equal(yh, from_torch_act(y))
 
 
+def test_host_entry_point_pinned_and_pageable_buffers(decode_layer):
+    """moe_layer_forward_host moves page-locked, device-mapped buffers with a small kernel over the
+    host link and pageable ones with copies: both must give moe_layer_forward's bits, T = 1, 5, 16,
+    including a pinned buffer at an odd byte offset (the byte-wise form of the kernel)."""
+    torch = _torch()
+    from routed_expert_ffn_07_b300 import capi
+    wl, wts, h = decode_layer
+    x_all = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=11)
+    for T in (1, 5, 16):
+        x = np.ascontiguousarray(x_all[:T])
+        y = torch.empty((T, wl.d), dtype=torch.bfloat16, device="cuda")
+        capi.moe_layer_forward(h, 0, to_torch_act(x), T, y)
+        torch.cuda.synchronize()
+        ref = from_torch_act(y)
+        # pageable numpy buffers: the copy path
+        yn = np.zeros_like(x)
+        capi.moe_layer_forward_host(h, 0, x, T, yn)
+        np.testing.assert_array_equal(yn, ref)
+        # page-locked torch buffers: the kernel path
+        xp = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+        yp = torch.zeros_like(xp).pin_memory()
+        capi.moe_layer_forward_host(h, 0, xp, T, yp)
+        np.testing.assert_array_equal(yp.numpy().view(np.uint16), ref)
+        # pinned, but one byte into the allocation: byte-wise loads and stores
+        nb = x.nbytes
+        xb = torch.zeros(nb + 1, dtype=torch.uint8).pin_memory()
+        yb = torch.zeros(nb + 1, dtype=torch.uint8).pin_memory()
+        xb[1:] = torch.from_numpy(x.view(np.uint8).reshape(-1).copy())
+        capi.moe_layer_forward_host(h, 0, xb.data_ptr() + 1, T, yb.data_ptr() + 1)
+        assert capi.moe_get_device_status(h) == 0
+        np.testing.assert_array_equal(yb[1:].numpy().view(np.uint16).reshape(T, wl.d), ref)
+        assert int(yb[0]) == 0  # nothing written before y
+
+
 def test_decode_layer_batch_sizes(decode_layer):
     wl, wts, h = decode_layer
     x = inputs.gen_activations(wl.seed, 16, wl.d, "bf16", layer=5)
