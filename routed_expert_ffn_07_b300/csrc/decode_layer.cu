@@ -219,6 +219,14 @@ __device__ __forceinline__ void sts_f4(uint32_t a, float4 v) {
 __device__ __forceinline__ void sts_v2(uint32_t a, uint2 v) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v.x), "r"(v.y) : "memory");
 }
+__device__ __forceinline__ int lds_acquire_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_release_s32(uint32_t a, int v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 
 // Named barriers: 1 = the 512 consumer threads, 2 + team = the 128 threads of a gate/up team,
 // 6 = the routing group (below).
@@ -419,6 +427,7 @@ struct UnitCtx {
   const uint4* xh;        // [T][XS] x fragments
   float4* pgu;            // [16 warps][NT][32] partial tiles
   uint32_t ring_a, xh_a, pgu_a, perm_a, w_a, tpos_a;  // the same regions as shared addresses
+  uint32_t avail_a;  // shared int: ring items whose copies the producer has issued (down items)
   const int4* slot_s;     // routed slots {expert, start, count, 0}
   const int* perm_s;
   const float* w_s;
@@ -684,6 +693,140 @@ __device__ __forceinline__ bool down_item(const UnitCtx& u, int k, int s, int ha
   return true;
 }
 
+// The same down item taken by one warp alone, over all of the slot's groups (used when a CTA has
+// at most 16 down items, so that they all run at once): wait for the slot's down rows of this
+// CTA's outputs, copy the slot's h rows from their epoch-tagged words into the stage (polling words
+// whose tag is not yet this launch's), and add all of the slot's 32-column groups into the warp's
+// accumulators D (rows g / g + 8 of the CTA's output tile, all T tokens as N; a token not in the
+// slot contributes zeros); free the stage.  With two token tiles (T > 8) an item covers at most 8 of
+// the slot's tokens, slot-local 8 half .. 8 half + 7, so that a stage holds the h rows of 8 tokens
+// at most.  Returns false (uniformly over the warp) when a wait gave up.
+template <int NT>
+__device__ __forceinline__ bool down_item_warp(const UnitCtx& u, int k, int s, int half, int lane,
+                                               float (&D)[NT][4]) {
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int st = k % u.NS;
+  // A parity wait tells a phase only from the one before it: a warp that came to this item early
+  // could see the stage's previous phase (item k - NS) still pending and take it for this one.  Once
+  // the producer has issued item k, item k - NS is consumed and its phase complete.
+  {
+    int ready = 1;
+    if (lane == 0) {
+      unsigned polls = 0;
+      while (lds_acquire_s32(u.avail_a) <= k) {
+        if (++polls > kDlSpinLimit || *u.abort) {
+          ready = 0;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+  }
+  // every lane polls the barrier, so every lane acquires the landed rows
+  if (!tc::mbar_wait_all(&u.full[st], (k / u.NS) & 1, u.abort)) return false;
+  if (__any_sync(0xffffffffu, *u.abort != 0)) return false;
+  uint8_t* stg = u.ring + (size_t)st * u.SB;
+  {
+    // the stage is this item's (its weights landed, so its previous item is done with it)
+    int n_s, hrow0;
+    if (s < u.HS) {
+      n_s = u.T;
+      hrow0 = 0;
+    } else {
+      const int4 sl = u.slot_s[s - u.HS];
+      n_s = sl.z;
+      hrow0 = u.HS * u.T + sl.y;
+    }
+    if constexpr (NT == 2) {  // the item's half of the slot: slot-local tokens 8 half .. 8 half + 7
+      n_s = half ? n_s - 8 : min(n_s, 8);
+      hrow0 += 8 * half;
+    }
+    const unsigned ept = (unsigned)(u.ep_tag >> 32);
+    const unsigned long long* src = u.hw + (size_t)hrow0 * (u.f / 2);
+    const uint32_t hdst = tc::smem_u32(stg) + (uint32_t)u.dn_h_off;  // [n_s][f/4] pairs of words' payloads
+    const int npair = n_s * (u.f / 4);
+    bool okh = true;
+#pragma unroll 1
+    for (int base = 0; okh && base < npair; base += 4 * 32) {
+      unsigned long long w[8];
+      int pending = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pi = base + lane + q * 32;
+        if (pi < npair)
+          ld_relaxed_gpu_v2(src + 2 * pi, w[2 * q], w[2 * q + 1]);
+        else
+          w[2 * q] = w[2 * q + 1] = u.ep_tag;
+        pending += ((unsigned)(w[2 * q] >> 32) != ept) + ((unsigned)(w[2 * q + 1] >> 32) != ept);
+      }
+      unsigned polls = 0;
+      while (pending) {
+        if (++polls > kDlSpinLimit || *u.abort) {
+          okh = false;
+          break;
+        }
+        __nanosleep(32);
+        pending = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int pi = base + lane + q * 32;
+          if ((unsigned)(w[2 * q] >> 32) != ept || (unsigned)(w[2 * q + 1] >> 32) != ept) {
+            ld_relaxed_gpu_v2(src + 2 * pi, w[2 * q], w[2 * q + 1]);
+            pending += ((unsigned)(w[2 * q] >> 32) != ept) + ((unsigned)(w[2 * q + 1] >> 32) != ept);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pi = base + lane + q * 32;
+        if (pi < npair) sts_v2(hdst + 8u * (uint32_t)pi, make_uint2((uint32_t)w[2 * q], (uint32_t)w[2 * q + 1]));
+      }
+    }
+    if (!__all_sync(0xffffffffu, okh && !*u.abort)) return false;
+    __syncwarp();  // the h rows are visible to the warp
+  }
+  const uint32_t sbase = tc::smem_u32(stg);
+  const uint32_t dsc = sbase + (uint32_t)u.dn_scale_off;  // [RB][GF] fp16
+  const uint32_t hrows = sbase + (uint32_t)u.dn_h_off;    // [n_s][f/8] 16-byte blocks
+  const uint32_t tp = u.tpos_a + (uint32_t)(s * kDlMaxT);
+  const int RB = u.RB, GF = u.GF;
+  int hpos[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int n = 8 * j + g8;
+    if constexpr (NT == 2) {  // the token's row among the item's staged rows, or -1
+      const int pr = n < u.T ? lds_s8(tp + (uint32_t)n) - 8 * half : -1;
+      hpos[j] = pr >= 0 && pr < 8 ? pr * (u.f / 8) : -1;
+    } else {
+      hpos[j] = n < u.T ? lds_s8(tp + (uint32_t)n) * (u.f / 8) : -1;
+    }
+  }
+  const int rga = min(g8, RB - 1), rgb = min(g8 + 8, RB - 1);
+  const int rrow = min((lane & 7) + 8 * ((lane >> 3) & 1), RB - 1);  // ldmatrix row address of this lane
+#pragma unroll 2
+  for (int jg = 0; jg < GF; ++jg) {
+    const int chd = jg >> 3, sub = jg & 7;
+    const uint32_t line = u.dn_swap ? (uint32_t)(chd * RB + rrow) : (uint32_t)(rrow * u.CHd + chd);
+    uint32_t wa, wb;
+    ldsm_x2(sbase + swz(line, (uint32_t)sub), wa, wb);
+    const float sa = lds_h2f(dsc + 2u * (uint32_t)(rga * GF + jg)), sb = lds_h2f(dsc + 2u * (uint32_t)(rgb * GF + jg));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const uint4 hb = hpos[j] >= 0 ? lds_v4(hrows + 16u * (uint32_t)(hpos[j] + 4 * jg + t4)) : make_uint4(0u, 0u, 0u, 0u);
+      float dd[4];
+      mma_group(dd, wa, wb, hb);
+      D[j][0] = fmaf(sa, dd[0], D[j][0]);
+      D[j][1] = fmaf(sa, dd[1], D[j][1]);
+      D[j][2] = fmaf(sb, dd[2], D[j][2]);
+      D[j][3] = fmaf(sb, dd[3], D[j][3]);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive_cnt(&u.empty[st], kDlWarps);  // the stage is free (one warp)
+  return true;
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int NT>  // n8 token tiles: 1 (T <= 8) or 2 (T <= 16)
 __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArgs a, const __grid_constant__ DlMaps m) {
@@ -731,7 +874,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
   __shared__ int s_ncand;
   __shared__ volatile int s_abort;
   __shared__ unsigned s_ep;
-  __shared__ int s_nact, s_issued;
+  __shared__ int s_nact, s_issued, s_avail;
   __shared__ int s_big[64], s_nbig;  // T > 8: the slots with more than 8 tokens (their second down items)
   __shared__ float lpart[kDlWarps * kDlMaxT];
   __shared__ float inv_s[kDlMaxT];
@@ -760,6 +903,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     tc::mbar_init(&route_ready, 1);
     s_abort = 0;
     s_issued = 0;
+    s_avail = 0;
     s_nbig = 0;
     UnitCtx& u = uc_s;
     u.ring = ring;
@@ -771,6 +915,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
     u.perm_a = tc::smem_u32(perm_s);
     u.w_a = tc::smem_u32(w_s);
     u.tpos_a = tc::smem_u32(tpos);
+    u.avail_a = tc::smem_u32(&s_avail);
     u.slot_s = slot_s;
     u.perm_s = perm_s;
     u.w_s = w_s;
@@ -920,6 +1065,7 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
           else
             tc::tma_load_3d(dst, mq, 0, 0, drow, &full[st]);
           tc::tma_load_2d(dst + dn_scale_off, ms, 0, drow, &full[st]);
+          sts_release_s32(tc::smem_u32(&s_avail), item + 1);  // item's copies are issued
           if (q == 0) DL_STAMP(kEvFirstDownIssued);
           if (q == nitems - 1) DL_STAMP(kEvLastDownIssued);
         }
@@ -1337,12 +1483,14 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
 
     // ---- phase 3: this CTA's items in order -- its gate/up units, then the down items of every
     // slot; team (k % 4) takes item k.  A team finishes all its gate/up units before any of its down
-    // items, so the slots' h rows (everywhere) do not wait on a down item.
+    // items, so the slots' h rows (everywhere) do not wait on a down item.  With at most 16 down
+    // items (one token) each is taken by one warp instead (warp q takes down item q), all at once.
     float D[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
+    const bool warp_items = nitems <= kDlWarps;
 #pragma unroll 1
-    for (int k = team; ok && k < nG + nitems; k += kDlTeams) {
+    for (int k = team; ok && k < nG + (warp_items ? 0 : nitems); k += kDlTeams) {
       if (k < nG) {
         ok = gu_unit<NT>(*uc, k, team, tw, lane);
         if (k + kDlTeams >= nG && tw == 0 && lane == 0) DL_STAMP(kEvUnitsDone);  // this team's last unit
@@ -1354,6 +1502,15 @@ __global__ void __launch_bounds__(kDlThreads, 1) decode_layer_kernel(const DlArg
           if (k == nG) DL_STAMP(kEvFirstDownDone);
           if (k == nG + nitems - 1) DL_STAMP(kEvLastDownDone);
         }
+      }
+    }
+    if (warp_items && ok && warp < nitems) {
+      const int q = warp;
+      if (q == 0 && lane == 0) DL_STAMP(kEvFirstDown);
+      ok = down_item_warp<NT>(*uc, nG + q, q < nslots ? q : s_big[q - nslots], q < nslots ? 0 : 1, lane, D);
+      if (lane == 0) {
+        if (q == 0) DL_STAMP(kEvFirstDownDone);
+        if (q == nitems - 1) DL_STAMP(kEvLastDownDone);
       }
     }
     ok = consumers_all(ok && !s_abort);
