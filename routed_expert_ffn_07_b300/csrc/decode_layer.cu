@@ -26,9 +26,9 @@
 //             words (launch epoch << 32 | two fp16), one strong store each;
 //   phase 4   down.  CTA c owns output rows [d c / #CTA, d (c + 1) / #CTA).  For every slot in
 //             order the producer streams the slot's down rows of those outputs (TMA) as soon as a
-//             stage is free; a team copies the slot's h rows into the stage, re-reading words whose
-//             tag is not yet this launch's, and multiplies them (N = all T tokens; a token that
-//             does not use the slot contributes zeros) into fp32 accumulators kept in registers
+//             stage is free; a team (one warp, with <= 16 items) copies the slot's h rows into the
+//             stage, re-reading words whose tag is not yet this launch's, and multiplies them (N =
+//             all T tokens; other tokens contribute zeros) into fp32 register accumulators kept
 //             across the slots.  The 16 warps' partial sums are added in warp order and the
 //             residual is added: y is written once, each element by one CTA.
 //
